@@ -1,0 +1,48 @@
+"""The oracle reproduces its stored tiny fixtures, and the pure-Python brute
+force agrees with them independently (forward quantities)."""
+import json
+import os
+
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+
+HERE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+with open(os.path.join(HERE, "tiny_oracle.json")) as fh:
+    FIX = json.load(fh)["cases"]
+
+
+def _t(x):
+    return None if x is None else torch.tensor(x, dtype=torch.float64)
+
+
+@pytest.mark.parametrize("c", FIX, ids=[c["name"] for c in FIX])
+def test_oracle_reproduces_fixture(c):
+    h, w, b = _t(c["hidden"]), _t(c["weight"]), _t(c["bias"])
+    t = torch.tensor(c["targets"], dtype=torch.int64)
+    args = (h, w, t, b, -100, c["logit_scale"], c["softcap"], c["reduction"])
+    f = oracle.forward(*args)
+    g = oracle.backward(*args, 1.0)
+    assert torch.allclose(f["loss"], _t(c["loss_rows"]), rtol=1e-12, atol=1e-15)
+    assert torch.allclose(f["lse"], _t(c["lse"]), rtol=1e-12)
+    assert f["argmax"].tolist() == c["argmax"]
+    assert f["loss_out"] == pytest.approx(c["loss_out"], rel=1e-12)
+    for k in ("grad_hidden", "grad_weight", "grad_bias"):
+        if c[k] is not None:
+            assert torch.allclose(g[k], _t(c[k]), rtol=1e-11, atol=1e-16)
+
+
+@pytest.mark.parametrize("c", FIX, ids=[c["name"] for c in FIX])
+def test_brute_force_agrees_with_fixture(c):
+    rows = brute.per_row(c["hidden"], c["weight"], c["targets"], c["bias"], -100,
+                         c["logit_scale"], c["softcap"])
+    for r, l, e, a in zip(rows, c["loss_rows"], c["entropy"], c["argmax"]):
+        assert r["loss"] == pytest.approx(l, rel=1e-12, abs=1e-15)
+        assert r["entropy"] == pytest.approx(e, rel=1e-12)
+        assert r["argmax"] == a
+    acc, ent = brute.metrics(c["hidden"], c["weight"], c["targets"], c["bias"], -100,
+                             c["logit_scale"], c["softcap"])
+    assert acc == pytest.approx(c["mean_token_accuracy"])
+    assert ent == pytest.approx(c["entropy_mean"], rel=1e-12)
