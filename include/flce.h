@@ -1,0 +1,182 @@
+/*
+ * flce.h -- C ABI of libflce.so: fused linear cross-entropy on one GB300
+ * (sm_103a) GPU.
+ *
+ * The operation ("fused-linear-ce" model card, trl-lib: §Full signature,
+ * §Metrics for free, §Algorithm):
+ *
+ *   lin_ij  = hidden_i . weight_j + bias_j                 (i < N, j < V)
+ *   u_ij    = logit_scale * lin_ij
+ *   z_ij    = softcap * tanh(u_ij / softcap)   if softcap > 0, else u_ij
+ *   lse_i   = log sum_j exp(z_ij),   p_ij = exp(z_ij - lse_i)
+ *   loss_i  = lse_i - z_{i,t_i}      (0 when t_i == ignore_index)
+ *   loss    = sum_i loss_i / n_valid ("mean") | sum_i loss_i ("sum") | loss_i ("none")
+ *   mean_token_accuracy = #{valid i : argmax_j z_ij == t_i} / n_valid
+ *   entropy             = sum_{valid i} (lse_i - sum_j p_ij z_ij) / n_valid   (nats)
+ *
+ * and its backward (§Algorithm: "forms p - onehot"):
+ *
+ *   D_ij          = g_i (p_ij - [j == t_i]) * logit_scale * (1 - tanh^2(u_ij/softcap))
+ *   grad_hidden   = D @ weight,  grad_weight = D^T @ hidden,  grad_bias = sum_i D_ij
+ *
+ * with g_i = grad_out/n_valid ("mean"), grad_out ("sum") or grad_out[i]
+ * ("none"), and g_i = 0 on ignored rows. n_valid counts rows whose target is
+ * not ignore_index. The N x V logit matrix is never stored: the forward keeps
+ * per-(row, vocabulary tile) softmax statistics, the backward recomputes the
+ * logits one vocabulary chunk at a time.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument except `p` is a DEVICE pointer on the current
+ *     CUDA device; `p` is a host pointer read during the call only.
+ *   - The caller owns all memory, including the workspace. The library never
+ *     allocates or frees device memory and never synchronises the stream:
+ *     every kernel is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and the call returns before the work completes.
+ *   - Tensors are dense row-major: hidden [N,H], weight [V,H], bias [V],
+ *     targets int64 [N]. hidden, weight and bias share `p->dtype`.
+ *   - FLCE_BF16 needs H % 8 == 0 and 16-byte aligned hidden/weight pointers
+ *     (tensor-memory-accelerator row pitch rule); FLCE_F32 needs 4-byte
+ *     alignment. Violations return FLCE_ERR_UNSUPPORTED before any launch.
+ *   - Argument errors are detected on the host, before any launch, and
+ *     return a non-OK status; flce_last_error() then describes the problem.
+ *     A failed launch returns FLCE_ERR_CUDA.
+ *   - Errors that only the device can see are ORed into `*err_word` (when it
+ *     is non-NULL) asynchronously: FLCE_DEVERR_TARGET_RANGE for a target
+ *     outside [0,V) that is not ignore_index (that row's loss is NaN and it
+ *     gets no gradient), FLCE_DEVERR_TIMEOUT when a kernel's bounded wait
+ *     expired (results are then invalid). The caller zeroes the word and
+ *     reads it after its own synchronisation.
+ *   - No C++ exception crosses this interface. Entry points are thread-safe;
+ *     calls that share a workspace must be ordered on one stream.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum flce_status {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,   /* bad shape, option, or NULL required pointer */
+  FLCE_ERR_UNSUPPORTED = 2,   /* valid but not supported (alignment, GPU arch) */
+  FLCE_ERR_WORKSPACE = 3,     /* workspace smaller than *_workspace_size() or misaligned */
+  FLCE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  FLCE_ERR_DEVICE_TIMEOUT = 5 /* reserved for callers that translate FLCE_DEVERR_TIMEOUT */
+} flce_status;
+
+typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1 } flce_dtype;
+
+typedef enum flce_reduction {
+  FLCE_RED_NONE = 0,
+  FLCE_RED_SUM = 1,
+  FLCE_RED_MEAN = 2
+} flce_reduction;
+
+/* Bits of the device error word. */
+#define FLCE_DEVERR_TARGET_RANGE 1
+#define FLCE_DEVERR_TIMEOUT 2
+
+/* Problem description (host struct, copied during the call).
+ *   n, h, v            tokens, hidden size, vocabulary size (n >= 0, h >= 1, v >= 1)
+ *   dtype              flce_dtype of hidden, weight and bias
+ *   has_bias           0 or 1
+ *   ignore_index       target value that marks an ignored row (default -100)
+ *   logit_scale        multiplies the linear logits (finite)
+ *   softcap            > 0 enables z = softcap*tanh(u/softcap); <= 0 disables
+ *   reduction          flce_reduction
+ *   grad_weight_dtype  dtype of grad_weight: FLCE_F32, or equal to dtype
+ *   vocab_chunk        backward vocabulary chunk width; 0 picks the default
+ *                      (the chunk's N x chunk dlogits buffer is the largest
+ *                      workspace item); rounded up to a multiple of 256
+ */
+typedef struct flce_problem {
+  int64_t n, h, v;
+  int32_t dtype;
+  int32_t has_bias;
+  int64_t ignore_index;
+  float logit_scale;
+  float softcap;
+  int32_t reduction;
+  int32_t grad_weight_dtype;
+  int64_t vocab_chunk;
+} flce_problem;
+
+/* Bytes of device workspace flce_forward() needs for `p` (0 if `p` is
+ * invalid). Cite: §Algorithm ("tiles over the vocabulary ... merges the tile
+ * into a running log-sum-exp"): the workspace holds the per-(row, vocabulary
+ * tile) statistics the merge combines, about N * ceil(V/256) * 16 bytes. */
+size_t flce_forward_workspace_size(const flce_problem* p);
+
+/* Forward pass. Cite: §Algorithm (forward), §Metrics for free.
+ *   hidden [N,H], weight [V,H], bias [V] (NULL unless p->has_bias), targets [N]
+ *   loss_rows    [N] fp32 out: per-row loss (0 on ignored rows)       required
+ *   lse_rows     [N] fp32 out: per-row log-sum-exp, kept for backward required
+ *   correct_rows [N] int32 out: 1 where argmax == target (valid rows) nullable
+ *   entropy_rows [N] fp32 out: per-row softmax entropy in nats       nullable
+ *   loss_out     scalar fp32 out: the reduced loss; required for "sum" and
+ *                "mean", ignored (may be NULL) for "none"
+ *   metrics_out  [2] fp32 out: {mean_token_accuracy, entropy}; NULL skips
+ *                them. Loss outputs are bit-identical either way.
+ *   n_valid      scalar int32 out: rows whose target != ignore_index  required
+ *   err_word     scalar int32, ORed with FLCE_DEVERR_* bits           nullable
+ *   workspace    >= flce_forward_workspace_size(p) bytes, 256-byte aligned
+ * With n_valid = 0, "mean" gives NaN loss and NaN metrics. */
+flce_status flce_forward(const flce_problem* p, const void* hidden,
+                         const void* weight, const void* bias,
+                         const int64_t* targets, float* loss_rows,
+                         float* lse_rows, int32_t* correct_rows,
+                         float* entropy_rows, float* loss_out,
+                         float* metrics_out, int32_t* n_valid,
+                         int32_t* err_word, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace flce_backward() needs for `p` (0 if invalid):
+ * the dlogits buffer of one vocabulary chunk (N x chunk, in bf16 for FLCE_BF16
+ * and fp32 for FLCE_F32), an fp32 [N,H] grad_hidden accumulator when there is
+ * more than one chunk and dtype is bf16, and fp32 grad_bias partial sums when
+ * has_bias. */
+size_t flce_backward_workspace_size(const flce_problem* p);
+
+/* Backward pass: all three gradients. Cite: §Algorithm (backward: recompute
+ * each logit tile, form p - onehot, grad_hidden = (p - onehot) @ weight,
+ * grad_weight = (p - onehot)^T @ hidden); §Full signature ("hidden, weight
+ * and bias all receive gradients").
+ *   hidden, weight, bias, targets   as for flce_forward (same values)
+ *   lse_rows    [N] fp32 in: from flce_forward on the same inputs   required
+ *   n_valid     scalar int32 in: from flce_forward                   required
+ *   grad_out    fp32 in: scalar d(objective)/d(loss) for "sum"/"mean",
+ *               [N] per-row upstream gradients for "none"            required
+ *   grad_hidden [N,H] out, dtype p->dtype                            required
+ *   grad_weight [V,H] out, dtype p->grad_weight_dtype                required
+ *   grad_bias   [V] out, dtype p->dtype; required iff p->has_bias
+ *   err_word    as for flce_forward                                  nullable
+ *   workspace   >= flce_backward_workspace_size(p) bytes, 256-byte aligned
+ * Outputs are overwritten, not accumulated into. */
+flce_status flce_backward(const flce_problem* p, const void* hidden,
+                          const void* weight, const void* bias,
+                          const int64_t* targets, const float* lse_rows,
+                          const int32_t* n_valid, const float* grad_out,
+                          void* grad_hidden, void* grad_weight,
+                          void* grad_bias, int32_t* err_word, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Static text for a status code. */
+const char* flce_status_string(flce_status s);
+
+/* Description of the last non-OK status returned on the calling thread
+ * (empty string if none). Valid until the next call on that thread. */
+const char* flce_last_error(void);
+
+/* 1 if the current CUDA device can run this library's kernels (compute
+ * capability 10.3, i.e. sm_103a), else 0. */
+int flce_device_supported(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

@@ -1,0 +1,176 @@
+"""ctypes binding of libflce.so (include/flce.h), one Python function per C
+entry point, same names. Argument marshalling only: pointers are passed as
+integers (``tensor.data_ptr()``), the stream as ``cudaStream_t`` integer.
+
+The library must have been built (``linear_cross_entropy_vocab_gb300.build``
+or ``__graft_entry__.build()``); loading fails loudly otherwise. There is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import native_build as _build
+
+FLCE_OK = 0
+FLCE_ERR_INVALID_ARG = 1
+FLCE_ERR_UNSUPPORTED = 2
+FLCE_ERR_WORKSPACE = 3
+FLCE_ERR_CUDA = 4
+FLCE_ERR_DEVICE_TIMEOUT = 5
+
+FLCE_F32 = 0
+FLCE_BF16 = 1
+
+FLCE_RED_NONE = 0
+FLCE_RED_SUM = 1
+FLCE_RED_MEAN = 2
+
+FLCE_DEVERR_TARGET_RANGE = 1
+FLCE_DEVERR_TIMEOUT = 2
+
+REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
+
+# Every symbol include/flce.h declares.
+EXPORTS = (
+    "flce_forward_workspace_size",
+    "flce_forward",
+    "flce_backward_workspace_size",
+    "flce_backward",
+    "flce_status_string",
+    "flce_last_error",
+    "flce_device_supported",
+)
+
+
+class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
+    _fields_ = [
+        ("n", ctypes.c_int64),
+        ("h", ctypes.c_int64),
+        ("v", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("has_bias", ctypes.c_int32),
+        ("ignore_index", ctypes.c_int64),
+        ("logit_scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+        ("reduction", ctypes.c_int32),
+        ("grad_weight_dtype", ctypes.c_int32),
+        ("vocab_chunk", ctypes.c_int64),
+    ]
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(what)
+
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_PROB = ctypes.POINTER(flce_problem)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libflce.so (built in-tree). Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -m linear_cross_entropy_vocab_gb300.native_build)")
+        lib = ctypes.CDLL(path)
+        lib.flce_forward_workspace_size.argtypes = [_PROB]
+        lib.flce_forward_workspace_size.restype = ctypes.c_size_t
+        lib.flce_backward_workspace_size.argtypes = [_PROB]
+        lib.flce_backward_workspace_size.restype = ctypes.c_size_t
+        lib.flce_forward.argtypes = [_PROB] + [_P] * 15
+        lib.flce_forward.argtypes[-2] = ctypes.c_size_t
+        lib.flce_forward.restype = ctypes.c_int
+        lib.flce_backward.argtypes = [_PROB] + [_P] * 14
+        lib.flce_backward.argtypes[-2] = ctypes.c_size_t
+        lib.flce_backward.restype = ctypes.c_int
+        lib.flce_status_string.argtypes = [ctypes.c_int]
+        lib.flce_status_string.restype = ctypes.c_char_p
+        lib.flce_last_error.argtypes = []
+        lib.flce_last_error.restype = ctypes.c_char_p
+        lib.flce_device_supported.argtypes = []
+        lib.flce_device_supported.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, call: str):
+    if status != FLCE_OK:
+        lib = load()
+        name = lib.flce_status_string(status).decode()
+        detail = lib.flce_last_error().decode()
+        raise FlceError(status, f"{call}: {name}: {detail}")
+
+
+def make_problem(n, h, v, dtype, has_bias, ignore_index=-100, logit_scale=1.0,
+                 softcap=None, reduction="mean", grad_weight_dtype=None,
+                 vocab_chunk=0) -> flce_problem:
+    p = flce_problem()
+    p.n, p.h, p.v = int(n), int(h), int(v)
+    p.dtype = int(dtype)
+    p.has_bias = 1 if has_bias else 0
+    p.ignore_index = int(ignore_index)
+    p.logit_scale = float(logit_scale)
+    p.softcap = float(softcap) if softcap is not None else 0.0
+    p.reduction = REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
+    p.grad_weight_dtype = int(dtype if grad_weight_dtype is None else grad_weight_dtype)
+    p.vocab_chunk = int(vocab_chunk)
+    return p
+
+
+def flce_forward_workspace_size(p: flce_problem) -> int:
+    return load().flce_forward_workspace_size(ctypes.byref(p))
+
+
+def flce_backward_workspace_size(p: flce_problem) -> int:
+    return load().flce_backward_workspace_size(ctypes.byref(p))
+
+
+def flce_forward(p, hidden, weight, bias, targets, loss_rows, lse_rows, correct_rows,
+                 entropy_rows, loss_out, metrics_out, n_valid, err_word, workspace,
+                 workspace_bytes, stream, check=True) -> int:
+    st = load().flce_forward(ctypes.byref(p), hidden, weight, bias, targets, loss_rows,
+                             lse_rows, correct_rows, entropy_rows, loss_out, metrics_out,
+                             n_valid, err_word, workspace, workspace_bytes, stream)
+    if check:
+        _check(st, "flce_forward")
+    return st
+
+
+def flce_backward(p, hidden, weight, bias, targets, lse_rows, n_valid, grad_out,
+                  grad_hidden, grad_weight, grad_bias, err_word, workspace,
+                  workspace_bytes, stream, check=True) -> int:
+    st = load().flce_backward(ctypes.byref(p), hidden, weight, bias, targets, lse_rows,
+                              n_valid, grad_out, grad_hidden, grad_weight, grad_bias,
+                              err_word, workspace, workspace_bytes, stream)
+    if check:
+        _check(st, "flce_backward")
+    return st
+
+
+def flce_status_string(status: int) -> str:
+    return load().flce_status_string(int(status)).decode()
+
+
+def flce_last_error() -> str:
+    return load().flce_last_error().decode()
+
+
+def flce_device_supported() -> bool:
+    return bool(load().flce_device_supported())

@@ -1,0 +1,181 @@
+"""Tensor-level API over the C ABI.
+
+``fused_linear_cross_entropy`` has the signature of the "fused-linear-ce"
+model card (trl-lib), §Full signature:
+
+    fused_linear_cross_entropy(hidden (N,H), weight (V,H), targets (N,) int64,
+        bias=None, ignore_index=-100, logit_scale=1.0, softcap=None,
+        reduction="mean", return_metrics=False)
+      -> loss | (loss, {"mean_token_accuracy": ..., "entropy": ...})
+
+hidden, weight and bias receive gradients; the metrics are forward-only
+(§Metrics for free). PyTorch supplies device memory and the current stream;
+every step of the computation runs in libflce.so's kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import abi
+
+__all__ = ["fused_linear_cross_entropy", "flce_forward_tensors", "flce_backward_tensors"]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return abi.FLCE_F32
+    if t.dtype == torch.bfloat16:
+        return abi.FLCE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check_inputs(hidden, weight, targets, bias):
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden must be (N, H) and weight (V, H)")
+    if targets.dim() != 1 or targets.shape[0] != hidden.shape[0]:
+        raise ValueError("targets must be (N,)")
+    if targets.dtype != torch.int64:
+        raise TypeError("targets must be int64")
+    if weight.dtype != hidden.dtype or (bias is not None and bias.dtype != hidden.dtype):
+        raise TypeError("hidden, weight and bias must share one dtype")
+    if bias is not None and (bias.dim() != 1 or bias.shape[0] != weight.shape[0]):
+        raise ValueError("bias must be (V,)")
+    for name, t in (("hidden", hidden), ("weight", weight), ("targets", targets), ("bias", bias)):
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != hidden.device:
+            raise ValueError(f"{name} is on {t.device}, hidden on {hidden.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
+                         logit_scale=1.0, softcap=None, reduction="mean",
+                         return_metrics=False, row_metrics=False, err_word=None,
+                         vocab_chunk=0) -> dict:
+    """Run flce_forward; returns a dict of freshly allocated output tensors:
+    loss (0-d, or [N] for 'none'), loss_rows, lse_rows, n_valid (0-d int32),
+    metrics ([2] or None), correct_rows / entropy_rows (when row_metrics)."""
+    _check_inputs(hidden, weight, targets, bias)
+    n, h = hidden.shape
+    v = weight.shape[0]
+    dev = hidden.device
+    prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
+                            logit_scale, softcap, reduction, vocab_chunk=vocab_chunk)
+    f32 = dict(dtype=torch.float32, device=dev)
+    loss_rows = torch.empty(n, **f32)
+    lse_rows = torch.empty(n, **f32)
+    n_valid = torch.empty((), dtype=torch.int32, device=dev)
+    loss_out = None if reduction == "none" else torch.empty((), **f32)
+    metrics = torch.empty(2, **f32) if return_metrics else None
+    correct_rows = torch.empty(n, dtype=torch.int32, device=dev) if row_metrics else None
+    entropy_rows = torch.empty(n, **f32) if row_metrics else None
+    with torch.cuda.device(dev):
+        ws_bytes = abi.flce_forward_workspace_size(prob)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        abi.flce_forward(prob, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
+                         _ptr(loss_rows), _ptr(lse_rows), _ptr(correct_rows),
+                         _ptr(entropy_rows), _ptr(loss_out), _ptr(metrics), _ptr(n_valid),
+                         _ptr(err_word), _ptr(ws), ws_bytes, stream)
+    return {
+        "loss": loss_rows if reduction == "none" else loss_out,
+        "loss_rows": loss_rows,
+        "lse_rows": lse_rows,
+        "n_valid": n_valid,
+        "metrics": metrics,
+        "correct_rows": correct_rows,
+        "entropy_rows": entropy_rows,
+    }
+
+
+def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, bias=None,
+                          ignore_index=-100, logit_scale=1.0, softcap=None,
+                          reduction="mean", grad_weight_dtype=None, err_word=None,
+                          vocab_chunk=0):
+    """Run flce_backward; returns (grad_hidden, grad_weight, grad_bias).
+    ``grad_out`` is a 0-d fp32 tensor ('sum'/'mean') or [N] ('none').
+    ``grad_weight_dtype`` torch.float32 keeps grad_weight in fp32."""
+    _check_inputs(hidden, weight, targets, bias)
+    n, h = hidden.shape
+    v = weight.shape[0]
+    dev = hidden.device
+    gw_dtype = hidden.dtype if grad_weight_dtype is None else grad_weight_dtype
+    gw_code = abi.FLCE_F32 if gw_dtype == torch.float32 else _dtype_code(hidden)
+    prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
+                            logit_scale, softcap, reduction, grad_weight_dtype=gw_code,
+                            vocab_chunk=vocab_chunk)
+    grad_out = grad_out.to(device=dev, dtype=torch.float32).contiguous()
+    grad_hidden = torch.empty_like(hidden)
+    grad_weight = torch.empty(v, h, dtype=gw_dtype, device=dev)
+    grad_bias = torch.empty_like(bias) if bias is not None else None
+    with torch.cuda.device(dev):
+        ws_bytes = abi.flce_backward_workspace_size(prob)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        abi.flce_backward(prob, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
+                          _ptr(lse_rows), _ptr(n_valid), _ptr(grad_out), _ptr(grad_hidden),
+                          _ptr(grad_weight), _ptr(grad_bias), _ptr(err_word), _ptr(ws),
+                          ws_bytes, stream)
+    return grad_hidden, grad_weight, grad_bias
+
+
+class _FusedLinearCrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, hidden, weight, bias, targets, ignore_index, logit_scale, softcap,
+                reduction, return_metrics):
+        out = flce_forward_tensors(hidden, weight, targets, bias, ignore_index, logit_scale,
+                                   softcap, reduction, return_metrics)
+        ctx.save_for_backward(hidden, weight, bias, targets, out["lse_rows"], out["n_valid"])
+        ctx.opts = (ignore_index, logit_scale, softcap, reduction)
+        metrics = out["metrics"]
+        if metrics is None:
+            metrics = torch.empty(0, dtype=torch.float32, device=hidden.device)
+        ctx.mark_non_differentiable(metrics)
+        return out["loss"], metrics
+
+    @staticmethod
+    def backward(ctx, grad_loss, _grad_metrics):
+        hidden, weight, bias, targets, lse_rows, n_valid = ctx.saved_tensors
+        ignore_index, logit_scale, softcap, reduction = ctx.opts
+        gh, gw, gb = flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid,
+                                           grad_loss, bias, ignore_index, logit_scale,
+                                           softcap, reduction)
+        need = ctx.needs_input_grad
+        return (gh if need[0] else None, gw if need[1] else None,
+                gb if (bias is not None and need[2]) else None,
+                None, None, None, None, None, None)
+
+
+def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
+                               targets: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                               ignore_index: int = -100, logit_scale: float = 1.0,
+                               softcap: Optional[float] = None, reduction: str = "mean",
+                               return_metrics: bool = False):
+    """Cross-entropy of softcap(logit_scale * (hidden @ weight.T + bias))
+    against targets, without materialising the (N, V) logits.
+
+    Returns the loss (0-d for 'mean'/'sum', (N,) for 'none'), or with
+    return_metrics ``(loss, {"mean_token_accuracy": 0-d, "entropy": 0-d})``;
+    metrics are over non-ignored positions, entropy in nats.
+    """
+    if reduction not in abi.REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(abi.REDUCTIONS)}")
+    hidden = hidden.contiguous()
+    weight = weight.contiguous()
+    targets = targets.contiguous()
+    bias = None if bias is None else bias.contiguous()
+    loss, metrics = _FusedLinearCrossEntropy.apply(hidden, weight, bias, targets,
+                                                   int(ignore_index), float(logit_scale),
+                                                   softcap, reduction, bool(return_metrics))
+    if not return_metrics:
+        return loss
+    return loss, {"mean_token_accuracy": metrics[0], "entropy": metrics[1]}

@@ -1,0 +1,563 @@
+// C ABI of libflce.so (declared in include/flce.h): argument checks,
+// workspace planning, tensor-map encoding and the launch sequence of the
+// forward and backward passes. No device memory is allocated here and no
+// call synchronises the caller's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "flce.h"
+#include "flce_internal.h"
+
+namespace {
+
+using flce::GemmGeom;
+
+thread_local char g_err[512] = {0};
+
+flce_status fail(flce_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+flce_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FLCE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ----------------------------------------------------------- device facts
+struct DeviceInfo {
+  int known = 0;
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.known) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return false;
+    d.known = 1;
+  }
+  *out = d;
+  return true;
+}
+
+// ---------------------------------------------------- tensor-map encoding
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeFn g_encode = nullptr;
+
+EncodeFn encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box
+// {box_inner, box_outer}, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+              int64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2u};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- planning
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kDefaultDlogitsBudget = int64_t(512) << 20;  // bytes of one dlogits chunk
+
+struct FwdPlan {
+  int64_t n_vt = 0;
+  size_t partials = 0, zt = 0, correct = 0, entropy = 0, total = 0;
+};
+
+struct BwdPlan {
+  int64_t chunk = 0, n_chunks = 0, gb_parts = 0;
+  size_t d = 0, acc = 0, gb = 0, total = 0;
+  bool use_acc = false;
+};
+
+bool is_bf16(const flce_problem* p) { return p->dtype == FLCE_BF16; }
+
+flce_status check_problem(const flce_problem* p) {
+  if (p == nullptr) return fail(FLCE_ERR_INVALID_ARG, "problem pointer is NULL");
+  if (p->n < 0 || p->h < 1 || p->v < 1)
+    return fail(FLCE_ERR_INVALID_ARG, "need n >= 0, h >= 1, v >= 1 (got n=%lld h=%lld v=%lld)",
+                (long long)p->n, (long long)p->h, (long long)p->v);
+  const int64_t lim = int64_t(1) << 30;
+  if (p->n >= lim || p->h >= lim || p->v >= lim)
+    return fail(FLCE_ERR_UNSUPPORTED, "n, h and v must each be below 2^30");
+  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16)
+    return fail(FLCE_ERR_INVALID_ARG, "dtype must be FLCE_F32 or FLCE_BF16");
+  if (p->has_bias != 0 && p->has_bias != 1)
+    return fail(FLCE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+  if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_MEAN)
+    return fail(FLCE_ERR_INVALID_ARG, "reduction must be none, sum or mean");
+  if (p->grad_weight_dtype != FLCE_F32 && p->grad_weight_dtype != p->dtype)
+    return fail(FLCE_ERR_INVALID_ARG, "grad_weight_dtype must be FLCE_F32 or the input dtype");
+  if (!std::isfinite(p->logit_scale))
+    return fail(FLCE_ERR_INVALID_ARG, "logit_scale must be finite");
+  if (std::isnan(p->softcap) || std::isinf(p->softcap))
+    return fail(FLCE_ERR_INVALID_ARG, "softcap must be finite (<= 0 disables it)");
+  if (p->vocab_chunk < 0) return fail(FLCE_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
+  if (is_bf16(p) && p->h % 8 != 0)
+    return fail(FLCE_ERR_UNSUPPORTED, "bf16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld",
+                (long long)p->h);
+  if (is_bf16(p)) {
+    const int64_t m_tiles = cdiv(p->n, flce::kBM), n_tiles = cdiv(p->v, flce::kBN);
+    if (m_tiles * n_tiles >= (int64_t(1) << 31))
+      return fail(FLCE_ERR_UNSUPPORTED, "too many tiles");
+  }
+  return FLCE_OK;
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+FwdPlan plan_forward(const flce_problem* p) {
+  FwdPlan f;
+  f.n_vt = cdiv(p->v, is_bf16(p) ? flce::kBN : flce::kSimtTileV);
+  size_t off = 0;
+  f.partials = off;
+  off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 16);
+  f.zt = off;
+  off = align_up(off + static_cast<size_t>(p->n) * 4);
+  f.correct = off;
+  off = align_up(off + static_cast<size_t>(p->n) * 4);
+  f.entropy = off;
+  off = align_up(off + static_cast<size_t>(p->n) * 4);
+  f.total = off;
+  return f;
+}
+
+BwdPlan plan_backward(const flce_problem* p) {
+  BwdPlan b;
+  const int64_t elem = is_bf16(p) ? 2 : 4;
+  const int64_t v_round = cdiv(p->v, 256) * 256;
+  int64_t c = p->vocab_chunk;
+  if (c > 0) {
+    c = cdiv(c, 256) * 256;
+  } else {
+    const int64_t rows = p->n > 0 ? p->n : 1;
+    c = (kDefaultDlogitsBudget / (rows * elem)) / 256 * 256;
+    if (c < 256) c = 256;
+  }
+  if (c > v_round) c = v_round;
+  b.chunk = c;
+  b.n_chunks = cdiv(p->v, c);
+  b.use_acc = is_bf16(p) && b.n_chunks > 1;
+  b.gb_parts = p->has_bias ? cdiv(p->n, is_bf16(p) ? flce::kBM : flce::kSimtTileN) : 0;
+  size_t off = 0;
+  b.d = off;
+  off = align_up(off + static_cast<size_t>(p->n) * c * elem);
+  b.acc = off;
+  if (b.use_acc) off = align_up(off + static_cast<size_t>(p->n) * p->h * 4);
+  b.gb = off;
+  if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
+  b.total = off;
+  return b;
+}
+
+flce::LogitXform make_xform(const flce_problem* p) {
+  flce::LogitXform xf;
+  xf.scale = p->logit_scale;
+  xf.has_cap = p->softcap > 0.0f ? 1 : 0;
+  xf.softcap = xf.has_cap ? p->softcap : 1.0f;
+  xf.inv_softcap = 1.0f / xf.softcap;
+  return xf;
+}
+
+flce_status check_device(DeviceInfo* dev) {
+  if (!device_info(dev)) return fail(FLCE_ERR_CUDA, "cannot query the current CUDA device");
+  if (!(dev->major == 10 && dev->minor == 3))
+    return fail(FLCE_ERR_UNSUPPORTED,
+                "libflce.so is built for sm_103a (GB300); current device is sm_%d%d", dev->major,
+                dev->minor);
+  return FLCE_OK;
+}
+
+flce_status check_workspace(void* ws, size_t have, size_t need) {
+  if (have < need)
+    return fail(FLCE_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", have,
+                need);
+  if (need > 0 && (ws == nullptr || !aligned(ws, kAlign)))
+    return fail(FLCE_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  return FLCE_OK;
+}
+
+int grid_for(int64_t tiles, int sms) {
+  return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_DEVICE_TIMEOUT: return "FLCE_ERR_DEVICE_TIMEOUT";
+  }
+  return "FLCE_ERR_UNKNOWN";
+}
+
+const char* flce_last_error(void) { return g_err; }
+
+int flce_device_supported(void) {
+  DeviceInfo d;
+  if (!device_info(&d)) return 0;
+  return (d.major == 10 && d.minor == 3) ? 1 : 0;
+}
+
+size_t flce_forward_workspace_size(const flce_problem* p) {
+  if (check_problem(p) != FLCE_OK) return 0;
+  return plan_forward(p).total;
+}
+
+size_t flce_backward_workspace_size(const flce_problem* p) {
+  if (check_problem(p) != FLCE_OK) return 0;
+  return plan_backward(p).total;
+}
+
+flce_status flce_forward(const flce_problem* p, const void* hidden, const void* weight,
+                         const void* bias, const int64_t* targets, float* loss_rows,
+                         float* lse_rows, int32_t* correct_rows, float* entropy_rows,
+                         float* loss_out, float* metrics_out, int32_t* n_valid, int32_t* err_word,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  flce_status st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  const bool bf16 = is_bf16(p);
+  const size_t in_align = bf16 ? 16 : 4;
+  if (weight == nullptr) return fail(FLCE_ERR_INVALID_ARG, "weight is NULL");
+  if (n_valid == nullptr) return fail(FLCE_ERR_INVALID_ARG, "n_valid is NULL");
+  if (p->reduction != FLCE_RED_NONE && loss_out == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "loss_out is NULL (required for sum and mean)");
+  if (p->has_bias && bias == nullptr) return fail(FLCE_ERR_INVALID_ARG, "has_bias but bias is NULL");
+  if (!p->has_bias && bias != nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "bias given but has_bias is 0");
+  if (p->n > 0) {
+    if (hidden == nullptr || targets == nullptr || loss_rows == nullptr || lse_rows == nullptr)
+      return fail(FLCE_ERR_INVALID_ARG, "hidden, targets, loss_rows and lse_rows are required");
+    if (!aligned(hidden, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "hidden is misaligned");
+    if (!aligned(targets, 8)) return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
+  }
+  if (!aligned(weight, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "weight is misaligned");
+  if (bias != nullptr && !aligned(bias, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
+  const FwdPlan plan = plan_forward(p);
+  st = check_workspace(workspace, workspace_bytes, plan.total);
+  if (st != FLCE_OK) return st;
+  DeviceInfo dev;
+  st = check_device(&dev);
+  if (st != FLCE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float4* partials = reinterpret_cast<float4*>(ws + plan.partials);
+  float* zt = reinterpret_cast<float*>(ws + plan.zt);
+  int32_t* correct_ws = reinterpret_cast<int32_t*>(ws + plan.correct);
+  float* entropy_ws = reinterpret_cast<float*>(ws + plan.entropy);
+  const flce::LogitXform xf = make_xform(p);
+  cudaError_t e;
+
+  if (p->n > 0) {
+    if (bf16) {
+      CUtensorMap tm_h, tm_w;
+      if (!make_map(&tm_h, hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+          !make_map(&tm_w, weight, p->h, p->v, p->h, flce::kBK, flce::kBN))
+        return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+      GemmGeom g{};
+      g.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
+      g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+      g.m_fastest = 1;
+      g.err_word = err_word;
+      flce::FwdStatsParams fp{};
+      fp.bias = static_cast<const __nv_bfloat16*>(bias);
+      fp.targets = targets;
+      fp.partials = partials;
+      fp.zt = zt;
+      fp.n_rows = p->n;
+      fp.v = p->v;
+      fp.n_vt = plan.n_vt;
+      fp.xf = xf;
+      e = flce::launch_tc_fwd_stats(tm_h, tm_w, g, fp,
+                                    grid_for(int64_t(g.m_tiles) * g.n_tiles, dev.sms), s);
+      if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
+    } else {
+      flce::SimtFwdParams fp{};
+      fp.hidden = static_cast<const float*>(hidden);
+      fp.weight = static_cast<const float*>(weight);
+      fp.bias = static_cast<const float*>(bias);
+      fp.targets = targets;
+      fp.partials = partials;
+      fp.zt = zt;
+      fp.n = p->n;
+      fp.h = p->h;
+      fp.v = p->v;
+      fp.n_vt = plan.n_vt;
+      fp.xf = xf;
+      e = flce::launch_simt_fwd(fp, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 forward kernel");
+    }
+    flce::MergeParams mp{};
+    mp.partials = partials;
+    mp.zt = zt;
+    mp.targets = targets;
+    mp.n = p->n;
+    mp.v = p->v;
+    mp.n_vt = plan.n_vt;
+    mp.ignore_index = p->ignore_index;
+    mp.loss_rows = loss_rows;
+    mp.lse_rows = lse_rows;
+    mp.correct_ws = correct_ws;
+    mp.entropy_ws = entropy_ws;
+    mp.correct_rows = correct_rows;
+    mp.entropy_rows = entropy_rows;
+    mp.err_word = err_word;
+    e = flce::launch_merge_rows(mp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "row merge kernel");
+  }
+  flce::FinalizeParams fin{};
+  fin.loss_rows = loss_rows;
+  fin.correct_ws = correct_ws;
+  fin.entropy_ws = entropy_ws;
+  fin.targets = targets;
+  fin.n = p->n;
+  fin.ignore_index = p->ignore_index;
+  fin.reduction = p->reduction;
+  fin.loss_out = p->reduction == FLCE_RED_NONE ? nullptr : loss_out;
+  fin.metrics_out = metrics_out;
+  fin.n_valid = n_valid;
+  e = flce::launch_finalize(fin, s);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize kernel");
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const flce_problem* p, const void* hidden, const void* weight,
+                          const void* bias, const int64_t* targets, const float* lse_rows,
+                          const int32_t* n_valid, const float* grad_out, void* grad_hidden,
+                          void* grad_weight, void* grad_bias, int32_t* err_word, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  flce_status st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  const bool bf16 = is_bf16(p);
+  const size_t in_align = bf16 ? 16 : 4;
+  if (weight == nullptr || grad_weight == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "weight and grad_weight are required");
+  if (p->has_bias && (bias == nullptr || grad_bias == nullptr))
+    return fail(FLCE_ERR_INVALID_ARG, "has_bias needs bias and grad_bias");
+  if (!p->has_bias && (bias != nullptr || grad_bias != nullptr))
+    return fail(FLCE_ERR_INVALID_ARG, "bias/grad_bias given but has_bias is 0");
+  if (p->n > 0) {
+    if (hidden == nullptr || targets == nullptr || lse_rows == nullptr || n_valid == nullptr ||
+        grad_out == nullptr || grad_hidden == nullptr)
+      return fail(FLCE_ERR_INVALID_ARG,
+                  "hidden, targets, lse_rows, n_valid, grad_out and grad_hidden are required");
+    if (!aligned(hidden, in_align) || !aligned(grad_hidden, in_align))
+      return fail(FLCE_ERR_UNSUPPORTED, "hidden or grad_hidden is misaligned");
+    if (!aligned(targets, 8)) return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
+  }
+  if (!aligned(weight, in_align) || !aligned(grad_weight, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "weight or grad_weight is misaligned");
+  if (bias != nullptr && !aligned(bias, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
+  const BwdPlan plan = plan_backward(p);
+  st = check_workspace(workspace, workspace_bytes, plan.total);
+  if (st != FLCE_OK) return st;
+  DeviceInfo dev;
+  st = check_device(&dev);
+  if (st != FLCE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t gw_elem = p->grad_weight_dtype == FLCE_F32 ? 4 : 2;
+  cudaError_t e;
+  if (p->n == 0) {
+    e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(p->v) * p->h * gw_elem, s);
+    if (e == cudaSuccess && grad_bias != nullptr)
+      e = cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(p->v) * (bf16 ? 2 : 4), s);
+    return e == cudaSuccess ? FLCE_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const flce::LogitXform xf = make_xform(p);
+  float* gb_partial = p->has_bias ? reinterpret_cast<float*>(ws + plan.gb) : nullptr;
+
+  if (bf16) {
+    __nv_bfloat16* dbuf = reinterpret_cast<__nv_bfloat16*>(ws + plan.d);
+    float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
+    CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
+    if (!make_map(&tm_h_k, hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+        !make_map(&tm_w_k, weight, p->h, p->v, p->h, flce::kBK, flce::kBN) ||
+        !make_map(&tm_h_mn, hidden, p->h, p->n, p->h, 64, flce::kBK) ||
+        !make_map(&tm_w_mn, weight, p->h, p->v, p->h, 64, flce::kBK))
+      return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
+    for (int64_t c = 0; c < plan.n_chunks; ++c) {
+      const int64_t c0 = c * plan.chunk;
+      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
+      CUtensorMap tm_d_k, tm_d_mn;
+      if (!make_map(&tm_d_k, dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
+          !make_map(&tm_d_mn, dbuf, width, p->n, plan.chunk, 64, flce::kBK))
+        return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed (dlogits)");
+
+      // 1. recompute the chunk's logits and form D
+      GemmGeom g1{};
+      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
+      g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+      g1.m_fastest = 1;
+      g1.b_mn0 = static_cast<int>(c0);
+      g1.err_word = err_word;
+      flce::DlogitsParams dp{};
+      dp.bias = static_cast<const __nv_bfloat16*>(bias);
+      dp.targets = targets;
+      dp.lse = lse_rows;
+      dp.grad_out = grad_out;
+      dp.n_valid = n_valid;
+      dp.d = dbuf;
+      dp.ldd = plan.chunk;
+      dp.gb_partial = gb_partial;
+      dp.gb_ld = p->v;
+      dp.n_rows = p->n;
+      dp.v = p->v;
+      dp.ignore_index = p->ignore_index;
+      dp.c0 = static_cast<int>(c0);
+      dp.width = static_cast<int>(width);
+      dp.reduction = p->reduction;
+      dp.xf = xf;
+      e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp,
+                                  grid_for(int64_t(g1.m_tiles) * g1.n_tiles, dev.sms), s);
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
+
+      // 2. grad_weight[c0 : c0+width] = D^T @ hidden
+      GemmGeom g2{};
+      g2.m_tiles = static_cast<int>(cdiv(width, flce::kBM));
+      g2.n_tiles = h_tiles;
+      g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
+      g2.m_fastest = 0;
+      g2.err_word = err_word;
+      flce::StoreRowsParams sp{};
+      sp.out = grad_weight;
+      sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
+      sp.ld = p->h;
+      sp.rows = width;
+      sp.row0 = c0;
+      sp.cols = static_cast<int>(p->h);
+      e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp,
+                                      grid_for(int64_t(g2.m_tiles) * g2.n_tiles, dev.sms), s);
+      if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
+
+      // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
+      GemmGeom g3{};
+      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g3.n_tiles = h_tiles;
+      g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
+      g3.m_fastest = 1;
+      g3.b_k0 = static_cast<int>(c0);
+      g3.err_word = err_word;
+      flce::AccRowsParams ap{};
+      ap.acc = acc;
+      ap.out = static_cast<__nv_bfloat16*>(grad_hidden);
+      if (plan.n_chunks == 1)
+        ap.mode = flce::kAccStoreOut;
+      else if (c == 0)
+        ap.mode = flce::kAccStore;
+      else if (c == plan.n_chunks - 1)
+        ap.mode = flce::kAccAddOut;
+      else
+        ap.mode = flce::kAccAdd;
+      ap.ld = p->h;
+      ap.rows = p->n;
+      ap.cols = static_cast<int>(p->h);
+      e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap,
+                                      grid_for(int64_t(g3.m_tiles) * g3.n_tiles, dev.sms), s);
+      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
+    }
+  } else {
+    float* dbuf = reinterpret_cast<float*>(ws + plan.d);
+    for (int64_t c = 0; c < plan.n_chunks; ++c) {
+      const int64_t c0 = c * plan.chunk;
+      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
+      flce::SimtDlogitsParams dp{};
+      dp.hidden = static_cast<const float*>(hidden);
+      dp.weight = static_cast<const float*>(weight);
+      dp.bias = static_cast<const float*>(bias);
+      dp.targets = targets;
+      dp.lse = lse_rows;
+      dp.grad_out = grad_out;
+      dp.n_valid = n_valid;
+      dp.d = dbuf;
+      dp.ldd = plan.chunk;
+      dp.gb_partial = gb_partial;
+      dp.gb_ld = p->v;
+      dp.n = p->n;
+      dp.h = p->h;
+      dp.v = p->v;
+      dp.ignore_index = p->ignore_index;
+      dp.c0 = c0;
+      dp.width = width;
+      dp.reduction = p->reduction;
+      dp.xf = xf;
+      e = flce::launch_simt_dlogits(dp, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 dlogits kernel");
+      // grad_weight rows [c0, c0+width) = D^T @ hidden
+      e = flce::launch_simt_gemm(width, p->h, p->n, dbuf, 1, plan.chunk,
+                                 static_cast<const float*>(hidden), p->h, 1,
+                                 static_cast<float*>(grad_weight) + c0 * p->h, p->h, 0, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_weight kernel");
+      // grad_hidden (+)= D @ weight[c0 : c0+width]
+      e = flce::launch_simt_gemm(p->n, p->h, width, dbuf, plan.chunk, 1,
+                                 static_cast<const float*>(weight) + c0 * p->h, p->h, 1,
+                                 static_cast<float*>(grad_hidden), p->h, c > 0 ? 1 : 0, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_hidden kernel");
+    }
+  }
+  if (p->has_bias) {
+    e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias, bf16 ? 1 : 0,
+                                 s);
+    if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
+  }
+  return FLCE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// Internal interfaces between the C ABI (flce_api.cu) and the kernels.
+// Host-side only declarations plus the plain-data parameter blocks passed by
+// value to the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "flce_math.cuh"
+#include "tc_gemm.cuh"
+
+namespace flce {
+
+// Width of one vocabulary tile of the forward statistics (tensor-core path);
+// the fp32 path uses kSimtTileV.
+constexpr int kSimtTileV = 128;
+constexpr int kSimtTileN = 32;
+
+struct FwdStatsParams {
+  const __nv_bfloat16* bias;  // [V] or null
+  const int64_t* targets;     // [N]
+  float4* partials;           // [N][n_vt] (m, s, t, argmax)
+  float* zt;                  // [N] target logit
+  int64_t n_rows;
+  int64_t v;
+  int64_t n_vt;
+  LogitXform xf;
+};
+
+struct DlogitsParams {
+  const __nv_bfloat16* bias;
+  const int64_t* targets;
+  const float* lse;
+  const float* grad_out;
+  const int32_t* n_valid;
+  __nv_bfloat16* d;  // [N][ldd] dlogits of this chunk
+  int64_t ldd;
+  float* gb_partial;  // [m_tiles][gb_ld] or null
+  int64_t gb_ld;
+  int64_t n_rows;
+  int64_t v;
+  int64_t ignore_index;
+  int c0;     // first vocabulary column of the chunk
+  int width;  // columns in the chunk
+  int reduction;
+  LogitXform xf;
+};
+
+struct StoreRowsParams {
+  void* out;
+  int out_f32;
+  int64_t ld;
+  int64_t rows;
+  int64_t row0;
+  int cols;
+};
+
+enum AccMode { kAccStore = 0, kAccAdd = 1, kAccAddOut = 2, kAccStoreOut = 3 };
+
+struct AccRowsParams {
+  float* acc;
+  __nv_bfloat16* out;
+  int mode;
+  int64_t ld;
+  int64_t rows;
+  int cols;
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
+                                const GemmGeom& g, const FwdStatsParams& p, int grid,
+                                cudaStream_t s);
+cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
+                              const GemmGeom& g, const DlogitsParams& p, int grid, cudaStream_t s);
+cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
+                                  const GemmGeom& g, const StoreRowsParams& p, int grid,
+                                  cudaStream_t s);
+cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
+                                  const GemmGeom& g, const AccRowsParams& p, int grid,
+                                  cudaStream_t s);
+
+// fp32 (SIMT) path
+struct SimtFwdParams {
+  const float* hidden;
+  const float* weight;
+  const float* bias;
+  const int64_t* targets;
+  float4* partials;
+  float* zt;
+  int64_t n, h, v, n_vt;
+  LogitXform xf;
+};
+cudaError_t launch_simt_fwd(const SimtFwdParams& p, cudaStream_t s);
+
+struct SimtDlogitsParams {
+  const float* hidden;
+  const float* weight;
+  const float* bias;
+  const int64_t* targets;
+  const float* lse;
+  const float* grad_out;
+  const int32_t* n_valid;
+  float* d;  // [N][ldd]
+  int64_t ldd;
+  float* gb_partial;  // [ceil(N/32)][gb_ld] or null
+  int64_t gb_ld;
+  int64_t n, h, v, ignore_index;
+  int64_t c0, width;
+  int reduction;
+  LogitXform xf;
+};
+cudaError_t launch_simt_dlogits(const SimtDlogitsParams& p, cudaStream_t s);
+
+// C[m, n] (+)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn], fp32.
+cudaError_t launch_simt_gemm(int64_t m, int64_t n, int64_t k, const float* a, int64_t sam,
+                             int64_t sak, const float* b, int64_t sbk, int64_t sbn, float* c,
+                             int64_t ldc, int accumulate, cudaStream_t s);
+
+// row kernels
+struct MergeParams {
+  const float4* partials;
+  const float* zt;
+  const int64_t* targets;
+  int64_t n, v, n_vt, ignore_index;
+  float* loss_rows;
+  float* lse_rows;
+  int32_t* correct_ws;     // [N] always written
+  float* entropy_ws;       // [N] always written
+  int32_t* correct_rows;   // user copy or null
+  float* entropy_rows;     // user copy or null
+  int32_t* err_word;
+};
+cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t s);
+
+struct FinalizeParams {
+  const float* loss_rows;
+  const int32_t* correct_ws;
+  const float* entropy_ws;
+  const int64_t* targets;
+  int64_t n, ignore_index;
+  int reduction;
+  float* loss_out;     // null for "none"
+  float* metrics_out;  // null to skip
+  int32_t* n_valid;
+};
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
+
+// out[j] = sum_{r < n_parts} part[r*ld + j] (fixed order), cast to bf16 or f32.
+cudaError_t launch_bias_reduce(const float* part, int64_t n_parts, int64_t ld, int64_t v,
+                               void* out, int out_bf16, cudaStream_t s);
+
+
+}  // namespace flce

@@ -1,0 +1,366 @@
+// bf16 tensor-core kernels of the fused linear cross-entropy (sm_103a).
+//
+// Four instances of the persistent tcgen05 GEMM (tc_gemm.cuh), one per
+// contraction of the method ("fused-linear-ce" model card, §Algorithm):
+//   fwd_stats   logits = hidden @ W^T per 128 x 256 tile, folded on the fly
+//               into per-(row, vocabulary tile) softmax statistics; nothing of
+//               size N x V is written.
+//   bwd_dlogits the same logits recomputed for one vocabulary chunk, turned
+//               into D = g (p - onehot) dz/dlin and stored in bf16.
+//   grad_weight grad_W[chunk] = D^T @ hidden (K = tokens, fp32 in TMEM,
+//               written once).
+//   grad_hidden grad_h += D @ W[chunk] (K = chunk width), accumulated in an
+//               fp32 buffer across chunks; the last chunk writes bf16.
+#include <cfloat>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "flce_internal.h"
+#include "flce_math.cuh"
+#include "tc_gemm.cuh"
+
+namespace flce {
+
+namespace {
+
+// 32 bias values of columns [c, c+32) (fewer when nv < 32; the rest are 0).
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int64_t c, int nv,
+                                            float (&b)[32]) {
+  if (bias == nullptr) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) b[k] = 0.0f;
+    return;
+  }
+  if (nv == 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(bias + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(src + q);
+      const uint32_t parts[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&parts[h]);
+        b[q * 8 + 2 * h] = __low2float(pr);
+        b[q * 8 + 2 * h + 1] = __high2float(pr);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) b[k] = (k < nv) ? __bfloat162float(bias[c + k]) : 0.0f;
+  }
+}
+
+// Fold 32 logits (the first nv valid) of columns [cb, cb+32) into st.
+template <bool FULL>
+__device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], int nv, int cb) {
+  float cm = -FLT_MAX;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    if (FULL || k < nv) cm = fmaxf(cm, z[k]);
+  }
+  if (cm > st.m) {
+    int kf = 0;
+#pragma unroll
+    for (int k = 31; k >= 0; --k) {
+      if ((FULL || k < nv) && z[k] == cm) kf = k;
+    }
+    st.a = cb + kf;
+    st.rebase(cm);
+  }
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    if (FULL || k < nv) st.add(z[k]);
+  }
+}
+
+// Lane l of the warp ends with the sum over the 32 lanes of v[l].
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ forward
+struct EpiFwdStats {
+  using Params = FwdStatsParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              int row_in_tile, int /*quarter*/, int /*lane*/, GemmCtl* /*ctl*/) {
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < p.n_rows;
+    const int64_t t = row_ok ? __ldg(p.targets + row) : INT64_MIN;
+    const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
+    RowStats st;
+    st.init();
+    float zt = 0.0f;
+    bool has_zt = false;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int64_t cb = col0 + ch * 32;
+      if (cb >= p.v) break;
+      const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
+      float z[32], b[32];
+      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_bias32(p.bias, cb, nv, b);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
+      if (nv == 32) {
+        fold_chunk<true>(st, z, nv, static_cast<int>(cb));
+      } else {
+        fold_chunk<false>(st, z, nv, static_cast<int>(cb));
+      }
+      const int64_t tk = t - cb;
+      if (tk >= 0 && tk < nv) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k == tk) zt = z[k];
+        }
+        has_zt = true;
+      }
+    }
+    if (row_ok) {
+      p.partials[row * p.n_vt + n_tile] = st.pack();
+      if (has_zt) p.zt[row] = zt;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ dlogits
+struct EpiDlogits {
+  using Params = DlogitsParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              int row_in_tile, int quarter, int lane, GemmCtl* ctl) {
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < p.n_rows;
+    const int64_t t = row_ok ? __ldg(p.targets + row) : p.ignore_index;
+    const float g = row_ok ? row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row)
+                           : 0.0f;
+    const float gs = g * p.xf.scale;
+    const float lse2 = row_ok ? __ldg(p.lse + row) * kLog2e : 0.0f;
+    const int64_t tl = t - p.c0;  // target column within this chunk
+    const int col0 = n_tile * kBN;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int cb = col0 + ch * 32;
+      if (cb >= p.width) break;
+      const int nv = p.width - cb < 32 ? p.width - cb : 32;
+      float z[32], b[32];
+      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_bias32(p.bias, p.c0 + cb, nv, b);
+      float d[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        z[k] = p.xf(z[k], b[k]);
+        d[k] = ex2_approx(fmaf(z[k], kLog2e, -lse2));
+      }
+      const int64_t tk = tl - cb;
+      if (tk >= 0 && tk < nv) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k == tk) d[k] -= 1.0f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        d[k] = row_ok ? d[k] * gs * p.xf.dz_du(z[k]) : 0.0f;
+      }
+      if (row_ok) {
+        __nv_bfloat16* dst = p.d + row * p.ldd + cb;
+        if (nv == 32) {
+          uint4* dv = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            dv[q] = make_uint4(pack_bf16x2(d[q * 8 + 0], d[q * 8 + 1]),
+                               pack_bf16x2(d[q * 8 + 2], d[q * 8 + 3]),
+                               pack_bf16x2(d[q * 8 + 4], d[q * 8 + 5]),
+                               pack_bf16x2(d[q * 8 + 6], d[q * 8 + 7]));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (k < nv) dst[k] = __float2bfloat16_rn(d[k]);
+          }
+        }
+      }
+      if (p.gb_partial != nullptr) {
+        // column sums of D over this tile's 128 rows, in a fixed order
+        const float colsum = transpose_reduce32(d, lane);
+        ctl->red[quarter][lane] = colsum;
+        named_bar_sync(1, kEpiThreads);
+        if (quarter == 0 && cb + lane < p.width) {
+          const float tot = ((ctl->red[0][lane] + ctl->red[1][lane]) + ctl->red[2][lane]) +
+                            ctl->red[3][lane];
+          p.gb_partial[static_cast<int64_t>(m_tile) * p.gb_ld + p.c0 + cb + lane] = tot;
+        }
+        named_bar_sync(1, kEpiThreads);
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------ grad_weight
+struct EpiStoreRows {
+  using Params = StoreRowsParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              int row_in_tile, int, int, GemmCtl*) {
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < p.rows;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int cb = n_tile * kBN + ch * 32;
+      if (cb >= p.cols) break;
+      float z[32];
+      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      if (!row_ok) continue;
+      const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
+      const int64_t off = (p.row0 + row) * p.ld + cb;
+      if (p.out_f32) {
+        float* dst = static_cast<float*>(p.out) + off;
+        if (nv == 32) {
+          float4* dv = reinterpret_cast<float4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dv[q] = make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) dst[k] = z[k];
+        }
+      } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + off;
+        if (nv == 32) {
+          uint4* dv = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dv[q] = make_uint4(pack_bf16x2(z[q * 8 + 0], z[q * 8 + 1]),
+                               pack_bf16x2(z[q * 8 + 2], z[q * 8 + 3]),
+                               pack_bf16x2(z[q * 8 + 4], z[q * 8 + 5]),
+                               pack_bf16x2(z[q * 8 + 6], z[q * 8 + 7]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) dst[k] = __float2bfloat16_rn(z[k]);
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------ grad_hidden
+struct EpiAccRows {
+  using Params = AccRowsParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              int row_in_tile, int, int, GemmCtl*) {
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < p.rows;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int cb = n_tile * kBN + ch * 32;
+      if (cb >= p.cols) break;
+      float z[32];
+      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      if (!row_ok) continue;
+      const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
+      const int64_t off = row * p.ld + cb;
+      if (p.mode == kAccAdd || p.mode == kAccAddOut) {
+        const float* src = p.acc + off;
+        if (nv == 32) {
+          const float4* sv = reinterpret_cast<const float4*>(src);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = sv[q];
+            z[4 * q] += a.x;
+            z[4 * q + 1] += a.y;
+            z[4 * q + 2] += a.z;
+            z[4 * q + 3] += a.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) z[k] += src[k];
+        }
+      }
+      if (p.mode == kAccStore || p.mode == kAccAdd) {
+        float* dst = p.acc + off;
+        if (nv == 32) {
+          float4* dv = reinterpret_cast<float4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dv[q] = make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) dst[k] = z[k];
+        }
+      } else {
+        __nv_bfloat16* dst = p.out + off;
+        if (nv == 32) {
+          uint4* dv = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dv[q] = make_uint4(pack_bf16x2(z[q * 8 + 0], z[q * 8 + 1]),
+                               pack_bf16x2(z[q * 8 + 2], z[q * 8 + 3]),
+                               pack_bf16x2(z[q * 8 + 4], z[q * 8 + 5]),
+                               pack_bf16x2(z[q * 8 + 6], z[q * 8 + 7]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < nv) dst[k] = __float2bfloat16_rn(z[k]);
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ launchers
+namespace {
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmGeom& g,
+                        const typename Epi::Params& ep, int grid, cudaStream_t stream) {
+  auto kern = tc_gemm_kernel<A_MN, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, g, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
+                                const GemmGeom& g, const FwdStatsParams& p, int grid,
+                                cudaStream_t s) {
+  return launch_gemm<false, false, EpiFwdStats>(tm_hidden_k, tm_weight_k, g, p, grid, s);
+}
+
+cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
+                              const GemmGeom& g, const DlogitsParams& p, int grid,
+                              cudaStream_t s) {
+  return launch_gemm<false, false, EpiDlogits>(tm_hidden_k, tm_weight_k, g, p, grid, s);
+}
+
+cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
+                                  const GemmGeom& g, const StoreRowsParams& p, int grid,
+                                  cudaStream_t s) {
+  return launch_gemm<true, true, EpiStoreRows>(tm_d_mn, tm_hidden_mn, g, p, grid, s);
+}
+
+cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
+                                  const GemmGeom& g, const AccRowsParams& p, int grid,
+                                  cudaStream_t s) {
+  return launch_gemm<false, true, EpiAccRows>(tm_d_k, tm_weight_mn, g, p, grid, s);
+}
+
+}  // namespace flce

@@ -1,0 +1,276 @@
+// Persistent, warp-specialised tcgen05 GEMM main loop with pluggable
+// epilogues, for sm_103a.
+//
+//   D[128 x 256 tile] = sum_k A[m, k] * B[n, k]      (bf16 in, fp32 in TMEM)
+//
+// Roles of the 192 threads of a CTA (one CTA per SM, persistent over tiles):
+//   warp 0   one thread issues TMA tile loads into a kStages-deep ring
+//   warp 1   allocates the tensor memory; one thread issues tcgen05.mma
+//   warps 2-5  the epilogue: each thread owns one accumulator row (TMEM
+//            lane), pulls its 256 fp32 columns with tcgen05.ld and hands them
+//            to the epilogue policy.
+// The 512 TMEM columns hold two 128 x 256 fp32 accumulators, so the epilogue
+// of tile i overlaps the MMAs of tile i+1.
+//
+// Each operand is K-major (rows of K contiguous elements) or MN-major (K rows
+// of contiguous M or N elements); both are staged with 128-byte swizzle:
+//   K-major:  one TMA box {64 (K), rows}; 8-row groups 1024 B apart.
+//   MN-major: boxes {64 (M/N), 64 (K)} of 8 KB each, side by side along M/N.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "tc_ptx.cuh"
+
+namespace flce {
+
+constexpr int kBM = 128;  // accumulator rows = TMEM lanes
+constexpr int kBN = 256;  // accumulator columns per buffer
+constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUK = 16;   // K per tcgen05.mma (kind::f16)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kGemmThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 2 * kBN;
+
+struct GemmCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  float red[4][32];  // epilogue scratch: per-warp column sums
+};
+
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /* 1 KB alignment slack */ +
+                               ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
+
+// Tile grid and TMA coordinate offsets of one GEMM launch.
+struct GemmGeom {
+  int m_tiles, n_tiles, k_iters;
+  int m_fastest;  // 1: tile u -> (u % m_tiles, u / m_tiles); 0: n fastest
+  int a_mn0, a_k0;  // A: offset along M and along K (elements / rows)
+  int b_mn0, b_k0;  // B: offset along N and along K
+  int* err_word;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmGeom& g, int u, int& m, int& n) {
+  if (g.m_fastest) {
+    m = u % g.m_tiles;
+    n = u / g.m_tiles;
+  } else {
+    n = u % g.n_tiles;
+    m = u / g.n_tiles;
+  }
+}
+
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int mn0, int k0) {
+  if constexpr (!MN) {
+    tma_load_2d(dst, map, bar, k0, mn0);  // box {64 along K, ROWS}
+  } else {
+#pragma unroll
+    for (int b = 0; b < ROWS / 64; ++b) {
+      tma_load_2d(dst + b * 8192, map, bar, mn0 + b * 64, k0);  // box {64 along M/N, 64 along K}
+    }
+  }
+}
+
+// Descriptor of the kk-th K=16 slice of a staged operand.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+  if constexpr (!MN) {
+    return smem_desc_sw128(base + kk * (kUK * 2), 16, 1024);
+  } else {
+    return smem_desc_sw128(base + kk * (kUK * 128), 8192, 1024);
+  }
+}
+
+// Bounded wait that ignores the abort flag: used to let copies and MMAs in
+// flight finish before the CTA releases its memory.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 1000000000ull) break;
+  }
+}
+
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+
+// Epi must provide:
+//   struct Params;
+//   static __device__ void tile(const Params&, int m_tile, int n_tile,
+//                               uint32_t taddr, int row_in_tile, int quarter,
+//                               int lane, GemmCtl* ctl);
+// `taddr` addresses this warp's 32 TMEM lanes at column 0 of the tile's
+// accumulator; the 128 epilogue threads may use named barrier 1.
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const GemmGeom g, const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = g.m_tiles * g.n_tiles;
+  volatile int* abort_flag = &ctl->abort;
+
+  auto stage_a = [&](int s) { return base + s * kStageBytes; };
+  auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&ctl->acc_full[b]), 1);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiThreads);
+    }
+    mbar_init(smem_addr(&ctl->mma_done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s has been loaded at least once
+      uint32_t last_phase = 0;  // bit s: phase of the last load into stage s
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        int m, n;
+        tile_coords(g, u, m, n);
+        for (int k = 0; k < g.k_iters; ++k) {
+          if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, g.err_word)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_addr(&ctl->full[stage]);
+          mbar_arrive_expect_tx(full, kStageBytes);
+          load_operand<A_MN, kBM>(stage_a(stage), &tm_a, full, g.a_mn0 + m * kBM,
+                                  g.a_k0 + k * kBK);
+          load_operand<B_MN, kBN>(stage_b(stage), &tm_b, full, g.b_mn0 + n * kBN,
+                                  g.b_k0 + k * kBK);
+          armed |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA exits
+        for (int s = 0; s < kStages; ++s) {
+          if (armed & (1u << s)) drain_wait(smem_addr(&ctl->full[s]), (last_phase >> s) & 1u);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, g.err_word)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
+        for (int k = 0; k < g.k_iters; ++k) {
+          if (!mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, g.err_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
+#pragma unroll
+          for (int kk = 0; kk < kBK / kUK; ++kk) {
+            umma_bf16(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc,
+                      (k | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_addr(&ctl->empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_addr(&ctl->acc_full[buf]));
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      umma_commit(smem_addr(&ctl->mma_done));
+      drain_wait(smem_addr(&ctl->mma_done), 0);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+      const bool got =
+          mbar_wait(smem_addr(&ctl->acc_full[buf]), use, abort_flag, g.err_word);
+      if (!epi_all(got)) break;
+      tc_fence_after_sync();
+      int m, n;
+      tile_coords(g, u, m, n);
+      const uint32_t taddr =
+          tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
+      Epi::tile(ep, m, n, taddr, row_in_tile, quarter, lane, ctl);
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&ctl->acc_empty[buf]));
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace flce

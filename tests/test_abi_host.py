@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI, runnable without a GPU: the library builds,
+loads and exports every function include/flce.h declares; the ctypes struct
+matches the C struct; workspace sizing; and argument validation, which
+returns its status before any CUDA call (no kernel is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_vocab_gb300 import abi, native_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    native_build.build()
+    return abi.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared == sorted(abi.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_struct_layout_matches_header():
+    # int64 n,h,v; int32 dtype,has_bias; int64 ignore_index; float scale, softcap;
+    # int32 reduction, grad_weight_dtype; int64 vocab_chunk
+    assert ctypes.sizeof(abi.flce_problem) == 64
+    assert abi.flce_problem.ignore_index.offset == 32
+    assert abi.flce_problem.logit_scale.offset == 40
+    assert abi.flce_problem.vocab_chunk.offset == 56
+
+
+def test_status_strings(lib):
+    assert abi.flce_status_string(abi.FLCE_OK) == "FLCE_OK"
+    assert abi.flce_status_string(abi.FLCE_ERR_WORKSPACE) == "FLCE_ERR_WORKSPACE"
+
+
+def test_workspace_sizes(lib):
+    p = abi.make_problem(8192, 4096, 128256, abi.FLCE_BF16, False)
+    fwd = abi.flce_forward_workspace_size(p)
+    # per-(row, 256-wide vocabulary tile) statistics: 16 bytes each
+    assert fwd >= 8192 * 501 * 16
+    assert fwd < 8192 * 128256 * 2 // 16  # far below the N x V logits
+    bwd = abi.flce_backward_workspace_size(p)
+    assert bwd < 8192 * 128256 * 2  # never N x V in bf16
+    p.vocab_chunk = 1000
+    small = abi.flce_backward_workspace_size(p)
+    assert small >= 8192 * 1024 * 2  # rounded up to a multiple of 256
+    bad = abi.make_problem(8, 12, 100, abi.FLCE_BF16, False)  # h % 8 != 0
+    assert abi.flce_forward_workspace_size(bad) == 0
+
+
+FAKE = 0x10000  # never dereferenced: validation fails before any device access
+
+
+def _fwd(p, **kw):
+    args = dict(hidden=FAKE, weight=FAKE, bias=None, targets=FAKE, loss_rows=FAKE,
+                lse_rows=FAKE, correct_rows=None, entropy_rows=None, loss_out=FAKE,
+                metrics_out=None, n_valid=FAKE, err_word=None, workspace=FAKE,
+                workspace_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return abi.flce_forward(p, check=False, **args)
+
+
+def _bwd(p, **kw):
+    args = dict(hidden=FAKE, weight=FAKE, bias=None, targets=FAKE, lse_rows=FAKE,
+                n_valid=FAKE, grad_out=FAKE, grad_hidden=FAKE, grad_weight=FAKE,
+                grad_bias=None, err_word=None, workspace=FAKE, workspace_bytes=1 << 40,
+                stream=None)
+    args.update(kw)
+    return abi.flce_backward(p, check=False, **args)
+
+
+def test_validation_statuses(lib):
+    ok = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False)
+    assert _fwd(ok, weight=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _fwd(ok, n_valid=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _fwd(ok, loss_out=None) == abi.FLCE_ERR_INVALID_ARG  # mean needs loss_out
+    assert _fwd(ok, bias=FAKE) == abi.FLCE_ERR_INVALID_ARG  # bias without has_bias
+    assert _fwd(ok, hidden=FAKE + 2) == abi.FLCE_ERR_UNSUPPORTED  # misaligned
+    assert _fwd(ok, workspace_bytes=16) == abi.FLCE_ERR_WORKSPACE
+    assert _fwd(ok, workspace=FAKE + 8) == abi.FLCE_ERR_WORKSPACE  # not 256-aligned
+    assert "workspace" in abi.flce_last_error()
+    neg = abi.make_problem(-1, 64, 100, abi.FLCE_BF16, False)
+    assert _fwd(neg) == abi.FLCE_ERR_INVALID_ARG
+    odd = abi.make_problem(64, 60, 100, abi.FLCE_BF16, False)
+    assert _fwd(odd) == abi.FLCE_ERR_UNSUPPORTED
+    red = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False)
+    red.reduction = 7
+    assert _fwd(red) == abi.FLCE_ERR_INVALID_ARG
+    cap = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False, softcap=float("nan"))
+    assert _fwd(cap) == abi.FLCE_ERR_INVALID_ARG
+    gw = abi.make_problem(64, 64, 100, abi.FLCE_F32, False, grad_weight_dtype=abi.FLCE_BF16)
+    assert _fwd(gw) == abi.FLCE_ERR_INVALID_ARG
+    none = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False, reduction="none")
+    assert _fwd(none, loss_out=None, workspace_bytes=8) == abi.FLCE_ERR_WORKSPACE
+    bias = abi.make_problem(64, 64, 100, abi.FLCE_BF16, True)
+    assert _bwd(bias) == abi.FLCE_ERR_INVALID_ARG  # bias and grad_bias missing
+    assert _bwd(ok, grad_out=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _bwd(ok, grad_hidden=FAKE + 4) == abi.FLCE_ERR_UNSUPPORTED
+    assert _bwd(ok, workspace_bytes=0) == abi.FLCE_ERR_WORKSPACE
+    assert lib.flce_forward(None, *([None] * 13), 0, None) == abi.FLCE_ERR_INVALID_ARG

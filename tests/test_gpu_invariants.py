@@ -1,0 +1,98 @@
+"""GPU invariants that hold at any size:
+  * repeated forward and backward passes are bitwise identical;
+  * return_metrics leaves the loss and the gradients bit-identical
+    ("fused-linear-ce" model card, §Metrics for free);
+  * the per-row loss does not depend on the backward's vocabulary chunking,
+    and the gradients differ across chunkings only by fp32 summation order
+    (the KL-divergence PR's partition-invariance note);
+  * with softcap off and logit_scale 1, sum_j grad_bias_j = 0 (each row's
+    p - onehot sums to zero over the vocabulary);
+  * the autograd entry point returns the same gradients as the raw calls.
+"""
+import pytest
+import torch
+
+from _parity import run_gpu, to_dev
+from linear_cross_entropy_vocab_gb300 import fused_linear_cross_entropy
+from linear_cross_entropy_vocab_gb300.workloads import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(dtype="bf16", **kw):
+    base = dict(bias_var=0.02, ignore_frac=0.1, softcap=20.0, logit_scale=0.8)
+    base.update(kw)
+    return Workload("inv", 700, 264, 3333, dtype, **base)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bitwise_repeatable(dtype):
+    w = _w(dtype)
+    xd = to_dev(make_inputs(w))
+    a = run_gpu(xd, w)
+    b = run_gpu(xd, w)
+    for k in ("loss", "loss_rows", "lse_rows", "metrics", "correct_rows", "entropy_rows",
+              "grad_hidden", "grad_weight", "grad_bias"):
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_metrics_leave_loss_and_grads_bit_identical(dtype):
+    w = _w(dtype)
+    x = to_dev(make_inputs(w))
+    res = []
+    for metrics in (False, True):
+        h = x["hidden"].clone().requires_grad_(True)
+        wt = x["weight"].clone().requires_grad_(True)
+        b = x["bias"].clone().requires_grad_(True)
+        out = fused_linear_cross_entropy(h, wt, x["targets"], b, softcap=w.softcap,
+                                         logit_scale=w.logit_scale, return_metrics=metrics)
+        loss = out[0] if metrics else out
+        loss.backward()
+        res.append((loss.detach().clone(), h.grad.clone(), wt.grad.clone(), b.grad.clone()))
+        if metrics:
+            m = out[1]
+            assert set(m) == {"mean_token_accuracy", "entropy"}
+            assert not m["entropy"].requires_grad
+    for u, v in zip(res[0], res[1]):
+        assert torch.equal(u, v)
+
+
+def test_autograd_matches_raw_calls():
+    w = _w("bf16", reduction="sum")
+    x = to_dev(make_inputs(w))
+    raw = run_gpu(x, w, grad_out=1.0)
+    h = x["hidden"].clone().requires_grad_(True)
+    wt = x["weight"].clone().requires_grad_(True)
+    b = x["bias"].clone().requires_grad_(True)
+    loss = fused_linear_cross_entropy(h, wt, x["targets"], b, softcap=w.softcap,
+                                      logit_scale=w.logit_scale, reduction="sum")
+    loss.backward()
+    assert torch.equal(loss.detach().cpu(), raw["loss"])
+    assert torch.equal(h.grad.cpu(), raw["grad_hidden"])
+    assert torch.equal(wt.grad.cpu(), raw["grad_weight"])
+    assert torch.equal(b.grad.cpu(), raw["grad_bias"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_vocab_chunk_invariance(dtype):
+    w = _w(dtype)
+    x = to_dev(make_inputs(w))
+    one = run_gpu(x, w, vocab_chunk=4096)  # a single chunk
+    many = run_gpu(x, w, vocab_chunk=512)  # seven chunks
+    assert torch.equal(one["loss_rows"], many["loss_rows"])
+    # grad_weight and grad_bias rows come from the same tiles in both plans
+    assert torch.equal(one["grad_weight"], many["grad_weight"])
+    assert torch.equal(one["grad_bias"], many["grad_bias"])
+    # grad_hidden sums chunks in fp32: equal up to summation order
+    d = (one["grad_hidden"].double() - many["grad_hidden"].double()).norm()
+    ref = one["grad_hidden"].double().norm()
+    assert float(d / ref) < (1e-2 if dtype == "bf16" else 1e-5)
+
+
+def test_posterior_mass_identity():
+    w = _w("f32", softcap=None, logit_scale=1.0, reduction="sum")
+    x = to_dev(make_inputs(w))
+    out = run_gpu(x, w)
+    gb = out["grad_bias"].double()
+    assert abs(float(gb.sum())) <= 1e-5 * float(gb.abs().sum())

@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element, at sizes the oracle finishes in seconds. The shapes cover
+several tiles with a ragged tail along each of N (tokens), V (vocabulary) and
+H (hidden), multi-chunk backward passes, every option of the kernel card's
+signature, and the degenerate cases.
+
+Tolerances are documented in ``tests/_parity.py``.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+from _parity import TOL, check_backward, check_forward, oracle_args, run_gpu, to_dev
+from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name, n, h, v, dtype="bf16", **kw):
+    return Workload(name, n, h, v, dtype, **kw)
+
+
+CASES = [
+    # the small fp32 workload exactly as specified (N=256, H=128, V=1000)
+    WORKLOADS["tiny_fp32"],
+    # ragged N (300 = 2*128+44), V (1000 = 3*256+232) and H (136 = 2*64+8)
+    _case("tails_bias_cap_sum", 300, 136, 1000, bias_var=0.02, softcap=30.0,
+          logit_scale=0.5, hidden_var=2.0, ignore_frac=0.3, reduction="sum"),
+    _case("v32003_mean", 512, 256, 32003, ignore_frac=0.05),
+    _case("n4097_none", 4097, 512, 4096, ignore_frac=0.1, reduction="none"),
+    _case("h3592_cap", 256, 3592, 2048, softcap=30.0, logit_scale=0.5, hidden_var=2.0,
+          ignore_frac=0.3, reduction="sum"),
+    _case("v152063", 256, 128, 152063, ignore_frac=0.02, return_metrics=True),
+    _case("zipf_bias_mean", 640, 192, 5000, bias_var=0.02, targets="zipf", ignore_frac=0.1),
+    _case("peaked_rows", 384, 256, 3000, peaked_frac=0.01, ignore_frac=0.05),
+    _case("f32_cap_none", 100, 50, 777, dtype="f32", bias_var=0.02, softcap=5.0,
+          logit_scale=1.5, ignore_frac=0.1, reduction="none"),
+    _case("f32_sum_bias", 257, 96, 2100, dtype="f32", bias_var=0.5, reduction="sum"),
+]
+
+
+def _grad_out(w, n):
+    if w.reduction == "none":
+        g = torch.Generator().manual_seed(7)
+        return torch.rand(n, generator=g, dtype=torch.float64) + 0.5
+    return 0.75
+
+
+def _check_case(w, vocab_chunk=0, grad_weight_dtype=None):
+    x = make_inputs(w)
+    go = _grad_out(w, w.n)
+    out = run_gpu(to_dev(x), w, grad_out=go.float() if torch.is_tensor(go) else go,
+                  vocab_chunk=vocab_chunk, grad_weight_dtype=grad_weight_dtype)
+    assert out["err_word"] == 0
+    ref = oracle.forward(*oracle_args(x, w))
+    tol = TOL[w.dtype]
+    check_forward(out, ref, w, tol)
+    gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"])
+    check_backward(out, gref, tol, x["bias"] is not None)
+
+
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+def test_parity(w):
+    _check_case(w)
+
+
+def test_parity_mid_workload():
+    """The bf16 mid workload exactly as specified: N=4096, H=2048, V=32000,
+    bias, Zipf targets, 10% ignored, mean; full tensors compared."""
+    _check_case(WORKLOADS["mid_bf16"])
+
+
+@pytest.mark.parametrize("chunk", [256, 1024, 2304])
+def test_parity_multi_chunk_backward(chunk):
+    """The backward in several vocabulary chunks (the last one ragged), with a
+    bias so grad_bias partials cross chunk boundaries."""
+    w = _case("chunked", 520, 200, 5000, bias_var=0.02, softcap=20.0, ignore_frac=0.1)
+    _check_case(w, vocab_chunk=chunk)
+
+
+def test_parity_grad_weight_fp32():
+    """grad_weight kept in fp32 (accumulated in fp32 tensor memory, stored once)."""
+    w = _case("gw_f32", 384, 256, 3000, ignore_frac=0.05)
+    _check_case(w, grad_weight_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_all_rows_ignored(dtype):
+    """n_valid = 0: 'mean' loss and metrics are NaN, every gradient is 0."""
+    w = _case("all_ignored", 200, 64, 700, dtype=dtype, bias_var=0.02, ignore_frac=1.0)
+    x = make_inputs(w)
+    out = run_gpu(to_dev(x), w)
+    assert int(out["n_valid"]) == 0
+    assert math.isnan(float(out["loss"]))
+    assert math.isnan(float(out["metrics"][0])) and math.isnan(float(out["metrics"][1]))
+    for k in ("grad_hidden", "grad_weight", "grad_bias"):
+        assert torch.count_nonzero(out[k]) == 0, k
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_single_row_and_vocab_of_one(dtype):
+    w = _case("one_row", 1, 64, 333, dtype=dtype, reduction="sum")
+    _check_case(w)
+    w1 = _case("v1", 50, 64, 1, dtype=dtype, reduction="mean", bias_var=0.02)
+    x = make_inputs(w1)
+    out = run_gpu(to_dev(x), w1)
+    assert float(out["loss"]) == 0.0
+    assert torch.all(out["lse_rows"] == out["lse_rows"])  # finite, no NaN
+    for k in ("grad_hidden", "grad_weight", "grad_bias"):
+        assert float(out[k].abs().max()) < 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_batch(dtype):
+    """N = 0: 'sum' gives 0, 'mean' NaN, grad_weight and grad_bias are 0."""
+    for red in ("sum", "mean"):
+        w = _case("empty", 0, 64, 300, dtype=dtype, bias_var=0.02, reduction=red)
+        x = make_inputs(w)
+        out = run_gpu(to_dev(x), w)
+        assert int(out["n_valid"]) == 0
+        if red == "sum":
+            assert float(out["loss"]) == 0.0
+        else:
+            assert math.isnan(float(out["loss"]))
+        assert out["grad_hidden"].shape == (0, 64)
+        assert torch.count_nonzero(out["grad_weight"]) == 0
+        assert torch.count_nonzero(out["grad_bias"]) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_target_out_of_range(dtype):
+    """A target outside [0, V) that is not ignore_index sets the error word,
+    gives that row a NaN loss and no gradient; other rows are unaffected."""
+    w = _case("bad_target", 130, 64, 500, dtype=dtype, reduction="sum")
+    x = make_inputs(w)
+    x["targets"][5] = 500
+    x["targets"][77] = -3
+    out = run_gpu(to_dev(x), w)
+    assert out["err_word"] & 1
+    assert math.isnan(float(out["loss_rows"][5])) and math.isnan(float(out["loss_rows"][77]))
+    assert math.isnan(float(out["loss"]))
+    ref = oracle.forward(*oracle_args(x, w))
+    ok = torch.ones(130, dtype=torch.bool)
+    ok[[5, 77]] = False
+    tol = TOL[dtype]
+    d = (out["loss_rows"].double() - ref["loss"])[ok].abs()
+    assert float(d.max()) <= tol["loss_rel"] * max(1.0, float(ref["loss"][ok].abs().max()))
+    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"])
+    check_backward(out, gref, tol, False)
