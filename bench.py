@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Fused linear cross-entropy forward+backward throughput on GB300.
+
+One step = flce_forward + flce_backward (all three gradients) over one batch of
+the Llama-3 LM-head workload: N=8192 tokens, H=4096, V=128256, bf16, no bias,
+2% ignored targets, reduction mean, metrics on. Inputs are seeded synthetic
+tensors resident in HBM; the 1.05 GB weight exceeds the 129 MB L2, so no L2
+flush is needed between steps.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload, on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, gemm_flops, make_inputs  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s at H4096 V128256 bf16; % of dense-BF16 tensor peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama3_head_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_ROLES = ("fwd_stats", "bwd_dlogits", "bwd_grad_weight", "bwd_grad_hidden")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.path = tempfile.mktemp(prefix="flce_clocks_", suffix=".csv")
+        self.proc = None
+        self.device_id = device_id
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.device_id],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+class Step:
+    """Preallocated buffers and the two C-ABI calls of one fwd+bwd step."""
+
+    def __init__(self, x: dict, w, dev):
+        from linear_cross_entropy_vocab_gb300 import abi
+
+        self.abi = abi
+        self.x = x
+        self.w = w
+        n, h = x["hidden"].shape
+        v = x["weight"].shape[0]
+        self.prob = abi.make_problem(n, h, v, abi.FLCE_BF16 if x["hidden"].dtype == torch.bfloat16
+                                     else abi.FLCE_F32, x["bias"] is not None, w.ignore_index,
+                                     w.logit_scale, w.softcap, w.reduction)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.loss_rows = torch.empty(n, **f32)
+        self.lse_rows = torch.empty(n, **f32)
+        self.loss = torch.empty((), **f32)
+        self.metrics = torch.empty(2, **f32) if w.return_metrics else None
+        self.n_valid = torch.empty((), dtype=torch.int32, device=dev)
+        self.err = torch.zeros((), dtype=torch.int32, device=dev)
+        self.grad_out = torch.ones((), **f32)
+        self.gh = torch.empty_like(x["hidden"])
+        self.gw = torch.empty_like(x["weight"])
+        self.gb = None if x["bias"] is None else torch.empty_like(x["bias"])
+        self.ws_f = abi.flce_forward_workspace_size(self.prob)
+        self.ws_b = abi.flce_backward_workspace_size(self.prob)
+        self.ws = torch.empty(max(self.ws_f, self.ws_b), dtype=torch.uint8, device=dev)
+
+    def __call__(self, stream):
+        a, x, p = self.abi, self.x, lambda t: None if t is None else t.data_ptr()
+        a.flce_forward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]), p(x["targets"]),
+                       p(self.loss_rows), p(self.lse_rows), None, None, p(self.loss),
+                       p(self.metrics), p(self.n_valid), p(self.err), p(self.ws), self.ws_f,
+                       stream)
+        a.flce_backward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]),
+                        p(x["targets"]), p(self.lse_rows), p(self.n_valid), p(self.grad_out),
+                        p(self.gh), p(self.gw), p(self.gb), p(self.err), p(self.ws), self.ws_b,
+                        stream)
+
+
+def bench_ours(args, rank, world, dev):
+    from linear_cross_entropy_vocab_gb300 import abi, api, native_build
+
+    native_build.build()
+    w = WORKLOADS[args.workload]
+    xc = make_inputs(w)
+    x = {k: (None if t is None else t.to(dev)) for k, t in xc.items()}
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    step = Step(x, w, dev)
+    n, h, v = w.n, w.h, w.v
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step(sh)
+    torch.cuda.synchronize(dev)
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(step.err.item())}")
+
+    # ------------------------------------------------------ device-timed region
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        smi_id = str(torch.cuda.current_device())
+    clocks = ClockSampler(smi_id)
+    clocks.start()
+    abi.flce_profile_enable(True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(sh)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = t0.elapsed_time(t1)
+    prof, dropped = abi.flce_profile_collect()
+    abi.flce_profile_enable(False)
+    clk = clocks.stop()
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # ------------------------------------------------------ end to end (host buffers)
+    pin = {k: (None if t is None else t.pin_memory()) for k, t in xc.items()}
+    loss_h = torch.empty((), dtype=torch.float32).pin_memory()
+    met_h = torch.empty(2, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+    h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+    d2h = loss_h.numel() * 4 + met_h.numel() * 4
+
+    def e2e_step():
+        for k, t in pin.items():
+            if t is not None:
+                x[k].copy_(t, non_blocking=True)
+        step(sh)
+        loss_h.copy_(step.loss, non_blocking=True)
+        met_h.copy_(step.metrics, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ------------------------------------------------------ peak memory of the public API
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    hh = x["hidden"].detach().requires_grad_(True)
+    ww = x["weight"].detach().requires_grad_(True)
+    loss, _m = api.fused_linear_cross_entropy(hh, ww, x["targets"], return_metrics=True)
+    loss.backward()
+    torch.cuda.synchronize(dev)
+    peak_incr = torch.cuda.max_memory_allocated(dev) - base
+    del hh, ww, loss, _m
+
+    peaks, peak_src = load_peaks()
+    flops_step = gemm_flops(n, h, v)
+    sec = ms / 1e3
+    tok_s = world * n * args.steps / sec
+    n_valid = int(step.n_valid.item())
+    achieved_step = flops_step * args.steps / sec / 1e12
+    # dominant kernel: the role with the largest share of device time
+    roles = {k: val for k, val in prof.items()}
+    dom = max(roles, key=lambda k: roles[k][1]) if roles else None
+    roofline = None
+    if dom is not None:
+        launches, tot_ms = roles[dom]
+        per_step_flops = 2.0 * n * h * v if dom in GEMM_ROLES else 0.0
+        launches_per_step = launches / args.steps
+        flops_per_launch = per_step_flops / launches_per_step
+        avg_ms = tot_ms / launches
+        achieved = flops_per_launch / (avg_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_kind": f"bf16 sustained, {peak_src}",
+                    "flops_per_launch": flops_per_launch, "avg_launch_ms": round(avg_ms, 4),
+                    "traffic": None}
+    kernels = {k: {"launches": val[0], "ms_per_step": round(val[1] / args.steps, 4),
+                   "share": round(val[1] / sum(u[1] for u in roles.values()), 4)}
+               for k, val in roles.items()}
+    out = {
+        "metric": METRIC,
+        "value": round(tok_s, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; hidden~N(0,1), weight~N(0,1/H), 2% ignored, uniform targets)",
+        "config": {"workload": f"{w.name}: N={n} H={h} V={v} bf16, no bias, 2% ignore_index, "
+                               "mean, return_metrics",
+                   "global_batch": n * world, "seq_len": None,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (weight 1.05 GB), no flush"},
+        "tensor_peak_frac": {
+            "achieved_tflops": round(achieved_step, 1),
+            "of_burst": round(achieved_step / peaks["bf16_tflops"], 4),
+            "of_sustained": round(achieved_step / peaks["bf16_tflops_sustained"], 4),
+            "of_burst_valid_rows": round(achieved_step * n_valid / n / peaks["bf16_tflops"], 4),
+            "flops_per_step": flops_step, "peaks": peak_src},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": int(sum(val[0] for val in roles.values())),
+        "profile_dropped": dropped,
+        "e2e": {"value": round(world * n * e2e_steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clk,
+        "memory": {"peak_incremental_bytes_public_api": int(peak_incr),
+                   "nxv_bf16_bytes": n * v * 2,
+                   "workspace_fwd_bytes": step.ws_f, "workspace_bwd_bytes": step.ws_b},
+    }
+    return out
+
+
+# ----------------------------------------------------------------- oracle timing
+def _oracle_sample_step(xc, w, rows):
+    import oracle
+
+    sl = {k: (None if t is None else (t[:rows] if k in ("hidden", "targets") else t))
+          for k, t in xc.items()}
+    args = (sl["hidden"], sl["weight"], sl["targets"], sl["bias"], w.ignore_index,
+            w.logit_scale, w.softcap, w.reduction)
+    f = oracle.forward(*args)
+    oracle.backward(*args, 1.0, lse=f["lse"])
+
+
+def _calibrate_rows(xc, w, budget_s, max_rows):
+    """Rows per sample so that one oracle step takes at most about budget_s
+    (linear in the rows of a 64-row trial, fixed costs included)."""
+    t = time.perf_counter()
+    _oracle_sample_step(xc, w, 64)
+    per_row = (time.perf_counter() - t) / 64
+    rows = int(budget_s / per_row)
+    return max(8, min(max_rows, rows)), per_row
+
+
+def cpu_baseline(xc, w, budget_s=15.0):
+    rows, _ = _calibrate_rows(xc, w, budget_s, w.n)
+    t = time.perf_counter()
+    _oracle_sample_step(xc, w, rows)
+    dt = time.perf_counter() - t
+    return {"value": round(rows / dt, 2), "unit": UNIT, "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 forward+backward of the first {rows} rows of the workload "
+                      f"(full H={w.h}, V={w.v}) as one batch; {dt:.1f} s"}
+
+
+def bench_reference(args):
+    w = WORKLOADS[args.workload]
+    xc = make_inputs(w)
+    total_budget = 150.0  # seconds for warmup + timed steps
+    per_step = total_budget / (args.steps + max(args.warmup, 3))
+    rows, _ = _calibrate_rows(xc, w, per_step, w.n)
+    for _ in range(max(args.warmup, 3)):
+        _oracle_sample_step(xc, w, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample_step(xc, w, rows)
+    dt = time.perf_counter() - t
+    val = round(rows * args.steps / dt, 2)
+    sample = (f"each step: fp64 forward+backward of the first {rows} rows of the workload "
+              f"(full H={w.h}, V={w.v})")
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={w.n} H={w.h} V={w.v}", "global_batch": rows},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": torch.get_num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args)), flush=True)
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    out = bench_ours(args, rank, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(make_inputs(WORKLOADS[args.workload]),
+                                           WORKLOADS[args.workload])
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -164,6 +164,33 @@ flce_status flce_backward(const flce_problem* p, const void* hidden,
                           void* grad_bias, int32_t* err_word, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Per-kernel timing, for measurement tools (not part of the method; the
+ * pages describe no profiler). While enabled, every kernel launch made by
+ * flce_forward / flce_backward on the calling process is bracketed by two
+ * CUDA events recorded on the caller's stream, so the launch sequence and
+ * its stream ordering are unchanged. Up to FLCE_PROFILE_MAX_RECORDS launches
+ * are recorded; later ones are counted in `dropped`. The events are created
+ * on the current device the first time profiling is enabled.
+ */
+#define FLCE_PROFILE_MAX_RECORDS 8192
+#define FLCE_PROFILE_NAME_LEN 40
+
+typedef struct flce_kernel_time {
+  char name[FLCE_PROFILE_NAME_LEN]; /* kernel role, e.g. "fwd_stats" */
+  int32_t launches;                 /* launches recorded since the last collect */
+  double total_ms;                  /* summed event-to-event time of those launches */
+} flce_kernel_time;
+
+/* Turn recording on (1) or off (0). Enabling clears earlier records. */
+flce_status flce_profile_enable(int enable);
+
+/* Synchronise on the recorded events, write up to `max_entries` per-kernel
+ * totals (one entry per kernel role, in first-launch order) and clear the
+ * record. Returns the number of entries written, or -1 on a CUDA error.
+ * `*dropped` (nullable) receives the launches not recorded. */
+int flce_profile_collect(flce_kernel_time* out, int max_entries, int32_t* dropped);
+
 /* Static text for a status code. */
 const char* flce_status_string(flce_status s);
 

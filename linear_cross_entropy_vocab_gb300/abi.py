@@ -42,7 +42,12 @@ EXPORTS = (
     "flce_status_string",
     "flce_last_error",
     "flce_device_supported",
+    "flce_profile_enable",
+    "flce_profile_collect",
 )
+
+FLCE_PROFILE_MAX_RECORDS = 8192
+FLCE_PROFILE_NAME_LEN = 40
 
 
 class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
@@ -58,6 +63,14 @@ class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
         ("reduction", ctypes.c_int32),
         ("grad_weight_dtype", ctypes.c_int32),
         ("vocab_chunk", ctypes.c_int64),
+    ]
+
+
+class flce_kernel_time(ctypes.Structure):  # noqa: N801  (C name)
+    _fields_ = [
+        ("name", ctypes.c_char * FLCE_PROFILE_NAME_LEN),
+        ("launches", ctypes.c_int32),
+        ("total_ms", ctypes.c_double),
     ]
 
 
@@ -106,6 +119,11 @@ def load() -> ctypes.CDLL:
         lib.flce_last_error.restype = ctypes.c_char_p
         lib.flce_device_supported.argtypes = []
         lib.flce_device_supported.restype = ctypes.c_int
+        lib.flce_profile_enable.argtypes = [ctypes.c_int]
+        lib.flce_profile_enable.restype = ctypes.c_int
+        lib.flce_profile_collect.argtypes = [ctypes.POINTER(flce_kernel_time), ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int32)]
+        lib.flce_profile_collect.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -174,3 +192,18 @@ def flce_last_error() -> str:
 
 def flce_device_supported() -> bool:
     return bool(load().flce_device_supported())
+
+
+def flce_profile_enable(enable: bool) -> None:
+    _check(load().flce_profile_enable(1 if enable else 0), "flce_profile_enable")
+
+
+def flce_profile_collect(max_entries: int = 16):
+    """Returns ({kernel role: (launches, total_ms)}, dropped launches)."""
+    arr = (flce_kernel_time * max_entries)()
+    dropped = ctypes.c_int32(0)
+    n = load().flce_profile_collect(arr, max_entries, ctypes.byref(dropped))
+    if n < 0:
+        raise FlceError(FLCE_ERR_CUDA, "flce_profile_collect: CUDA error")
+    return ({arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n)},
+            dropped.value)

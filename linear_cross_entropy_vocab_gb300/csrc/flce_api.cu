@@ -42,9 +42,13 @@ struct DeviceInfo {
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 
+// Also makes the current device's primary context current on the calling
+// thread (a thread that never made a runtime call, such as an autograd worker,
+// may have none, and the tensor-map encoder needs one).
 bool device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cudaSetDevice(dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
   if (!d.known) {
@@ -80,18 +84,80 @@ EncodeFn encoder() {
 
 // 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box
 // {box_inner, box_outer}, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
-              int64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+// On failure records the driver's result in the thread's error text.
+bool make_map(CUtensorMap* map, const char* what, const void* base, int64_t inner,
+              int64_t outer, int64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
   EncodeFn enc = encoder();
-  if (!enc) return false;
+  if (!enc) {
+    fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return false;
+  }
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2u};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fail(FLCE_ERR_CUDA,
+         "cuTensorMapEncodeTiled(%s) failed with CUresult %d (base %p, dims %lld x %lld, "
+         "pitch %lld, box %u x %u)",
+         what, static_cast<int>(r), base, (long long)inner, (long long)outer,
+         (long long)pitch_elems, box_inner, box_outer);
+    return false;
+  }
+  return true;
 }
+
+// ------------------------------------------------------------ profiler
+// Optional CUDA-event brackets around each launch (flce_profile_*).
+struct ProfRecord {
+  int role;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+bool g_prof_ready = false;
+ProfRecord g_prof[FLCE_PROFILE_MAX_RECORDS];
+int g_prof_n = 0;
+int32_t g_prof_dropped = 0;
+const char* g_role_names[16];
+int g_n_roles = 0;
+
+int role_id(const char* name) {
+  for (int i = 0; i < g_n_roles; ++i)
+    if (std::strcmp(g_role_names[i], name) == 0) return i;
+  if (g_n_roles < 16) {
+    g_role_names[g_n_roles] = name;
+    return g_n_roles++;
+  }
+  return 15;
+}
+
+// Brackets one kernel launch with events on `s` while profiling is enabled.
+class ProfScope {
+ public:
+  ProfScope(const char* role, cudaStream_t s) : s_(s) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    if (g_prof_n >= FLCE_PROFILE_MAX_RECORDS) {
+      ++g_prof_dropped;
+      return;
+    }
+    rec_ = &g_prof[g_prof_n++];
+    rec_->role = role_id(role);
+    cudaEventRecord(rec_->start, s_);
+  }
+  ~ProfScope() {
+    if (rec_ != nullptr) cudaEventRecord(rec_->stop, s_);
+  }
+
+ private:
+  cudaStream_t s_;
+  ProfRecord* rec_ = nullptr;
+};
 
 // ------------------------------------------------------------- planning
 constexpr size_t kAlign = 256;
@@ -240,6 +306,54 @@ const char* flce_status_string(flce_status s) {
 
 const char* flce_last_error(void) { return g_err; }
 
+flce_status flce_profile_enable(int enable) {
+  g_err[0] = 0;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (enable && !g_prof_ready) {
+    for (int i = 0; i < FLCE_PROFILE_MAX_RECORDS; ++i) {
+      if (cudaEventCreate(&g_prof[i].start) != cudaSuccess ||
+          cudaEventCreate(&g_prof[i].stop) != cudaSuccess)
+        return fail(FLCE_ERR_CUDA, "cudaEventCreate failed");
+    }
+    g_prof_ready = true;
+  }
+  g_prof_on = enable != 0;
+  g_prof_n = 0;
+  g_prof_dropped = 0;
+  return FLCE_OK;
+}
+
+int flce_profile_collect(flce_kernel_time* out, int max_entries, int32_t* dropped) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double total[16] = {0};
+  int count[16] = {0};
+  int order[16];
+  int n_used = 0;
+  for (int r = 0; r < g_prof_n; ++r) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(g_prof[r].stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof[r].start, g_prof[r].stop) != cudaSuccess)
+      return -1;
+    const int role = g_prof[r].role;
+    if (count[role] == 0) order[n_used++] = role;
+    ++count[role];
+    total[role] += ms;
+  }
+  int written = 0;
+  for (int k = 0; k < n_used && written < max_entries; ++k) {
+    const int role = order[k];
+    std::memset(out[written].name, 0, FLCE_PROFILE_NAME_LEN);
+    std::strncpy(out[written].name, g_role_names[role], FLCE_PROFILE_NAME_LEN - 1);
+    out[written].launches = count[role];
+    out[written].total_ms = total[role];
+    ++written;
+  }
+  if (dropped) *dropped = g_prof_dropped;
+  g_prof_n = 0;
+  g_prof_dropped = 0;
+  return written;
+}
+
 int flce_device_supported(void) {
   DeviceInfo d;
   if (!device_info(&d)) return 0;
@@ -301,9 +415,9 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
   if (p->n > 0) {
     if (bf16) {
       CUtensorMap tm_h, tm_w;
-      if (!make_map(&tm_h, hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
-          !make_map(&tm_w, weight, p->h, p->v, p->h, flce::kBK, flce::kBN))
-        return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+      if (!make_map(&tm_h, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+          !make_map(&tm_w, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBN))
+        return FLCE_ERR_CUDA;
       GemmGeom g{};
       g.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
       g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
@@ -319,6 +433,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.v = p->v;
       fp.n_vt = plan.n_vt;
       fp.xf = xf;
+      ProfScope ps("fwd_stats", s);
       e = flce::launch_tc_fwd_stats(tm_h, tm_w, g, fp,
                                     grid_for(int64_t(g.m_tiles) * g.n_tiles, dev.sms), s);
       if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
@@ -335,6 +450,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.v = p->v;
       fp.n_vt = plan.n_vt;
       fp.xf = xf;
+      ProfScope ps("fwd_stats_f32", s);
       e = flce::launch_simt_fwd(fp, s);
       if (e != cudaSuccess) return cuda_fail(e, "fp32 forward kernel");
     }
@@ -353,7 +469,10 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
     mp.correct_rows = correct_rows;
     mp.entropy_rows = entropy_rows;
     mp.err_word = err_word;
-    e = flce::launch_merge_rows(mp, s);
+    {
+      ProfScope ps("merge_rows", s);
+      e = flce::launch_merge_rows(mp, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "row merge kernel");
   }
   flce::FinalizeParams fin{};
@@ -367,7 +486,10 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
   fin.loss_out = p->reduction == FLCE_RED_NONE ? nullptr : loss_out;
   fin.metrics_out = metrics_out;
   fin.n_valid = n_valid;
-  e = flce::launch_finalize(fin, s);
+  {
+    ProfScope ps("finalize", s);
+    e = flce::launch_finalize(fin, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "finalize kernel");
   return FLCE_OK;
 }
@@ -426,19 +548,19 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
     __nv_bfloat16* dbuf = reinterpret_cast<__nv_bfloat16*>(ws + plan.d);
     float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
     CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
-    if (!make_map(&tm_h_k, hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
-        !make_map(&tm_w_k, weight, p->h, p->v, p->h, flce::kBK, flce::kBN) ||
-        !make_map(&tm_h_mn, hidden, p->h, p->n, p->h, 64, flce::kBK) ||
-        !make_map(&tm_w_mn, weight, p->h, p->v, p->h, 64, flce::kBK))
-      return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    if (!make_map(&tm_h_k, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+        !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBN) ||
+        !make_map(&tm_h_mn, "hidden^T", hidden, p->h, p->n, p->h, 64, flce::kBK) ||
+        !make_map(&tm_w_mn, "weight^T", weight, p->h, p->v, p->h, 64, flce::kBK))
+      return FLCE_ERR_CUDA;
     const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
     for (int64_t c = 0; c < plan.n_chunks; ++c) {
       const int64_t c0 = c * plan.chunk;
       const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
       CUtensorMap tm_d_k, tm_d_mn;
-      if (!make_map(&tm_d_k, dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
-          !make_map(&tm_d_mn, dbuf, width, p->n, plan.chunk, 64, flce::kBK))
-        return fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled failed (dlogits)");
+      if (!make_map(&tm_d_k, "dlogits", dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
+          !make_map(&tm_d_mn, "dlogits^T", dbuf, width, p->n, plan.chunk, 64, flce::kBK))
+        return FLCE_ERR_CUDA;
 
       // 1. recompute the chunk's logits and form D
       GemmGeom g1{};
@@ -465,8 +587,11 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.width = static_cast<int>(width);
       dp.reduction = p->reduction;
       dp.xf = xf;
-      e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp,
+      {
+        ProfScope ps("bwd_dlogits", s);
+        e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp,
                                   grid_for(int64_t(g1.m_tiles) * g1.n_tiles, dev.sms), s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
 
       // 2. grad_weight[c0 : c0+width] = D^T @ hidden
@@ -483,8 +608,11 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       sp.rows = width;
       sp.row0 = c0;
       sp.cols = static_cast<int>(p->h);
-      e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp,
+      {
+        ProfScope ps("bwd_grad_weight", s);
+        e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp,
                                       grid_for(int64_t(g2.m_tiles) * g2.n_tiles, dev.sms), s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
 
       // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
@@ -509,8 +637,11 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       ap.ld = p->h;
       ap.rows = p->n;
       ap.cols = static_cast<int>(p->h);
-      e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap,
+      {
+        ProfScope ps("bwd_grad_hidden", s);
+        e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap,
                                       grid_for(int64_t(g3.m_tiles) * g3.n_tiles, dev.sms), s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
     }
   } else {
@@ -538,21 +669,31 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.width = width;
       dp.reduction = p->reduction;
       dp.xf = xf;
-      e = flce::launch_simt_dlogits(dp, s);
+      {
+        ProfScope ps("bwd_dlogits_f32", s);
+        e = flce::launch_simt_dlogits(dp, s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "fp32 dlogits kernel");
       // grad_weight rows [c0, c0+width) = D^T @ hidden
-      e = flce::launch_simt_gemm(width, p->h, p->n, dbuf, 1, plan.chunk,
+      {
+        ProfScope ps("bwd_grad_weight_f32", s);
+        e = flce::launch_simt_gemm(width, p->h, p->n, dbuf, 1, plan.chunk,
                                  static_cast<const float*>(hidden), p->h, 1,
-                                 static_cast<float*>(grad_weight) + c0 * p->h, p->h, 0, s);
+                                   static_cast<float*>(grad_weight) + c0 * p->h, p->h, 0, s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_weight kernel");
       // grad_hidden (+)= D @ weight[c0 : c0+width]
-      e = flce::launch_simt_gemm(p->n, p->h, width, dbuf, plan.chunk, 1,
+      {
+        ProfScope ps("bwd_grad_hidden_f32", s);
+        e = flce::launch_simt_gemm(p->n, p->h, width, dbuf, plan.chunk, 1,
                                  static_cast<const float*>(weight) + c0 * p->h, p->h, 1,
-                                 static_cast<float*>(grad_hidden), p->h, c > 0 ? 1 : 0, s);
+                                   static_cast<float*>(grad_hidden), p->h, c > 0 ? 1 : 0, s);
+      }
       if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_hidden kernel");
     }
   }
   if (p->has_bias) {
+    ProfScope ps("bwd_bias_reduce", s);
     e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias, bf16 ? 1 : 0,
                                  s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");

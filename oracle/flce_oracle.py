@@ -117,6 +117,9 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
     n_valid = int(valid_all.sum())
     target_error = bool((valid_all & ~_in_range(targets, v)).any())
 
+    # widen once; every logit below is formed from these exact fp64 copies
+    weight = weight.to(_F64)
+    bias = None if bias is None else bias.to(_F64)
     idx = torch.arange(n) if rows is None else torch.as_tensor(list(rows), dtype=torch.int64)
     k = idx.numel()
     out = {name: torch.empty(k, dtype=_F64) for name in
@@ -239,10 +242,12 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
     v = weight.shape[0]
     targets = targets.to(torch.int64)
     g_all = row_weights(targets, v, ignore_index, reduction, grad_out)
+    weight = weight.to(_F64)
+    bias = None if bias is None else bias.to(_F64)
     out = {}
     if want_hidden:
         idx = torch.arange(n) if rows is None else torch.as_tensor(list(rows), dtype=torch.int64)
-        w64 = weight.to(_F64)
+        w64 = weight
         gh = torch.empty(idx.numel(), hidden.shape[1], dtype=_F64)
         blk = _row_block(v)
         for s in range(0, idx.numel(), blk):
@@ -267,8 +272,11 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
         # column of each vocabulary id among the selected rows, -1 if absent
         col_of = torch.full((v,), -1, dtype=torch.int64)
         col_of[jdx] = torch.arange(jdx.numel())
-        w_sel = weight[jdx]
-        b_sel = None if bias is None else bias[jdx]
+        if vocab_rows is None:
+            w_sel, b_sel = weight, bias
+        else:
+            w_sel = weight[jdx]
+            b_sel = None if bias is None else bias[jdx]
         gw = torch.zeros(jdx.numel(), hidden.shape[1], dtype=_F64)
         gb = torch.zeros(jdx.numel(), dtype=_F64)
         blk = _row_block(jdx.numel())

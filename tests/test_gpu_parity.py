@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from _parity import TOL, check_backward, check_forward, oracle_args, run_gpu, to_dev
+from _parity import TOL, check_backward, check_forward, grad_scale, oracle_args, run_gpu, to_dev
 from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +58,7 @@ def _check_case(w, vocab_chunk=0, grad_weight_dtype=None):
     tol = TOL[w.dtype]
     check_forward(out, ref, w, tol)
     gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"])
-    check_backward(out, gref, tol, x["bias"] is not None)
+    check_backward(out, gref, tol, x["bias"] is not None, grad_scale(w.reduction, ref["n_valid"]))
 
 
 @pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
@@ -148,4 +148,4 @@ def test_target_out_of_range(dtype):
     d = (out["loss_rows"].double() - ref["loss"])[ok].abs()
     assert float(d.max()) <= tol["loss_rel"] * max(1.0, float(ref["loss"][ok].abs().max()))
     gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"])
-    check_backward(out, gref, tol, False)
+    check_backward(out, gref, tol, False, grad_scale("sum", ref["n_valid"]))
