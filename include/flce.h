@@ -134,6 +134,34 @@ flce_status flce_forward(const flce_problem* p, const void* hidden,
                          int32_t* err_word, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* Forward pass that allocates nothing and takes no workspace. The method's
+ * pages have no counterpart to it; it exists for callers that cannot call
+ * cudaMalloc and have no workspace to hand in: for example a host framework
+ * whose memory pool owns the whole device and refuses allocations from
+ * libraries, or a latency-bound loop where a cudaMalloc (which may
+ * synchronise the device) is not allowed.
+ *   Arguments and outputs are those of flce_forward() without `workspace`
+ *   and `workspace_bytes`; results are the same as flce_forward's.
+ *   Scratch: a fixed 16 MiB array inside the library, held by every GPU that
+ *   loads the library until the process exits. Problems whose forward
+ *   workspace (flce_forward_workspace_size) exceeds 16 MiB -- roughly
+ *   N * ceil(V/256) * 16 bytes for bf16, e.g. N <= 2000 at V = 128256 -- are
+ *   rejected with FLCE_ERR_UNSUPPORTED before any launch.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one array, which keeps the last call's contents:
+ *   calls whose work overlaps on the GPU (for example on two streams without
+ *   ordering between them) race and corrupt each other's results. Order them
+ *   on one stream. */
+flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden,
+                                 const void* weight, const void* bias,
+                                 const int64_t* targets, float* loss_rows,
+                                 float* lse_rows, int32_t* correct_rows,
+                                 float* entropy_rows, float* loss_out,
+                                 float* metrics_out, int32_t* n_valid,
+                                 int32_t* err_word, void* stream);
+
 /* Bytes of device workspace flce_backward() needs for `p` (0 if invalid):
  * the dlogits buffer of one vocabulary chunk (N x chunk, in bf16 for FLCE_BF16
  * and fp32 for FLCE_F32), an fp32 [N,H] grad_hidden accumulator when there is

@@ -37,6 +37,7 @@ REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
 EXPORTS = (
     "flce_forward_workspace_size",
     "flce_forward",
+    "flce_forward_noalloc",
     "flce_backward_workspace_size",
     "flce_backward",
     "flce_status_string",
@@ -110,6 +111,8 @@ def load() -> ctypes.CDLL:
         lib.flce_forward.argtypes = [_PROB] + [_P] * 15
         lib.flce_forward.argtypes[-2] = ctypes.c_size_t
         lib.flce_forward.restype = ctypes.c_int
+        lib.flce_forward_noalloc.argtypes = [_PROB] + [_P] * 13
+        lib.flce_forward_noalloc.restype = ctypes.c_int
         lib.flce_backward.argtypes = [_PROB] + [_P] * 14
         lib.flce_backward.argtypes[-2] = ctypes.c_size_t
         lib.flce_backward.restype = ctypes.c_int
@@ -168,6 +171,19 @@ def flce_forward(p, hidden, weight, bias, targets, loss_rows, lse_rows, correct_
                              n_valid, err_word, workspace, workspace_bytes, stream)
     if check:
         _check(st, "flce_forward")
+    return st
+
+
+def flce_forward_noalloc(p, hidden, weight, bias, targets, loss_rows, lse_rows, correct_rows,
+                         entropy_rows, loss_out, metrics_out, n_valid, err_word, stream,
+                         check=True) -> int:
+    """flce_forward without a workspace: for callers that cannot allocate
+    device memory; the scratch is a fixed 16 MiB array inside the library."""
+    st = load().flce_forward_noalloc(ctypes.byref(p), hidden, weight, bias, targets, loss_rows,
+                                     lse_rows, correct_rows, entropy_rows, loss_out,
+                                     metrics_out, n_valid, err_word, stream)
+    if check:
+        _check(st, "flce_forward_noalloc")
     return st
 
 

@@ -290,6 +290,41 @@ int grid_for(int64_t tiles, int sms) {
 
 }  // namespace
 
+// ------------------------------------------------- fixed forward scratch
+// Scratch for flce_forward_noalloc(). It is one fixed array per GPU that
+// loads this library and stays allocated until the process exits, so it is
+// kept small: 16 MiB.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char flce_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+// Device address of flce_static_scratch on the current device. The host-side
+// name of the array is only a stand-in, so the address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current.
+flce_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FLCE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    e = cudaSetDevice(dev);  // bind this device's primary context to the thread
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, flce_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(flce_static_scratch)");
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return FLCE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* flce_status_string(flce_status s) {
@@ -699,6 +734,33 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
     if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
   }
   return FLCE_OK;
+}
+
+// Forward pass for callers that cannot provide a workspace: the same kernels
+// as flce_forward(), with their scratch taken from flce_static_scratch.
+flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden, const void* weight,
+                                 const void* bias, const int64_t* targets, float* loss_rows,
+                                 float* lse_rows, int32_t* correct_rows, float* entropy_rows,
+                                 float* loss_out, float* metrics_out, int32_t* n_valid,
+                                 int32_t* err_word, void* stream) {
+  g_err[0] = 0;
+  flce_status st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  const size_t need = plan_forward(p).total;
+  if (need > kStaticScratchBytes)
+    return fail(FLCE_ERR_UNSUPPORTED,
+                "flce_forward_noalloc: this problem needs %zu bytes of scratch, the fixed "
+                "scratch holds %zu (about N * ceil(V/256) * 16 bytes for bf16 must fit); "
+                "call flce_forward with a workspace instead",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != FLCE_OK) return st;
+  // Nothing in the scratch needs to start at zero: every element the kernels
+  // read is first written by the same call.
+  return flce_forward(p, hidden, weight, bias, targets, loss_rows, lse_rows, correct_rows,
+                      entropy_rows, loss_out, metrics_out, n_valid, err_word, scratch,
+                      kStaticScratchBytes, stream);
 }
 
 }  // extern "C"
