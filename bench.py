@@ -194,7 +194,7 @@ def bench_ours(args, rank, world, dev):
     met_h = torch.empty(2, dtype=torch.float32).pin_memory()
     e2e_steps = max(1, min(args.steps, 10))
     h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
-    d2h = loss_h.numel() * 4 + met_h.numel() * 4
+    d2h = loss_h.numel() * 4 + (met_h.numel() * 4 if step.metrics is not None else 0)
 
     def e2e_step():
         for k, t in pin.items():
@@ -202,7 +202,8 @@ def bench_ours(args, rank, world, dev):
                 x[k].copy_(t, non_blocking=True)
         step(sh)
         loss_h.copy_(step.loss, non_blocking=True)
-        met_h.copy_(step.metrics, non_blocking=True)
+        if step.metrics is not None:
+            met_h.copy_(step.metrics, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
