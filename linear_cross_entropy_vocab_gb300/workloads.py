@@ -30,7 +30,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "gemm_flops"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "peaked_rows", "gemm_flops"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -127,6 +127,14 @@ def make_inputs(w: Workload) -> dict:
         "bias": None if bias is None else bias.to(dt),
         "targets": targets,
     }
+
+
+def peaked_rows(w: Workload) -> torch.Tensor:
+    """The weight rows that make_inputs scaled by ``peaked_factor`` (same draw)."""
+    if w.peaked_frac <= 0:
+        return torch.empty(0, dtype=torch.int64)
+    n_peak = int(round(w.peaked_frac * w.v))
+    return torch.randperm(w.v, generator=_gen(w.seed, 5))[:n_peak]
 
 
 def gemm_flops(n: int, h: int, v: int) -> float:

@@ -1,0 +1,99 @@
+"""Full-size parity at the three large workloads, in the launch configuration
+bench.py times (default vocabulary chunking, one stream).
+
+The oracle runs its fp64 forward over every row: per-row loss, lse, entropy
+and argmax are compared for all N rows, and the reduced loss and metrics
+exactly. The gradients are compared on samples the oracle computes one by
+one:
+  * 512 grad_hidden rows, stratified: first and last rows, ignored rows,
+    rows whose target is a peaked (x8) weight row, the rest random;
+  * 256 grad_weight (and grad_bias) rows: vocabulary ids 0, 1, V-1, tile
+    and chunk boundaries, peaked rows, targets of sampled rows, the rest
+    random.
+Plus a property that holds at any size: with softcap off and logit_scale 1,
+sum_j grad_weight[j, :] = 0 up to bf16 rounding.
+
+These take minutes of host fp64 work each (the oracle's full forward is
+2·N·H·V multiply-adds).
+"""
+import pytest
+import torch
+
+import oracle
+from _parity import TOL, check_backward, check_forward, grad_scale, oracle_args, run_gpu, to_dev
+from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, make_inputs, peaked_rows
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+BWD_CHUNK_BF16_BUDGET = 512 << 20  # default dlogits chunk budget of the library
+
+
+def _sample_rows(w, targets, peaked, k=512, seed=11):
+    n = w.n
+    g = torch.Generator().manual_seed(seed)
+    picks = [0, 1, n - 1, n - 2, min(n - 1, 127), min(n - 1, 128)]
+    picks += torch.nonzero(targets == w.ignore_index).flatten()[:48].tolist()
+    if peaked.numel():
+        hit = torch.isin(targets, peaked)
+        picks += torch.nonzero(hit).flatten()[:64].tolist()
+    picks += torch.randperm(n, generator=g)[:k].tolist()
+    out = []
+    for r in picks:
+        if r not in out:
+            out.append(int(r))
+    return sorted(out[:k])
+
+
+def _sample_vocab(w, targets, rows, peaked, k=256, seed=12):
+    v = w.v
+    g = torch.Generator().manual_seed(seed)
+    chunk = max(256, (BWD_CHUNK_BF16_BUDGET // (w.n * 2)) // 256 * 256)
+    picks = [0, 1, v - 1, v - 2, 255, 256, 257]
+    c = chunk
+    while c < v:
+        picks += [c - 1, c]
+        c += chunk
+    picks += peaked[:32].tolist()
+    t = targets[rows]
+    picks += t[(t >= 0) & (t < v)][:48].tolist()
+    picks += torch.randperm(v, generator=g)[:k].tolist()
+    out = []
+    for j in picks:
+        if 0 <= j < v and j not in out:
+            out.append(int(j))
+    return sorted(out[:k])
+
+
+@pytest.mark.parametrize("name", ["llama3_head_bf16", "softcap_bf16", "long_bf16"])
+def test_fullsize_parity(name):
+    w = WORKLOADS[name]
+    x = make_inputs(w)
+    xd = to_dev(x)
+    tol = TOL[w.dtype]
+    if name == "long_bf16":
+        # first phase of this workload: forward only, reduction none
+        w_none = w.with_shape(reduction="none")
+        fwd_none = run_gpu(xd, w_none, backward=False)
+    out = run_gpu(xd, w, grad_out=1.0)
+    assert out["err_word"] == 0
+    ref = oracle.forward(*oracle_args(x, w))
+    check_forward(out, ref, w, tol)
+    if name == "long_bf16":
+        assert torch.equal(fwd_none["loss_rows"], out["loss_rows"])
+        assert torch.equal(fwd_none["lse_rows"], out["lse_rows"])
+    peaked = peaked_rows(w)
+    rows = _sample_rows(w, x["targets"], peaked)
+    vocab = _sample_vocab(w, x["targets"], rows, peaked)
+    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab)
+    sampled = {
+        "grad_hidden": out["grad_hidden"][rows],
+        "grad_weight": out["grad_weight"][vocab],
+        "grad_bias": None if out["grad_bias"] is None else out["grad_bias"][vocab],
+    }
+    check_backward(sampled, gref, tol, x["bias"] is not None,
+                   grad_scale(w.reduction, ref["n_valid"]))
+    if w.softcap is None and w.logit_scale == 1.0:
+        gw = out["grad_weight"].double()
+        col = gw.sum(dim=0).abs()
+        mag = gw.abs().sum(dim=0)
+        assert bool((col <= 1e-2 * mag + 1e-12).all()), float((col / mag).max())
