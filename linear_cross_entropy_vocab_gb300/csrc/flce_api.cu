@@ -204,7 +204,7 @@ flce_status check_problem(const flce_problem* p) {
     return fail(FLCE_ERR_UNSUPPORTED, "bf16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld",
                 (long long)p->h);
   if (is_bf16(p)) {
-    const int64_t m_tiles = cdiv(p->n, flce::kBM), n_tiles = cdiv(p->v, flce::kBN);
+    const int64_t m_tiles = cdiv(p->n, flce::kBM), n_tiles = cdiv(p->v, flce::kBM);
     if (m_tiles * n_tiles >= (int64_t(1) << 31))
       return fail(FLCE_ERR_UNSUPPORTED, "too many tiles");
   }
@@ -282,10 +282,6 @@ flce_status check_workspace(void* ws, size_t have, size_t need) {
   if (need > 0 && (ws == nullptr || !aligned(ws, kAlign)))
     return fail(FLCE_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   return FLCE_OK;
-}
-
-int grid_for(int64_t tiles, int sms) {
-  return static_cast<int>(tiles < sms ? tiles : sms);
 }
 
 }  // namespace
@@ -451,10 +447,10 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
     if (bf16) {
       CUtensorMap tm_h, tm_w;
       if (!make_map(&tm_h, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
-          !make_map(&tm_w, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBN))
+          !make_map(&tm_w, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC))
         return FLCE_ERR_CUDA;
       GemmGeom g{};
-      g.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
       g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
       g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g.m_fastest = 1;
@@ -469,8 +465,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.n_vt = plan.n_vt;
       fp.xf = xf;
       ProfScope ps("fwd_stats", s);
-      e = flce::launch_tc_fwd_stats(tm_h, tm_w, g, fp,
-                                    grid_for(int64_t(g.m_tiles) * g.n_tiles, dev.sms), s);
+      e = flce::launch_tc_fwd_stats(tm_h, tm_w, g, fp, dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
     } else {
       flce::SimtFwdParams fp{};
@@ -584,7 +579,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
     float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
     CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
     if (!make_map(&tm_h_k, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
-        !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBN) ||
+        !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC) ||
         !make_map(&tm_h_mn, "hidden^T", hidden, p->h, p->n, p->h, 64, flce::kBK) ||
         !make_map(&tm_w_mn, "weight^T", weight, p->h, p->v, p->h, 64, flce::kBK))
       return FLCE_ERR_CUDA;
@@ -599,7 +594,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
 
       // 1. recompute the chunk's logits and form D
       GemmGeom g1{};
-      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
       g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
       g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g1.m_fastest = 1;
@@ -624,14 +619,13 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.xf = xf;
       {
         ProfScope ps("bwd_dlogits", s);
-        e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp,
-                                  grid_for(int64_t(g1.m_tiles) * g1.n_tiles, dev.sms), s);
+        e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
 
       // 2. grad_weight[c0 : c0+width] = D^T @ hidden
       GemmGeom g2{};
-      g2.m_tiles = static_cast<int>(cdiv(width, flce::kBM));
+      g2.m_tiles = static_cast<int>(cdiv(width, flce::kTileRowsTC));
       g2.n_tiles = h_tiles;
       g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
       g2.m_fastest = 0;
@@ -645,14 +639,13 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       sp.cols = static_cast<int>(p->h);
       {
         ProfScope ps("bwd_grad_weight", s);
-        e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp,
-                                      grid_for(int64_t(g2.m_tiles) * g2.n_tiles, dev.sms), s);
+        e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
 
       // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
       GemmGeom g3{};
-      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kBM));
+      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
       g3.n_tiles = h_tiles;
       g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
       g3.m_fastest = 1;
@@ -674,8 +667,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       ap.cols = static_cast<int>(p->h);
       {
         ProfScope ps("bwd_grad_hidden", s);
-        e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap,
-                                      grid_for(int64_t(g3.m_tiles) * g3.n_tiles, dev.sms), s);
+        e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
     }

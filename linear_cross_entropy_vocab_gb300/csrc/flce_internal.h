@@ -14,6 +14,12 @@
 
 namespace flce {
 
+// CTAs per tensor-core GEMM tile: 2 = CTA pairs (tcgen05.mma.cta_group::2,
+// 256-row tiles), 1 = single CTAs (128-row tiles).
+constexpr int kPairCG = 2;
+constexpr int kTileRowsTC = kBM * kPairCG;
+constexpr int kBLoadRowsTC = kBN / kPairCG;
+
 // Width of one vocabulary tile of the forward statistics (tensor-core path);
 // the fp32 path uses kSimtTileV.
 constexpr int kSimtTileV = 128;
@@ -71,15 +77,15 @@ struct AccRowsParams {
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                                const GemmGeom& g, const FwdStatsParams& p, int grid,
+                                const GemmGeom& g, const FwdStatsParams& p, int sms,
                                 cudaStream_t s);
 cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                              const GemmGeom& g, const DlogitsParams& p, int grid, cudaStream_t s);
+                              const GemmGeom& g, const DlogitsParams& p, int sms, cudaStream_t s);
 cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
-                                  const GemmGeom& g, const StoreRowsParams& p, int grid,
+                                  const GemmGeom& g, const StoreRowsParams& p, int sms,
                                   cudaStream_t s);
 cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
-                                  const GemmGeom& g, const AccRowsParams& p, int grid,
+                                  const GemmGeom& g, const AccRowsParams& p, int sms,
                                   cudaStream_t s);
 
 // fp32 (SIMT) path

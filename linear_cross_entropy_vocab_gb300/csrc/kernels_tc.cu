@@ -193,7 +193,7 @@ struct EpiDlogits {
           }
         }
       }
-      if (p.gb_partial != nullptr) {
+      if (p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < p.n_rows) {
         // column sums of D over this tile's 128 rows, in a fixed order
         const float colsum = transpose_reduce32(d, lane);
         ctl->red[quarter][lane] = colsum;
@@ -326,41 +326,75 @@ struct EpiAccRows {
 // ------------------------------------------------------------------ launchers
 namespace {
 
-template <bool A_MN, bool B_MN, class Epi>
+// Persistent grid: one CTA (CG = 1) or one CTA pair (CG = 2) per resident
+// slot, never more than there are tiles.
+template <int CG, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmGeom& g,
-                        const typename Epi::Params& ep, int grid, cudaStream_t stream) {
-  auto kern = tc_gemm_kernel<A_MN, B_MN, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kGemmSmemBytes);
+                        const typename Epi::Params& ep, int sms, cudaStream_t stream) {
+  auto kern = tc_gemm_kernel<CG, A_MN, B_MN, Epi>;
+  constexpr int smem = gemm_smem_bytes<CG>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, g, ep);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  int units = sms;
+  if constexpr (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int max_clusters[64] = {0};  // resident pairs, per device
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (max_clusters[dev] == 0) {
+      cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      max_clusters[dev] = n;
+    }
+    units = max_clusters[dev];
+  }
+  const int64_t total = static_cast<int64_t>(g.m_tiles) * g.n_tiles;
+  const int64_t grid_units = total < units ? total : units;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CG), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, g, ep);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                                const GemmGeom& g, const FwdStatsParams& p, int grid,
+                                const GemmGeom& g, const FwdStatsParams& p, int sms,
                                 cudaStream_t s) {
-  return launch_gemm<false, false, EpiFwdStats>(tm_hidden_k, tm_weight_k, g, p, grid, s);
+  return launch_gemm<kPairCG, false, false, EpiFwdStats>(tm_hidden_k, tm_weight_k, g, p, sms, s);
 }
 
 cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                              const GemmGeom& g, const DlogitsParams& p, int grid,
+                              const GemmGeom& g, const DlogitsParams& p, int sms,
                               cudaStream_t s) {
-  return launch_gemm<false, false, EpiDlogits>(tm_hidden_k, tm_weight_k, g, p, grid, s);
+  return launch_gemm<kPairCG, false, false, EpiDlogits>(tm_hidden_k, tm_weight_k, g, p, sms, s);
 }
 
 cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
-                                  const GemmGeom& g, const StoreRowsParams& p, int grid,
+                                  const GemmGeom& g, const StoreRowsParams& p, int sms,
                                   cudaStream_t s) {
-  return launch_gemm<true, true, EpiStoreRows>(tm_d_mn, tm_hidden_mn, g, p, grid, s);
+  return launch_gemm<kPairCG, true, true, EpiStoreRows>(tm_d_mn, tm_hidden_mn, g, p, sms, s);
 }
 
 cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
-                                  const GemmGeom& g, const AccRowsParams& p, int grid,
+                                  const GemmGeom& g, const AccRowsParams& p, int sms,
                                   cudaStream_t s) {
-  return launch_gemm<false, true, EpiAccRows>(tm_d_k, tm_weight_mn, g, p, grid, s);
+  return launch_gemm<kPairCG, false, true, EpiAccRows>(tm_d_k, tm_weight_mn, g, p, sms, s);
 }
 
 }  // namespace flce

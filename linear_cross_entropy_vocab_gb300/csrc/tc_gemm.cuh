@@ -1,16 +1,24 @@
 // Persistent, warp-specialised tcgen05 GEMM main loop with pluggable
 // epilogues, for sm_103a.
 //
-//   D[128 x 256 tile] = sum_k A[m, k] * B[n, k]      (bf16 in, fp32 in TMEM)
+//   D[tile] = sum_k A[m, k] * B[n, k]      (bf16 in, fp32 accumulate in TMEM)
+//
+// CG = 1: one CTA computes a 128 x 256 tile (tcgen05.mma.cta_group::1).
+// CG = 2: a cluster of two CTAs computes a 256 x 256 tile with
+//   tcgen05.mma.cta_group::2 issued by the even CTA: each CTA stages its own
+//   128 rows of A and 128 of the 256 rows of B, and receives its 128 rows of
+//   D in its own TMEM. Per flop, each SM stages a third less operand data,
+//   which leaves room for a deeper (6-stage) copy ring.
 //
 // Roles of the 192 threads of a CTA (one CTA per SM, persistent over tiles):
-//   warp 0   one thread issues TMA tile loads into a kStages-deep ring
-//   warp 1   allocates the tensor memory; one thread issues tcgen05.mma
+//   warp 0   one thread issues TMA tile loads into the stage ring
+//   warp 1   allocates tensor memory; one thread (of the even CTA) issues the
+//            MMAs and commits them to mbarriers
 //   warps 2-5  the epilogue: each thread owns one accumulator row (TMEM
 //            lane), pulls its 256 fp32 columns with tcgen05.ld and hands them
 //            to the epilogue policy.
-// The 512 TMEM columns hold two 128 x 256 fp32 accumulators, so the epilogue
-// of tile i overlaps the MMAs of tile i+1.
+// The 512 TMEM columns hold two 128 x 256 fp32 accumulators per CTA, so the
+// epilogue of tile i overlaps the MMAs of tile i+1.
 //
 // Each operand is K-major (rows of K contiguous elements) or MN-major (K rows
 // of contiguous M or N elements); both are staged with 128-byte swizzle:
@@ -25,21 +33,29 @@
 
 namespace flce {
 
-constexpr int kBM = 128;  // accumulator rows = TMEM lanes
+constexpr int kBM = 128;  // accumulator rows per CTA = TMEM lanes
 constexpr int kBN = 256;  // accumulator columns per buffer
 constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUK = 16;   // K per tcgen05.mma (kind::f16)
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 4;
 constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kMaxStages = 6;
+
+template <int CG>
+struct TileCfg {
+  static constexpr int kBNLoad = kBN / CG;  // rows of B staged per CTA
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = kBNLoad * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = CG == 1 ? 4 : 6;
+  static constexpr int kTileRows = kBM * CG;  // M rows of one (pair) tile
+};
 
 struct GemmCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
@@ -48,10 +64,14 @@ struct GemmCtl {
   float red[4][32];  // epilogue scratch: per-warp column sums
 };
 
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /* 1 KB alignment slack */ +
-                               ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
+template <int CG>
+constexpr int gemm_smem_bytes() {
+  return TileCfg<CG>::kStages * TileCfg<CG>::kStageBytes + 1024 /* alignment slack */ +
+         ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
+}
 
-// Tile grid and TMA coordinate offsets of one GEMM launch.
+// Tile grid and TMA coordinate offsets of one GEMM launch. m_tiles counts
+// tiles of TileCfg<CG>::kTileRows rows.
 struct GemmGeom {
   int m_tiles, n_tiles, k_iters;
   int m_fastest;  // 1: tile u -> (u % m_tiles, u / m_tiles); 0: n fastest
@@ -70,15 +90,21 @@ __device__ __forceinline__ void tile_coords(const GemmGeom& g, int u, int& m, in
   }
 }
 
-template <bool MN, int ROWS>
+template <int CG, bool MN, int ROWS>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                              int mn0, int k0) {
   if constexpr (!MN) {
-    tma_load_2d(dst, map, bar, k0, mn0);  // box {64 along K, ROWS}
+    if constexpr (CG == 1)
+      tma_load_2d(dst, map, bar, k0, mn0);  // box {64 along K, ROWS}
+    else
+      tma_load_2d_pair(dst, map, bar, k0, mn0);
   } else {
 #pragma unroll
-    for (int b = 0; b < ROWS / 64; ++b) {
-      tma_load_2d(dst + b * 8192, map, bar, mn0 + b * 64, k0);  // box {64 along M/N, 64 along K}
+    for (int b = 0; b < ROWS / 64; ++b) {  // boxes {64 along M/N, 64 along K}
+      if constexpr (CG == 1)
+        tma_load_2d(dst + b * 8192, map, bar, mn0 + b * 64, k0);
+      else
+        tma_load_2d_pair(dst + b * 8192, map, bar, mn0 + b * 64, k0);
     }
   }
 }
@@ -93,11 +119,33 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
   }
 }
 
+template <int CG>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* err_word) {
+  if constexpr (CG == 1) {
+    return mbar_wait(bar, parity, abort_flag, err_word);
+  } else {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if ((it & 63u) == 0u) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+          *abort_flag = 1;
+          if (err_word) atomicOr(err_word, 2 /* FLCE_DEVERR_TIMEOUT */);
+          return false;
+        }
+      }
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag: used to let copies and MMAs in
 // flight finish before the CTA releases its memory.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (globaltimer_ns() - t0 > 1000000000ull) break;
   }
 }
@@ -117,35 +165,42 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 
 // Epi must provide:
 //   struct Params;
-//   static __device__ void tile(const Params&, int m_tile, int n_tile,
+//   static __device__ void tile(const Params&, int m_block, int n_tile,
 //                               uint32_t taddr, int row_in_tile, int quarter,
 //                               int lane, GemmCtl* ctl);
-// `taddr` addresses this warp's 32 TMEM lanes at column 0 of the tile's
-// accumulator; the 128 epilogue threads may use named barrier 1.
-template <bool A_MN, bool B_MN, class Epi>
+// m_block indexes 128-row blocks of M (this CTA's rows are
+// m_block*128 + [0, 128)). `taddr` addresses this warp's 32 TMEM lanes at
+// column 0 of the tile's accumulator; the 128 epilogue threads may use named
+// barrier 1.
+template <int CG, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const GemmGeom g, const typename Epi::Params ep) {
+  using Cfg = TileCfg<CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + kStages * kStageBytes);
+  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int total = g.m_tiles * g.n_tiles;
   volatile int* abort_flag = &ctl->abort;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
-  auto stage_a = [&](int s) { return base + s * kStageBytes; };
-  auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
+  auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
+  auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + Cfg::kABytes; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiThreads);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiWarps * CG);
     }
     mbar_init(smem_addr(&ctl->mma_done), 1);
     ctl->abort = 0;
@@ -156,11 +211,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_b);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (CG == 1) {
+      tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 1) {
+    __syncthreads();
+  } else {
+    cluster_sync();  // the peer's barriers are initialised before any remote use
+  }
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -169,57 +233,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ------------------------------------------------ TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0;  // bit s: stage s has been loaded at least once
+      uint32_t armed = 0;       // bit s: stage s has been loaded at least once
       uint32_t last_phase = 0;  // bit s: phase of the last load into stage s
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      for (int u = unit0; u < total && ok; u += units) {
         int m, n;
         tile_coords(g, u, m, n);
         for (int k = 0; k < g.k_iters; ++k) {
-          if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, g.err_word)) {
+          if (!wait_bar<CG>(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, g.err_word)) {
             ok = false;
             break;
           }
-          const uint32_t full = smem_addr(&ctl->full[stage]);
-          mbar_arrive_expect_tx(full, kStageBytes);
-          load_operand<A_MN, kBM>(stage_a(stage), &tm_a, full, g.a_mn0 + m * kBM,
-                                  g.a_k0 + k * kBK);
-          load_operand<B_MN, kBN>(stage_b(stage), &tm_b, full, g.b_mn0 + n * kBN,
-                                  g.b_k0 + k * kBK);
+          const uint32_t full_local = smem_addr(&ctl->full[stage]);
+          uint32_t full = full_local;
+          if constexpr (CG == 2) full = map_to_rank(full_local, 0);
+          if (leader) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
+          load_operand<CG, A_MN, kBM>(stage_a(stage), &tm_a, full,
+                                      g.a_mn0 + m * Cfg::kTileRows + static_cast<int>(rank) * kBM,
+                                      g.a_k0 + k * kBK);
+          load_operand<CG, B_MN, Cfg::kBNLoad>(
+              stage_b(stage), &tm_b, full,
+              g.b_mn0 + n * kBN + static_cast<int>(rank) * Cfg::kBNLoad, g.b_k0 + k * kBK);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // let every copy already issued land before the CTA exits
-        for (int s = 0; s < kStages; ++s) {
+      if (!ok && leader) {
+        // let every copy already issued land before the CTAs exit
+        for (int s = 0; s < Cfg::kStages; ++s) {
           if (armed & (1u << s)) drain_wait(smem_addr(&ctl->full[s]), (last_phase >> s) & 1u);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+      for (int u = unit0; u < total && ok; u += units, ++it) {
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!mbar_wait(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, g.err_word)) {
+        if (!wait_bar<CG>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, g.err_word)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
         for (int k = 0; k < g.k_iters; ++k) {
-          if (!mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, g.err_word)) {
+          if (!wait_bar<CG>(smem_addr(&ctl->full[stage]), phase, abort_flag, g.err_word)) {
             ok = false;
             break;
           }
@@ -227,49 +295,82 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
 #pragma unroll
           for (int kk = 0; kk < kBK / kUK; ++kk) {
-            umma_bf16(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc,
-                      (k | kk) != 0 ? 1u : 0u);
+            const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
+            if constexpr (CG == 1)
+              umma_bf16(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc, acc);
+            else
+              umma_bf16_pair(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc,
+                             acc);
           }
-          umma_commit(smem_addr(&ctl->empty[stage]));
-          if (++stage == kStages) {
+          if constexpr (CG == 1)
+            umma_commit(smem_addr(&ctl->empty[stage]));
+          else
+            umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+          if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(smem_addr(&ctl->acc_full[buf]));
+        if constexpr (CG == 1)
+          umma_commit(smem_addr(&ctl->acc_full[buf]));
+        else
+          umma_commit_pair(smem_addr(&ctl->acc_full[buf]), 0x3);
       }
       // all MMAs issued by this thread complete before TMEM is released
-      umma_commit(smem_addr(&ctl->mma_done));
+      if constexpr (CG == 1)
+        umma_commit(smem_addr(&ctl->mma_done));
+      else
+        umma_commit_pair(smem_addr(&ctl->mma_done), 0x3);
+      drain_wait(smem_addr(&ctl->mma_done), 0);
+    } else if (lane == 0 && CG == 2) {
+      // the odd CTA's TMEM is written by the even CTA's MMAs: wait for them
       drain_wait(smem_addr(&ctl->mma_done), 0);
     }
   } else {
     // -------------------------------------------------- epilogue warps
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
     const int row_in_tile = quarter * 32 + lane;
+    uint32_t acc_empty_leader = smem_addr(&ctl->acc_empty[0]);
+    if constexpr (CG == 2) acc_empty_leader = map_to_rank(acc_empty_leader, 0);
     int it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    for (int u = unit0; u < total; u += units, ++it) {
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-      const bool got =
-          mbar_wait(smem_addr(&ctl->acc_full[buf]), use, abort_flag, g.err_word);
+      const bool got = wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, g.err_word);
       if (!epi_all(got)) break;
       tc_fence_after_sync();
       int m, n;
       tile_coords(g, u, m, n);
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
-      Epi::tile(ep, m, n, taddr, row_in_tile, quarter, lane, ctl);
+      Epi::tile(ep, m * CG + static_cast<int>(rank), n, taddr, row_in_tile, quarter, lane, ctl);
       tc_fence_before_sync();
-      mbar_arrive(smem_addr(&ctl->acc_empty[buf]));
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = acc_empty_leader + static_cast<uint32_t>(buf * sizeof(uint64_t));
+        if constexpr (CG == 1)
+          mbar_arrive(bar);
+        else
+          mbar_arrive_cluster(bar);
+      }
     }
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  __syncwarp();
+  if constexpr (CG == 1) {
+    __syncthreads();
+  } else {
+    cluster_sync();
+  }
   if (warp == 1) {
+    __syncwarp();  // the release is warp-collective
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (CG == 1)
+      tmem_dealloc(tmem, kTmemCols);
+    else
+      tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
