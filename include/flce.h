@@ -92,6 +92,8 @@ typedef enum flce_reduction {
  *   vocab_chunk        backward vocabulary chunk width; 0 picks the default
  *                      (the chunk's N x chunk dlogits buffer is the largest
  *                      workspace item); rounded up to a multiple of 256
+ *   flags              OR of FLCE_SKIP_IGNORED_ROWS; 0 for none
+ *   reserved           must be 0
  */
 typedef struct flce_problem {
   int64_t n, h, v;
@@ -103,7 +105,19 @@ typedef struct flce_problem {
   int32_t reduction;
   int32_t grad_weight_dtype;
   int64_t vocab_chunk;
+  int32_t flags;
+  int32_t reserved;
 } flce_problem;
+
+/* Leave rows whose target is ignore_index out of every contraction (bf16 path;
+ * the fp32 path computes every row either way). The non-ignored rows are
+ * gathered, in their original order, into the workspace, and the GEMMs run
+ * over them alone: ignored rows contribute nothing to the loss or to any
+ * gradient, so their logits are never needed. Loss, metrics and gradients are
+ * unchanged; loss_rows and correct_rows of ignored rows are 0 as without the
+ * flag, but lse_rows and entropy_rows of ignored rows are not computed (NaN).
+ * Grad_hidden rows of ignored rows are written as 0. */
+#define FLCE_SKIP_IGNORED_ROWS 1
 
 /* Bytes of device workspace flce_forward() needs for `p` (0 if `p` is
  * invalid). Cite: §Algorithm ("tiles over the vocabulary ... merges the tile

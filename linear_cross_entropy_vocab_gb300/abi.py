@@ -28,6 +28,8 @@ FLCE_RED_NONE = 0
 FLCE_RED_SUM = 1
 FLCE_RED_MEAN = 2
 
+FLCE_SKIP_IGNORED_ROWS = 1
+
 FLCE_DEVERR_TARGET_RANGE = 1
 FLCE_DEVERR_TIMEOUT = 2
 
@@ -64,6 +66,8 @@ class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
         ("reduction", ctypes.c_int32),
         ("grad_weight_dtype", ctypes.c_int32),
         ("vocab_chunk", ctypes.c_int64),
+        ("flags", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -141,7 +145,7 @@ def _check(status: int, call: str):
 
 def make_problem(n, h, v, dtype, has_bias, ignore_index=-100, logit_scale=1.0,
                  softcap=None, reduction="mean", grad_weight_dtype=None,
-                 vocab_chunk=0) -> flce_problem:
+                 vocab_chunk=0, skip_ignored=False) -> flce_problem:
     p = flce_problem()
     p.n, p.h, p.v = int(n), int(h), int(v)
     p.dtype = int(dtype)
@@ -152,6 +156,8 @@ def make_problem(n, h, v, dtype, has_bias, ignore_index=-100, logit_scale=1.0,
     p.reduction = REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
     p.grad_weight_dtype = int(dtype if grad_weight_dtype is None else grad_weight_dtype)
     p.vocab_chunk = int(vocab_chunk)
+    p.flags = FLCE_SKIP_IGNORED_ROWS if skip_ignored else 0
+    p.reserved = 0
     return p
 
 

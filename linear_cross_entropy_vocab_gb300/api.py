@@ -60,16 +60,19 @@ def _check_inputs(hidden, weight, targets, bias):
 def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
                          logit_scale=1.0, softcap=None, reduction="mean",
                          return_metrics=False, row_metrics=False, err_word=None,
-                         vocab_chunk=0) -> dict:
+                         vocab_chunk=0, skip_ignored=False) -> dict:
     """Run flce_forward; returns a dict of freshly allocated output tensors:
     loss (0-d, or [N] for 'none'), loss_rows, lse_rows, n_valid (0-d int32),
-    metrics ([2] or None), correct_rows / entropy_rows (when row_metrics)."""
+    metrics ([2] or None), correct_rows / entropy_rows (when row_metrics).
+    ``skip_ignored`` leaves ignored rows out of the contractions (their
+    lse_rows / entropy_rows are then NaN)."""
     _check_inputs(hidden, weight, targets, bias)
     n, h = hidden.shape
     v = weight.shape[0]
     dev = hidden.device
     prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
-                            logit_scale, softcap, reduction, vocab_chunk=vocab_chunk)
+                            logit_scale, softcap, reduction, vocab_chunk=vocab_chunk,
+                            skip_ignored=skip_ignored)
     f32 = dict(dtype=torch.float32, device=dev)
     loss_rows = torch.empty(n, **f32)
     lse_rows = torch.empty(n, **f32)
@@ -100,10 +103,11 @@ def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
 def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, bias=None,
                           ignore_index=-100, logit_scale=1.0, softcap=None,
                           reduction="mean", grad_weight_dtype=None, err_word=None,
-                          vocab_chunk=0):
+                          vocab_chunk=0, skip_ignored=False):
     """Run flce_backward; returns (grad_hidden, grad_weight, grad_bias).
     ``grad_out`` is a 0-d fp32 tensor ('sum'/'mean') or [N] ('none').
-    ``grad_weight_dtype`` torch.float32 keeps grad_weight in fp32."""
+    ``grad_weight_dtype`` torch.float32 keeps grad_weight in fp32.
+    ``skip_ignored`` leaves ignored rows out of the contractions."""
     _check_inputs(hidden, weight, targets, bias)
     n, h = hidden.shape
     v = weight.shape[0]
@@ -112,7 +116,7 @@ def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, 
     gw_code = abi.FLCE_F32 if gw_dtype == torch.float32 else _dtype_code(hidden)
     prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
                             logit_scale, softcap, reduction, grad_weight_dtype=gw_code,
-                            vocab_chunk=vocab_chunk)
+                            vocab_chunk=vocab_chunk, skip_ignored=skip_ignored)
     grad_out = grad_out.to(device=dev, dtype=torch.float32).contiguous()
     grad_hidden = torch.empty_like(hidden)
     grad_weight = torch.empty(v, h, dtype=gw_dtype, device=dev)
@@ -132,8 +136,9 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, ignore_index, logit_scale, softcap,
                 reduction, return_metrics):
+        # ignored rows contribute nothing, so they are left out of the GEMMs
         out = flce_forward_tensors(hidden, weight, targets, bias, ignore_index, logit_scale,
-                                   softcap, reduction, return_metrics)
+                                   softcap, reduction, return_metrics, skip_ignored=True)
         ctx.save_for_backward(hidden, weight, bias, targets, out["lse_rows"], out["n_valid"])
         ctx.opts = (ignore_index, logit_scale, softcap, reduction)
         metrics = out["metrics"]
@@ -148,7 +153,7 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
         ignore_index, logit_scale, softcap, reduction = ctx.opts
         gh, gw, gb = flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid,
                                            grad_loss, bias, ignore_index, logit_scale,
-                                           softcap, reduction)
+                                           softcap, reduction, skip_ignored=True)
         need = ctx.needs_input_grad
         return (gh if need[0] else None, gw if need[1] else None,
                 gb if (bias is not None and need[2]) else None,

@@ -166,18 +166,52 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kDefaultDlogitsBudget = int64_t(512) << 20;  // bytes of one dlogits chunk
 
+// Workspace items of valid-row compaction (FLCE_SKIP_IGNORED_ROWS).
+struct CompactPlan {
+  bool on = false;
+  size_t row_map = 0, n_kept = 0, hidden_c = 0, targets_c = 0, lse_c = 0, grad_c = 0;
+};
+
 struct FwdPlan {
   int64_t n_vt = 0;
   size_t partials = 0, zt = 0, correct = 0, entropy = 0, total = 0;
+  CompactPlan cp;
 };
 
 struct BwdPlan {
   int64_t chunk = 0, n_chunks = 0, gb_parts = 0;
   size_t d = 0, acc = 0, gb = 0, total = 0;
   bool use_acc = false;
+  CompactPlan cp;
 };
 
 bool is_bf16(const flce_problem* p) { return p->dtype == FLCE_BF16; }
+
+bool skips_ignored(const flce_problem* p) {
+  return is_bf16(p) && (p->flags & FLCE_SKIP_IGNORED_ROWS) != 0;
+}
+
+// Appends the compaction items at `off`; returns the new end.
+size_t plan_compaction(const flce_problem* p, bool backward, size_t off, CompactPlan* c) {
+  c->on = skips_ignored(p);
+  if (!c->on) return off;
+  const size_t n = static_cast<size_t>(p->n);
+  c->row_map = off;
+  off = align_up(off + n * 4);
+  c->n_kept = off;
+  off = align_up(off + 4);
+  c->hidden_c = off;
+  off = align_up(off + n * static_cast<size_t>(p->h) * 2);
+  c->targets_c = off;
+  off = align_up(off + n * 8);
+  if (backward) {
+    c->lse_c = off;
+    off = align_up(off + n * 4);
+    c->grad_c = off;
+    off = align_up(off + n * 4);
+  }
+  return off;
+}
 
 flce_status check_problem(const flce_problem* p) {
   if (p == nullptr) return fail(FLCE_ERR_INVALID_ARG, "problem pointer is NULL");
@@ -200,6 +234,8 @@ flce_status check_problem(const flce_problem* p) {
   if (std::isnan(p->softcap) || std::isinf(p->softcap))
     return fail(FLCE_ERR_INVALID_ARG, "softcap must be finite (<= 0 disables it)");
   if (p->vocab_chunk < 0) return fail(FLCE_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
+  if ((p->flags & ~FLCE_SKIP_IGNORED_ROWS) != 0 || p->reserved != 0)
+    return fail(FLCE_ERR_INVALID_ARG, "unknown flags or non-zero reserved field");
   if (is_bf16(p) && p->h % 8 != 0)
     return fail(FLCE_ERR_UNSUPPORTED, "bf16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld",
                 (long long)p->h);
@@ -225,6 +261,7 @@ FwdPlan plan_forward(const flce_problem* p) {
   off = align_up(off + static_cast<size_t>(p->n) * 4);
   f.entropy = off;
   off = align_up(off + static_cast<size_t>(p->n) * 4);
+  off = plan_compaction(p, false, off, &f.cp);
   f.total = off;
   return f;
 }
@@ -253,6 +290,7 @@ BwdPlan plan_backward(const flce_problem* p) {
   if (b.use_acc) off = align_up(off + static_cast<size_t>(p->n) * p->h * 4);
   b.gb = off;
   if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
+  off = plan_compaction(p, true, off, &b.cp);
   b.total = off;
   return b;
 }
@@ -444,9 +482,52 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
   cudaError_t e;
 
   if (p->n > 0) {
+    // valid-row compaction: the GEMMs read the kept rows from a gathered copy
+    const bool compact = plan.cp.on;
+    int32_t* row_map = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.row_map) : nullptr;
+    int32_t* n_kept = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.n_kept) : nullptr;
+    const void* rows_src = hidden;
+    const int64_t* rows_targets = targets;
+    if (compact) {
+      flce::CompactParams cp{};
+      cp.targets = targets;
+      cp.n = p->n;
+      cp.ignore_index = p->ignore_index;
+      cp.row_map = row_map;
+      cp.n_kept = n_kept;
+      cp.loss_rows = loss_rows;
+      cp.lse_rows = lse_rows;
+      cp.correct_ws = correct_ws;
+      cp.entropy_ws = entropy_ws;
+      cp.correct_rows = correct_rows;
+      cp.entropy_rows = entropy_rows;
+      flce::GatherParams gp{};
+      gp.hidden = static_cast<const __nv_bfloat16*>(hidden);
+      gp.n = p->n;
+      gp.h = p->h;
+      gp.row_map = row_map;
+      gp.n_kept = n_kept;
+      gp.pad_rows = flce::kTileRowsTC;
+      gp.hidden_c = reinterpret_cast<__nv_bfloat16*>(ws + plan.cp.hidden_c);
+      gp.targets = targets;
+      gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
+      gp.ignore_index = p->ignore_index;
+      {
+        ProfScope ps("compact_rows", s);
+        e = flce::launch_compact_rows(cp, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "row compaction kernel");
+      {
+        ProfScope ps("gather_rows", s);
+        e = flce::launch_gather_rows(gp, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
+      rows_src = gp.hidden_c;
+      rows_targets = gp.targets_c;
+    }
     if (bf16) {
       CUtensorMap tm_h, tm_w;
-      if (!make_map(&tm_h, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+      if (!make_map(&tm_h, "hidden", rows_src, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
           !make_map(&tm_w, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC))
         return FLCE_ERR_CUDA;
       GemmGeom g{};
@@ -454,13 +535,16 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
       g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g.m_fastest = 1;
+      g.dyn_rows = n_kept;
+      g.dyn_axis = 0;
       g.err_word = err_word;
       flce::FwdStatsParams fp{};
       fp.bias = static_cast<const __nv_bfloat16*>(bias);
-      fp.targets = targets;
+      fp.targets = rows_targets;
       fp.partials = partials;
       fp.zt = zt;
       fp.n_rows = p->n;
+      fp.n_rows_dyn = n_kept;
       fp.v = p->v;
       fp.n_vt = plan.n_vt;
       fp.xf = xf;
@@ -487,7 +571,9 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
     flce::MergeParams mp{};
     mp.partials = partials;
     mp.zt = zt;
-    mp.targets = targets;
+    mp.targets = rows_targets;
+    mp.row_map = row_map;
+    mp.n_dyn = n_kept;
     mp.n = p->n;
     mp.v = p->v;
     mp.n_vt = plan.n_vt;
@@ -577,10 +663,64 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   if (bf16) {
     __nv_bfloat16* dbuf = reinterpret_cast<__nv_bfloat16*>(ws + plan.d);
     float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
+    // valid-row compaction: rows of hidden, targets, lse and per-row
+    // upstream gradients are gathered; grad_hidden is scattered back
+    const bool compact = plan.cp.on;
+    int32_t* row_map = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.row_map) : nullptr;
+    int32_t* n_kept = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.n_kept) : nullptr;
+    const void* rows_src = hidden;
+    const int64_t* rows_targets = targets;
+    const float* rows_lse = lse_rows;
+    const float* rows_grad = grad_out;
+    if (compact) {
+      flce::CompactParams cp{};
+      cp.targets = targets;
+      cp.n = p->n;
+      cp.ignore_index = p->ignore_index;
+      cp.row_map = row_map;
+      cp.n_kept = n_kept;
+      flce::GatherParams gp{};
+      gp.hidden = static_cast<const __nv_bfloat16*>(hidden);
+      gp.n = p->n;
+      gp.h = p->h;
+      gp.row_map = row_map;
+      gp.n_kept = n_kept;
+      gp.pad_rows = flce::kTileRowsTC;
+      gp.hidden_c = reinterpret_cast<__nv_bfloat16*>(ws + plan.cp.hidden_c);
+      gp.targets = targets;
+      gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
+      gp.ignore_index = p->ignore_index;
+      gp.lse = lse_rows;
+      gp.lse_c = reinterpret_cast<float*>(ws + plan.cp.lse_c);
+      if (p->reduction == FLCE_RED_NONE) {
+        gp.grad_rows = grad_out;
+        gp.grad_rows_c = reinterpret_cast<float*>(ws + plan.cp.grad_c);
+      }
+      {
+        ProfScope ps("compact_rows", s);
+        e = flce::launch_compact_rows(cp, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "row compaction kernel");
+      {
+        ProfScope ps("gather_rows", s);
+        e = flce::launch_gather_rows(gp, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
+      {
+        ProfScope ps("zero_ignored_rows", s);
+        e = flce::launch_zero_ignored_rows(targets, p->n, p->ignore_index,
+                                           static_cast<__nv_bfloat16*>(grad_hidden), p->h, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden zero kernel");
+      rows_src = gp.hidden_c;
+      rows_targets = gp.targets_c;
+      rows_lse = gp.lse_c;
+      if (p->reduction == FLCE_RED_NONE) rows_grad = gp.grad_rows_c;
+    }
     CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
-    if (!make_map(&tm_h_k, "hidden", hidden, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+    if (!make_map(&tm_h_k, "hidden", rows_src, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
         !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC) ||
-        !make_map(&tm_h_mn, "hidden^T", hidden, p->h, p->n, p->h, 64, flce::kBK) ||
+        !make_map(&tm_h_mn, "hidden^T", rows_src, p->h, p->n, p->h, 64, flce::kBK) ||
         !make_map(&tm_w_mn, "weight^T", weight, p->h, p->v, p->h, 64, flce::kBK))
       return FLCE_ERR_CUDA;
     const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
@@ -599,18 +739,21 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g1.m_fastest = 1;
       g1.b_mn0 = static_cast<int>(c0);
+      g1.dyn_rows = n_kept;
+      g1.dyn_axis = 0;
       g1.err_word = err_word;
       flce::DlogitsParams dp{};
       dp.bias = static_cast<const __nv_bfloat16*>(bias);
-      dp.targets = targets;
-      dp.lse = lse_rows;
-      dp.grad_out = grad_out;
+      dp.targets = rows_targets;
+      dp.lse = rows_lse;
+      dp.grad_out = rows_grad;
       dp.n_valid = n_valid;
       dp.d = dbuf;
       dp.ldd = plan.chunk;
       dp.gb_partial = gb_partial;
       dp.gb_ld = p->v;
       dp.n_rows = p->n;
+      dp.n_rows_dyn = n_kept;
       dp.v = p->v;
       dp.ignore_index = p->ignore_index;
       dp.c0 = static_cast<int>(c0);
@@ -629,6 +772,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g2.n_tiles = h_tiles;
       g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
       g2.m_fastest = 0;
+      g2.dyn_rows = n_kept;  // the contraction runs over the kept rows
+      g2.dyn_axis = 1;
       g2.err_word = err_word;
       flce::StoreRowsParams sp{};
       sp.out = grad_weight;
@@ -650,6 +795,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
       g3.m_fastest = 1;
       g3.b_k0 = static_cast<int>(c0);
+      g3.dyn_rows = n_kept;
+      g3.dyn_axis = 0;
       g3.err_word = err_word;
       flce::AccRowsParams ap{};
       ap.acc = acc;
@@ -664,6 +811,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
         ap.mode = flce::kAccAdd;
       ap.ld = p->h;
       ap.rows = p->n;
+      ap.rows_dyn = n_kept;
+      ap.row_map = row_map;
       ap.cols = static_cast<int>(p->h);
       {
         ProfScope ps("bwd_grad_hidden", s);
@@ -721,8 +870,10 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   }
   if (p->has_bias) {
     ProfScope ps("bwd_bias_reduce", s);
+    const int32_t* n_dyn =
+        plan.cp.on ? reinterpret_cast<const int32_t*>(ws + plan.cp.n_kept) : nullptr;
     e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias, bf16 ? 1 : 0,
-                                 s);
+                                 n_dyn, flce::kBM, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
   }
   return FLCE_OK;

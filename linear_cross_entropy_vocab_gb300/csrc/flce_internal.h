@@ -30,7 +30,8 @@ struct FwdStatsParams {
   const int64_t* targets;     // [N]
   float4* partials;           // [N][n_vt] (m, s, t, argmax)
   float* zt;                  // [N] target logit
-  int64_t n_rows;
+  int64_t n_rows;             // rows of the buffers
+  const int32_t* n_rows_dyn;  // rows actually present (device count) or null
   int64_t v;
   int64_t n_vt;
   LogitXform xf;
@@ -46,7 +47,8 @@ struct DlogitsParams {
   int64_t ldd;
   float* gb_partial;  // [m_tiles][gb_ld] or null
   int64_t gb_ld;
-  int64_t n_rows;
+  int64_t n_rows;             // rows of the buffers
+  const int32_t* n_rows_dyn;  // rows actually present (device count) or null
   int64_t v;
   int64_t ignore_index;
   int c0;     // first vocabulary column of the chunk
@@ -72,6 +74,8 @@ struct AccRowsParams {
   int mode;
   int64_t ld;
   int64_t rows;
+  const int32_t* rows_dyn;  // rows actually present (device count) or null
+  const int32_t* row_map;   // output row of each accumulator row, or null (identity)
   int cols;
 };
 
@@ -129,7 +133,9 @@ cudaError_t launch_simt_gemm(int64_t m, int64_t n, int64_t k, const float* a, in
 struct MergeParams {
   const float4* partials;
   const float* zt;
-  const int64_t* targets;
+  const int64_t* targets;     // of the (possibly compacted) rows
+  const int32_t* row_map;     // original row of each compacted row, or null
+  const int32_t* n_dyn;       // compacted row count (device) or null
   int64_t n, v, n_vt, ignore_index;
   float* loss_rows;
   float* lse_rows;
@@ -155,8 +161,47 @@ struct FinalizeParams {
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 
 // out[j] = sum_{r < n_parts} part[r*ld + j] (fixed order), cast to bf16 or f32.
+// With n_dyn, n_parts = ceil(*n_dyn / rows_per_part) (at most the static one).
 cudaError_t launch_bias_reduce(const float* part, int64_t n_parts, int64_t ld, int64_t v,
-                               void* out, int out_bf16, cudaStream_t s);
+                               void* out, int out_bf16, const int32_t* n_dyn,
+                               int rows_per_part, cudaStream_t s);
+
+// ---- valid-row compaction (FLCE_SKIP_IGNORED_ROWS)
+struct CompactParams {
+  const int64_t* targets;
+  int64_t n, ignore_index;
+  int32_t* row_map;  // [N] out: original row of compacted row j (stable order)
+  int32_t* n_kept;   // out: number of kept rows
+  // forward only (null in the backward): outputs of the ignored rows
+  float* loss_rows;
+  float* lse_rows;
+  int32_t* correct_ws;
+  float* entropy_ws;
+  int32_t* correct_rows;
+  float* entropy_rows;
+};
+cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t s);
+
+struct GatherParams {
+  const __nv_bfloat16* hidden;
+  int64_t n, h;
+  const int32_t* row_map;
+  const int32_t* n_kept;
+  int pad_rows;  // rows [n_kept, roundup(n_kept, pad_rows)) are zero-filled
+  __nv_bfloat16* hidden_c;
+  const int64_t* targets;
+  int64_t* targets_c;
+  int64_t ignore_index;
+  const float* lse;   // backward: gathered into lse_c (nullable)
+  float* lse_c;
+  const float* grad_rows;  // backward, reduction none (nullable)
+  float* grad_rows_c;
+};
+cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s);
+
+// grad_hidden rows of ignored targets := 0 (bf16 [N, h]).
+cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,
+                                     __nv_bfloat16* out, int64_t h, cudaStream_t s);
 
 
 }  // namespace flce

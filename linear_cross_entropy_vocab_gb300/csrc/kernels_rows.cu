@@ -23,7 +23,8 @@ constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const MergeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
-  if (row >= p.n) return;  // warp-uniform
+  const int64_t n_rows = p.n_dyn != nullptr ? static_cast<int64_t>(*p.n_dyn) : p.n;
+  if (row >= n_rows) return;  // warp-uniform
   const float4* part = p.partials + row * p.n_vt;
   RowStats st;
   st.init();
@@ -46,12 +47,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
       if (p.err_word) atomicOr(p.err_word, 1 /* FLCE_DEVERR_TARGET_RANGE */);
     }
   }
-  p.loss_rows[row] = loss;
-  p.lse_rows[row] = lse;
-  p.correct_ws[row] = correct;
-  p.entropy_ws[row] = entropy;
-  if (p.correct_rows) p.correct_rows[row] = correct;
-  if (p.entropy_rows) p.entropy_rows[row] = entropy;
+  const int64_t orig = p.row_map != nullptr ? static_cast<int64_t>(p.row_map[row]) : row;
+  p.loss_rows[orig] = loss;
+  p.lse_rows[orig] = lse;
+  p.correct_ws[orig] = correct;
+  p.entropy_ws[orig] = entropy;
+  if (p.correct_rows) p.correct_rows[orig] = correct;
+  if (p.entropy_rows) p.entropy_rows[orig] = entropy;
 }
 
 constexpr int kFinThreads = 1024;
@@ -103,9 +105,13 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 
 __global__ void __launch_bounds__(256)
     bias_reduce_kernel(const float* __restrict__ part, int64_t n_parts, int64_t ld, int64_t v,
-                       void* out, int out_bf16) {
+                       void* out, int out_bf16, const int32_t* n_dyn, int rows_per_part) {
   const int64_t j = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   if (j >= v) return;
+  if (n_dyn != nullptr) {
+    const int64_t parts = (static_cast<int64_t>(*n_dyn) + rows_per_part - 1) / rows_per_part;
+    n_parts = parts < n_parts ? parts : n_parts;
+  }
   float acc = 0.0f;
   for (int64_t r = 0; r < n_parts; ++r) acc += part[r * ld + j];
   if (out_bf16) {
@@ -115,7 +121,113 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Stable compaction of the rows whose target is not ignore_index: one block
+// scans the rows in order, 1024 at a time (ballot + warp-total scan), so
+// compacted row j is the j-th kept row. Ignored rows get their forward
+// outputs here.
+constexpr int kCompactThreads = 1024;
+
+__global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const CompactParams p) {
+  __shared__ int warp_off[32];
+  __shared__ int chunk_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int carry = 0;
+  for (int64_t base = 0; base < p.n; base += kCompactThreads) {
+    const int64_t i = base + tid;
+    const bool in = i < p.n;
+    const bool keep = in && p.targets[i] != p.ignore_index;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    const int before = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_off[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_off[lane];
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      warp_off[lane] = incl - v;
+      if (lane == 31) chunk_total = incl;
+    }
+    __syncthreads();
+    if (keep) {
+      p.row_map[carry + warp_off[warp] + before] = static_cast<int32_t>(i);
+    } else if (in && p.loss_rows != nullptr) {
+      const float nan = __int_as_float(0x7fc00000);
+      p.loss_rows[i] = 0.0f;
+      p.lse_rows[i] = nan;
+      p.correct_ws[i] = 0;
+      p.entropy_ws[i] = nan;
+      if (p.correct_rows) p.correct_rows[i] = 0;
+      if (p.entropy_rows) p.entropy_rows[i] = nan;
+    }
+    carry += chunk_total;
+    __syncthreads();
+  }
+  if (tid == 0) *p.n_kept = carry;
+}
+
+constexpr int kGatherThreads = 128;
+
+// Compacted row j <- original row row_map[j]; rows [n_kept, pad) are zero so
+// that a contraction over rows reads zeros past the last kept row.
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherParams p) {
+  const int64_t j = blockIdx.x;
+  const int64_t kept = *p.n_kept;
+  const int64_t pad = (kept + p.pad_rows - 1) / p.pad_rows * p.pad_rows;
+  if (j >= pad || j >= p.n) return;
+  const int64_t vecs = p.h / 8;  // 8 bf16 per 16-byte vector (h % 8 == 0)
+  uint4* dst = reinterpret_cast<uint4*>(p.hidden_c + j * p.h);
+  if (j < kept) {
+    const int64_t src_row = p.row_map[j];
+    const uint4* src = reinterpret_cast<const uint4*>(p.hidden + src_row * p.h);
+    for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = __ldg(src + q);
+    if (threadIdx.x == 0) {
+      p.targets_c[j] = p.targets[src_row];
+      if (p.lse_c) p.lse_c[j] = p.lse[src_row];
+      if (p.grad_rows_c) p.grad_rows_c[j] = p.grad_rows[src_row];
+    }
+  } else {
+    for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+      p.targets_c[j] = p.ignore_index;
+      if (p.lse_c) p.lse_c[j] = 0.0f;
+      if (p.grad_rows_c) p.grad_rows_c[j] = 0.0f;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kGatherThreads)
+    zero_ignored_rows_kernel(const int64_t* __restrict__ targets, int64_t ignore_index,
+                             __nv_bfloat16* out, int64_t h) {
+  const int64_t i = blockIdx.x;
+  if (targets[i] != ignore_index) return;
+  uint4* dst = reinterpret_cast<uint4*>(out + i * h);
+  for (int64_t q = threadIdx.x; q < h / 8; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
+}
+
 }  // namespace
+
+cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t s) {
+  compact_rows_kernel<<<1, kCompactThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s) {
+  if (p.n == 0) return cudaSuccess;
+  gather_rows_kernel<<<static_cast<unsigned>(p.n), kGatherThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,
+                                     __nv_bfloat16* out, int64_t h, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  zero_ignored_rows_kernel<<<static_cast<unsigned>(n), kGatherThreads, 0, s>>>(targets,
+                                                                                ignore_index, out, h);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge_rows(const MergeParams& p, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((p.n + kMergeWarps - 1) / kMergeWarps);
@@ -129,9 +241,11 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_bias_reduce(const float* part, int64_t n_parts, int64_t ld, int64_t v,
-                               void* out, int out_bf16, cudaStream_t s) {
+                               void* out, int out_bf16, const int32_t* n_dyn,
+                               int rows_per_part, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((v + 255) / 256);
-  bias_reduce_kernel<<<grid, 256, 0, s>>>(part, n_parts, ld, v, out, out_bf16);
+  bias_reduce_kernel<<<grid, 256, 0, s>>>(part, n_parts, ld, v, out, out_bf16, n_dyn,
+                                          rows_per_part);
   return cudaGetLastError();
 }
 

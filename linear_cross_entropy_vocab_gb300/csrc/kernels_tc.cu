@@ -96,9 +96,11 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 struct EpiFwdStats {
   using Params = FwdStatsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              int row_in_tile, int /*quarter*/, int /*lane*/, GemmCtl* /*ctl*/) {
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*lane*/,
+                              GemmCtl* /*ctl*/) {
+    const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
-    const bool row_ok = row < p.n_rows;
+    const bool row_ok = row < n_eff;
     const int64_t t = row_ok ? __ldg(p.targets + row) : INT64_MIN;
     const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
     RowStats st;
@@ -111,7 +113,7 @@ struct EpiFwdStats {
       if (cb >= p.v) break;
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
       float z[32], b[32];
-      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32(p.bias, cb, nv, b);
 #pragma unroll
       for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
@@ -140,9 +142,11 @@ struct EpiFwdStats {
 struct EpiDlogits {
   using Params = DlogitsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              int row_in_tile, int quarter, int lane, GemmCtl* ctl) {
+                              bool acc_zero, int row_in_tile, int quarter, int lane,
+                              GemmCtl* ctl) {
+    const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
-    const bool row_ok = row < p.n_rows;
+    const bool row_ok = row < n_eff;
     const int64_t t = row_ok ? __ldg(p.targets + row) : p.ignore_index;
     const float g = row_ok ? row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row)
                            : 0.0f;
@@ -156,7 +160,7 @@ struct EpiDlogits {
       if (cb >= p.width) break;
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
       float z[32], b[32];
-      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32(p.bias, p.c0 + cb, nv, b);
       float d[32];
 #pragma unroll
@@ -175,7 +179,7 @@ struct EpiDlogits {
       for (int k = 0; k < 32; ++k) {
         d[k] = row_ok ? d[k] * gs * p.xf.dz_du(z[k]) : 0.0f;
       }
-      if (row_ok) {
+      if (row < p.n_rows) {  // rows past the present ones get zeros (d = 0 there)
         __nv_bfloat16* dst = p.d + row * p.ldd + cb;
         if (nv == 32) {
           uint4* dv = reinterpret_cast<uint4*>(dst);
@@ -193,7 +197,7 @@ struct EpiDlogits {
           }
         }
       }
-      if (p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < p.n_rows) {
+      if (p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff) {
         // column sums of D over this tile's 128 rows, in a fixed order
         const float colsum = transpose_reduce32(d, lane);
         ctl->red[quarter][lane] = colsum;
@@ -213,7 +217,7 @@ struct EpiDlogits {
 struct EpiStoreRows {
   using Params = StoreRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              int row_in_tile, int, int, GemmCtl*) {
+                              bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < p.rows;
 #pragma unroll 1
@@ -221,7 +225,7 @@ struct EpiStoreRows {
       const int cb = n_tile * kBN + ch * 32;
       if (cb >= p.cols) break;
       float z[32];
-      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       if (!row_ok) continue;
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = (p.row0 + row) * p.ld + cb;
@@ -261,18 +265,23 @@ struct EpiStoreRows {
 struct EpiAccRows {
   using Params = AccRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              int row_in_tile, int, int, GemmCtl*) {
+                              bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
+    const int64_t n_eff = p.rows_dyn != nullptr ? *p.rows_dyn : p.rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
-    const bool row_ok = row < p.rows;
+    const bool row_ok = row < n_eff;
+    // accumulator rows are in the (possibly compacted) row order; the final
+    // output goes to row_map[row]
+    const int64_t out_row = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = n_tile * kBN + ch * 32;
       if (cb >= p.cols) break;
       float z[32];
-      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), z);
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       if (!row_ok) continue;
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = row * p.ld + cb;
+      const int64_t out_off = out_row * p.ld + cb;
       if (p.mode == kAccAdd || p.mode == kAccAddOut) {
         const float* src = p.acc + off;
         if (nv == 32) {
@@ -304,7 +313,7 @@ struct EpiAccRows {
             if (k < nv) dst[k] = z[k];
         }
       } else {
-        __nv_bfloat16* dst = p.out + off;
+        __nv_bfloat16* dst = p.out + out_off;
         if (nv == 32) {
           uint4* dv = reinterpret_cast<uint4*>(dst);
 #pragma unroll

@@ -77,16 +77,32 @@ struct GemmGeom {
   int m_fastest;  // 1: tile u -> (u % m_tiles, u / m_tiles); 0: n fastest
   int a_mn0, a_k0;  // A: offset along M and along K (elements / rows)
   int b_mn0, b_k0;  // B: offset along N and along K
+  // Optional device-side row count: when non-null, the M extent (axis 0) or
+  // the K extent (axis 1) is *dyn_rows rows, at most the static extent. It is
+  // read at kernel start, so the host needs no synchronisation to learn it.
+  const int32_t* dyn_rows;
+  int dyn_axis;
   int* err_word;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmGeom& g, int u, int& m, int& n) {
+__device__ __forceinline__ void tile_coords(const GemmGeom& g, int m_tiles, int u, int& m,
+                                            int& n) {
   if (g.m_fastest) {
-    m = u % g.m_tiles;
-    n = u / g.m_tiles;
+    m = u % m_tiles;
+    n = u / m_tiles;
   } else {
     n = u % g.n_tiles;
     m = u / g.n_tiles;
+  }
+}
+
+// 32 accumulator columns, or zeros when the contraction was empty (K = 0).
+__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32], bool zero) {
+  if (zero) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  } else {
+    tmem_load_32cols(taddr, v);
   }
 }
 
@@ -166,12 +182,12 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 // Epi must provide:
 //   struct Params;
 //   static __device__ void tile(const Params&, int m_block, int n_tile,
-//                               uint32_t taddr, int row_in_tile, int quarter,
-//                               int lane, GemmCtl* ctl);
+//                               uint32_t taddr, bool acc_zero, int row_in_tile,
+//                               int quarter, int lane, GemmCtl* ctl);
 // m_block indexes 128-row blocks of M (this CTA's rows are
 // m_block*128 + [0, 128)). `taddr` addresses this warp's 32 TMEM lanes at
-// column 0 of the tile's accumulator; the 128 epilogue threads may use named
-// barrier 1.
+// column 0 of the tile's accumulator (read it with load_acc(..., acc_zero));
+// the 128 epilogue threads may use named barrier 1.
 template <int CG, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -183,7 +199,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int total = g.m_tiles * g.n_tiles;
+  int m_tiles = g.m_tiles;
+  int k_iters = g.k_iters;
+  if (g.dyn_rows != nullptr) {
+    const int r = *g.dyn_rows;
+    if (g.dyn_axis == 0) {
+      const int t = (r + Cfg::kTileRows - 1) / Cfg::kTileRows;
+      m_tiles = t < m_tiles ? t : m_tiles;
+    } else {
+      const int t = (r + kBK - 1) / kBK;
+      k_iters = t < k_iters ? t : k_iters;
+    }
+  }
+  const int total = m_tiles * g.n_tiles;
   volatile int* abort_flag = &ctl->abort;
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
@@ -238,8 +266,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int u = unit0; u < total && ok; u += units) {
         int m, n;
-        tile_coords(g, u, m, n);
-        for (int k = 0; k < g.k_iters; ++k) {
+        tile_coords(g, m_tiles, u, m, n);
+        for (int k = 0; k < k_iters; ++k) {
           if (!wait_bar<CG>(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, g.err_word)) {
             ok = false;
             break;
@@ -286,7 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
-        for (int k = 0; k < g.k_iters; ++k) {
+        for (int k = 0; k < k_iters; ++k) {
           if (!wait_bar<CG>(smem_addr(&ctl->full[stage]), phase, abort_flag, g.err_word)) {
             ok = false;
             break;
@@ -341,10 +369,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!epi_all(got)) break;
       tc_fence_after_sync();
       int m, n;
-      tile_coords(g, u, m, n);
+      tile_coords(g, m_tiles, u, m, n);
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
-      Epi::tile(ep, m * CG + static_cast<int>(rank), n, taddr, row_in_tile, quarter, lane, ctl);
+      Epi::tile(ep, m * CG + static_cast<int>(rank), n, taddr, k_iters == 0, row_in_tile,
+                quarter, lane, ctl);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {

@@ -38,12 +38,13 @@ def to_dev(x: dict) -> dict:
 
 
 def run_gpu(xd: dict, w, grad_out=1.0, row_metrics=True, vocab_chunk=0,
-            grad_weight_dtype=None, backward=True):
+            grad_weight_dtype=None, backward=True, skip_ignored=False):
     """Forward (+ backward) through the C ABI; returns CPU tensors."""
     err = torch.zeros((), dtype=torch.int32, device="cuda")
     f = api.flce_forward_tensors(xd["hidden"], xd["weight"], xd["targets"], xd["bias"],
                                  w.ignore_index, w.logit_scale, w.softcap, w.reduction,
-                                 return_metrics=True, row_metrics=row_metrics, err_word=err)
+                                 return_metrics=True, row_metrics=row_metrics, err_word=err,
+                                 skip_ignored=skip_ignored)
     out = {k: (None if t is None else t.detach().cpu()) for k, t in f.items()}
     if backward:
         if w.reduction == "none":
@@ -53,7 +54,8 @@ def run_gpu(xd: dict, w, grad_out=1.0, row_metrics=True, vocab_chunk=0,
         gh, gw, gb = api.flce_backward_tensors(
             xd["hidden"], xd["weight"], xd["targets"], f["lse_rows"], f["n_valid"], go,
             xd["bias"], w.ignore_index, w.logit_scale, w.softcap, w.reduction,
-            grad_weight_dtype=grad_weight_dtype, err_word=err, vocab_chunk=vocab_chunk)
+            grad_weight_dtype=grad_weight_dtype, err_word=err, vocab_chunk=vocab_chunk,
+            skip_ignored=skip_ignored)
         out["grad_hidden"] = gh.cpu()
         out["grad_weight"] = gw.cpu()
         out["grad_bias"] = None if gb is None else gb.cpu()
@@ -97,12 +99,17 @@ def assert_grad_close(name, got, ref, tol, scale=1.0):
         assert dn <= tol["g_atol"] * math.sqrt(max(1, ref.numel())), f"{name}: expected zeros"
 
 
-def check_forward(out, ref, w, tol):
+def check_forward(out, ref, w, tol, skipped=False):
+    """``skipped``: ignored rows were left out of the contractions, so their
+    lse and entropy are not computed (NaN) and only valid rows are compared."""
     nv = ref["n_valid"]
     assert int(out["n_valid"]) == nv
     valid = ref["valid"]
     assert_rows_close("loss_rows", out["loss_rows"], ref["loss"], tol["loss_rel"])
-    assert_rows_close("lse_rows", out["lse_rows"], ref["lse"], tol["loss_rel"])
+    stat_rows = valid if skipped else None
+    assert_rows_close("lse_rows", out["lse_rows"], ref["lse"], tol["loss_rel"], stat_rows)
+    if skipped:
+        assert bool(torch.isnan(out["lse_rows"][~valid]).all())
     assert torch.all(out["loss_rows"][~valid] == 0)
     if w.reduction != "none":
         r = ref["loss_out"]
@@ -115,7 +122,8 @@ def check_forward(out, ref, w, tol):
     decisive = ref["top2_gap"] > 1e-2
     corr = out["correct_rows"].bool()
     assert torch.equal(corr[decisive], ref["correct"][decisive]), "correct_rows differ"
-    assert_rows_close("entropy_rows", out["entropy_rows"], ref["entropy"], tol["ent_rel"])
+    assert_rows_close("entropy_rows", out["entropy_rows"], ref["entropy"], tol["ent_rel"],
+                      stat_rows)
     if nv > 0:
         acc_ref = ref["mean_token_accuracy"]
         # rows with a near-tie may legitimately resolve either way

@@ -35,11 +35,12 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_matches_header():
     # int64 n,h,v; int32 dtype,has_bias; int64 ignore_index; float scale, softcap;
-    # int32 reduction, grad_weight_dtype; int64 vocab_chunk
-    assert ctypes.sizeof(abi.flce_problem) == 64
+    # int32 reduction, grad_weight_dtype; int64 vocab_chunk; int32 flags, reserved
+    assert ctypes.sizeof(abi.flce_problem) == 72
     assert abi.flce_problem.ignore_index.offset == 32
     assert abi.flce_problem.logit_scale.offset == 40
     assert abi.flce_problem.vocab_chunk.offset == 56
+    assert abi.flce_problem.flags.offset == 64
 
 
 def test_status_strings(lib):

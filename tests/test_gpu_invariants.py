@@ -59,9 +59,11 @@ def test_metrics_leave_loss_and_grads_bit_identical(dtype):
 
 
 def test_autograd_matches_raw_calls():
+    """The autograd entry point leaves ignored rows out of the GEMMs; it equals
+    the raw calls made with the same flag."""
     w = _w("bf16", reduction="sum")
     x = to_dev(make_inputs(w))
-    raw = run_gpu(x, w, grad_out=1.0)
+    raw = run_gpu(x, w, grad_out=1.0, skip_ignored=True)
     h = x["hidden"].clone().requires_grad_(True)
     wt = x["weight"].clone().requires_grad_(True)
     b = x["bias"].clone().requires_grad_(True)
@@ -96,3 +98,25 @@ def test_posterior_mass_identity():
     out = run_gpu(x, w)
     gb = out["grad_bias"].double()
     assert abs(float(gb.sum())) <= 1e-5 * float(gb.abs().sum())
+
+
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_skip_ignored_matches_all_rows(reduction):
+    """Leaving ignored rows out changes no kept row's result: loss rows, the
+    kept rows' lse and grad_hidden are bitwise identical (each row's logits
+    and gradient row do not depend on other rows); grad_weight and grad_bias
+    sum the same terms in another order."""
+    w = _w("bf16", reduction=reduction, ignore_frac=0.3)
+    x = to_dev(make_inputs(w))
+    go = torch.linspace(0.5, 1.5, w.n) if reduction == "none" else 1.0
+    a = run_gpu(x, w, grad_out=go)
+    b = run_gpu(x, w, grad_out=go, skip_ignored=True)
+    keep = x["targets"].cpu() != w.ignore_index
+    assert torch.equal(a["loss_rows"], b["loss_rows"])
+    assert torch.equal(a["lse_rows"][keep], b["lse_rows"][keep])
+    assert torch.equal(a["correct_rows"], b["correct_rows"])
+    assert torch.equal(a["metrics"], b["metrics"])
+    assert torch.equal(a["grad_hidden"], b["grad_hidden"])
+    for k in ("grad_weight", "grad_bias"):
+        d = (a[k].double() - b[k].double()).norm() / a[k].double().norm()
+        assert float(d) < 1e-2, (k, float(d))

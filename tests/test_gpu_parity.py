@@ -48,15 +48,16 @@ def _grad_out(w, n):
     return 0.75
 
 
-def _check_case(w, vocab_chunk=0, grad_weight_dtype=None):
+def _check_case(w, vocab_chunk=0, grad_weight_dtype=None, skip_ignored=False):
     x = make_inputs(w)
     go = _grad_out(w, w.n)
     out = run_gpu(to_dev(x), w, grad_out=go.float() if torch.is_tensor(go) else go,
-                  vocab_chunk=vocab_chunk, grad_weight_dtype=grad_weight_dtype)
+                  vocab_chunk=vocab_chunk, grad_weight_dtype=grad_weight_dtype,
+                  skip_ignored=skip_ignored)
     assert out["err_word"] == 0
     ref = oracle.forward(*oracle_args(x, w))
     tol = TOL[w.dtype]
-    check_forward(out, ref, w, tol)
+    check_forward(out, ref, w, tol, skipped=skip_ignored and w.dtype == "bf16")
     gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"])
     check_backward(out, gref, tol, x["bias"] is not None, grad_scale(w.reduction, ref["n_valid"]))
 
@@ -149,3 +150,36 @@ def test_target_out_of_range(dtype):
     assert float(d.max()) <= tol["loss_rel"] * max(1.0, float(ref["loss"][ok].abs().max()))
     gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"])
     check_backward(out, gref, tol, False, grad_scale("sum", ref["n_valid"]))
+
+
+SKIP_CASES = [
+    _case("skip_tails_cap_sum", 300, 136, 1000, bias_var=0.02, softcap=30.0, logit_scale=0.5,
+          hidden_var=2.0, ignore_frac=0.3, reduction="sum"),
+    _case("skip_none_4097", 4097, 512, 4096, ignore_frac=0.1, reduction="none"),
+    _case("skip_zipf_bias", 640, 192, 5000, bias_var=0.02, targets="zipf", ignore_frac=0.45),
+    _case("skip_most_ignored", 900, 256, 3000, ignore_frac=0.97, bias_var=0.02),
+    _case("skip_none_ignored", 520, 128, 2000, ignore_frac=0.0),
+]
+
+
+@pytest.mark.parametrize("w", SKIP_CASES, ids=[w.name for w in SKIP_CASES])
+def test_parity_skip_ignored(w):
+    """Ignored rows left out of every contraction (FLCE_SKIP_IGNORED_ROWS):
+    same loss, metrics and gradients as the oracle; the kept rows' lse."""
+    _check_case(w, skip_ignored=True)
+
+
+def test_parity_skip_ignored_multi_chunk():
+    w = _case("skip_chunked", 777, 200, 5000, bias_var=0.02, softcap=20.0, ignore_frac=0.3)
+    _check_case(w, vocab_chunk=1024, skip_ignored=True)
+
+
+def test_skip_ignored_all_rows_ignored():
+    w = _case("skip_all_ignored", 300, 64, 700, bias_var=0.02, ignore_frac=1.0)
+    x = make_inputs(w)
+    out = run_gpu(to_dev(x), w, skip_ignored=True)
+    assert int(out["n_valid"]) == 0
+    assert math.isnan(float(out["loss"]))
+    assert torch.all(out["loss_rows"] == 0)
+    for k in ("grad_hidden", "grad_weight", "grad_bias"):
+        assert torch.count_nonzero(out[k]) == 0, k
