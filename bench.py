@@ -74,6 +74,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def workload_of(args):
+    """The workload, with the --dtype / --forward-only variants applied."""
+    w = WORKLOADS[args.workload]
+    if args.dtype is not None:
+        w = w.with_shape(dtype=args.dtype)
+    if args.forward_only and w.name == "long_bf16":
+        w = w.with_shape(reduction="none")  # this workload's forward-only phase
+    return w
+
+
 def describe(w) -> str:
     parts = [f"{w.name}: N={w.n} H={w.h} V={w.v} {w.dtype}",
              "bias" if w.bias_var is not None else "no bias",
@@ -141,16 +151,18 @@ class ClockSampler:
 class Step:
     """Preallocated buffers and the two C-ABI calls of one fwd+bwd step."""
 
-    def __init__(self, x: dict, w, dev, skip_ignored: bool = True):
+    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False):
         from linear_cross_entropy_vocab_gb300 import abi
 
         self.abi = abi
         self.x = x
         self.w = w
+        self.forward_only = forward_only
         n, h = x["hidden"].shape
         v = x["weight"].shape[0]
-        self.prob = abi.make_problem(n, h, v, abi.FLCE_BF16 if x["hidden"].dtype == torch.bfloat16
-                                     else abi.FLCE_F32, x["bias"] is not None, w.ignore_index,
+        code = {torch.bfloat16: abi.FLCE_BF16, torch.float16: abi.FLCE_F16,
+                torch.float32: abi.FLCE_F32}[x["hidden"].dtype]
+        self.prob = abi.make_problem(n, h, v, code, x["bias"] is not None, w.ignore_index,
                                      w.logit_scale, w.softcap, w.reduction,
                                      skip_ignored=skip_ignored)
         f32 = dict(dtype=torch.float32, device=dev)
@@ -178,9 +190,12 @@ class Step:
     def __call__(self, stream):
         a, x, p = self.abi, self.x, lambda t: None if t is None else t.data_ptr()
         a.flce_forward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]), p(x["targets"]),
-                       p(self.loss_rows), p(self.lse_rows), None, None, p(self.loss),
+                       p(self.loss_rows), p(self.lse_rows), None, None,
+                       None if self.w.reduction == "none" else p(self.loss),
                        p(self.metrics), p(self.n_valid), p(self.err), p(self.ws), self.ws_f,
                        stream)
+        if self.forward_only:
+            return
         a.flce_backward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]),
                         p(x["targets"]), p(self.lse_rows), p(self.n_valid), p(self.grad_out),
                         p(self.gh), p(self.gw), p(self.gb), p(self.err), p(self.ws), self.ws_b,
@@ -191,12 +206,12 @@ def bench_ours(args, rank, world, dev):
     from linear_cross_entropy_vocab_gb300 import abi, api, native_build
 
     native_build.build()
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     xc = make_inputs(w)
     x = {k: (None if t is None else t.to(dev)) for k, t in xc.items()}
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    step = Step(x, w, dev, skip_ignored=not args.all_rows)
+    step = Step(x, w, dev, skip_ignored=not args.all_rows, forward_only=args.forward_only)
     n, h, v = w.n, w.h, w.v
 
     def barrier():
@@ -306,7 +321,7 @@ def bench_ours(args, rank, world, dev):
     del hh, ww, loss, _m
 
     peaks, peak_src = load_peaks()
-    flops_step = gemm_flops(n, h, v)
+    flops_step = gemm_flops(n, h, v) / (4.0 if args.forward_only else 1.0)
     sec = ms / 1e3
     tok_s = world * n * args.steps / sec
     n_valid = int(step.n_valid.item())
@@ -345,13 +360,14 @@ def bench_ours(args, rank, world, dev):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": w.dtype,
         "data": "synthetic, seeded (distributions as in the workload description)",
         "config": {"workload": describe(w),
                    "global_batch": n * world, "seq_len": None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weight 1.05 GB), no flush",
-                   "skip_ignored_rows": not args.all_rows},
+                   "skip_ignored_rows": not args.all_rows,
+                   "step": "forward only" if args.forward_only else "forward+backward"},
         "tensor_peak_frac": {
             "achieved_tflops": round(achieved_step, 1),
             "of_burst": round(achieved_step / peaks["bf16_tflops"], 4),
@@ -441,6 +457,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default=None,
+                    help="run the workload with this input type (default: the workload's)")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time flce_forward alone (the long workload uses reduction none)")
     ap.add_argument("--all-rows", action="store_true",
                     help="run ignored rows through the GEMMs too (FLCE_SKIP_IGNORED_ROWS off)")
     args = ap.parse_args()
@@ -461,8 +481,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     out = bench_ours(args, rank, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(make_inputs(WORKLOADS[args.workload]),
-                                           WORKLOADS[args.workload])
+        w = workload_of(args)
+        out["cpu_baseline"] = cpu_baseline(make_inputs(w), w)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -34,9 +34,12 @@
  *     default stream) and the call returns before the work completes.
  *   - Tensors are dense row-major: hidden [N,H], weight [V,H], bias [V],
  *     targets int64 [N]. hidden, weight and bias share `p->dtype`.
- *   - FLCE_BF16 needs H % 8 == 0 and 16-byte aligned hidden/weight pointers
- *     (tensor-memory-accelerator row pitch rule); FLCE_F32 needs 4-byte
- *     alignment. Violations return FLCE_ERR_UNSUPPORTED before any launch.
+ *   - FLCE_BF16 and FLCE_F16 need H % 8 == 0 and 16-byte aligned
+ *     hidden/weight/bias pointers (tensor-memory-accelerator row pitch rule);
+ *     FLCE_F32 needs 4-byte alignment. Violations return FLCE_ERR_UNSUPPORTED
+ *     before any launch.
+ *   - Dtypes: FLCE_BF16 and FLCE_F16 run on the tensor cores (bf16 or fp16
+ *     products, fp32 accumulation); FLCE_F32 runs fp32 FFMA kernels.
  *   - Argument errors are detected on the host, before any launch, and
  *     return a non-OK status; flce_last_error() then describes the problem.
  *     A failed launch returns FLCE_ERR_CUDA.
@@ -68,7 +71,7 @@ typedef enum flce_status {
   FLCE_ERR_DEVICE_TIMEOUT = 5 /* reserved for callers that translate FLCE_DEVERR_TIMEOUT */
 } flce_status;
 
-typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1 } flce_dtype;
+typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1, FLCE_F16 = 2 } flce_dtype;
 
 typedef enum flce_reduction {
   FLCE_RED_NONE = 0,
@@ -109,8 +112,8 @@ typedef struct flce_problem {
   int32_t reserved;
 } flce_problem;
 
-/* Leave rows whose target is ignore_index out of every contraction (bf16 path;
- * the fp32 path computes every row either way). The non-ignored rows are
+/* Leave rows whose target is ignore_index out of every contraction (bf16 and
+ * fp16 paths; the fp32 path computes every row either way). The non-ignored rows are
  * gathered, in their original order, into the workspace, and the GEMMs run
  * over them alone: ignored rows contribute nothing to the loss or to any
  * gradient, so their logits are never needed. Loss, metrics and gradients are
@@ -177,10 +180,10 @@ flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden,
                                  int32_t* err_word, void* stream);
 
 /* Bytes of device workspace flce_backward() needs for `p` (0 if invalid):
- * the dlogits buffer of one vocabulary chunk (N x chunk, in bf16 for FLCE_BF16
- * and fp32 for FLCE_F32), an fp32 [N,H] grad_hidden accumulator when there is
- * more than one chunk and dtype is bf16, and fp32 grad_bias partial sums when
- * has_bias. */
+ * the dlogits buffer of one vocabulary chunk (N x chunk, in the input type for
+ * FLCE_BF16 / FLCE_F16 and fp32 for FLCE_F32), an fp32 [N,H] grad_hidden
+ * accumulator when there is more than one chunk on the tensor-core path, and
+ * fp32 grad_bias partial sums when has_bias. */
 size_t flce_backward_workspace_size(const flce_problem* p);
 
 /* Backward pass: all three gradients. Cite: §Algorithm (backward: recompute

@@ -23,6 +23,7 @@ FLCE_ERR_DEVICE_TIMEOUT = 5
 
 FLCE_F32 = 0
 FLCE_BF16 = 1
+FLCE_F16 = 2
 
 FLCE_RED_NONE = 0
 FLCE_RED_SUM = 1

@@ -28,7 +28,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return abi.FLCE_F32
     if t.dtype == torch.bfloat16:
         return abi.FLCE_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return abi.FLCE_F16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32, bfloat16 or float16")
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -82,7 +82,10 @@ EncodeFn encoder() {
   return g_encode;
 }
 
-// 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box
+thread_local CUtensorMapDataType g_map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+// 2-D tensor of 16-bit elements (of type g_map_type: the input type of the
+// current call) [outer][inner] with row pitch `pitch_elems`, box
 // {box_inner, box_outer}, 128-byte swizzle, zero fill out of bounds.
 // On failure records the driver's result in the thread's error text.
 bool make_map(CUtensorMap* map, const char* what, const void* base, int64_t inner,
@@ -97,7 +100,7 @@ bool make_map(CUtensorMap* map, const char* what, const void* base, int64_t inne
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
-      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+      enc(map, g_map_type, 2, const_cast<void*>(base), dims, strides, box,
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -180,15 +183,18 @@ struct FwdPlan {
 
 struct BwdPlan {
   int64_t chunk = 0, n_chunks = 0, gb_parts = 0;
-  size_t d = 0, acc = 0, gb = 0, total = 0;
+  size_t d = 0, acc = 0, gb = 0, scales = 0, total = 0;
   bool use_acc = false;
   CompactPlan cp;
 };
 
-bool is_bf16(const flce_problem* p) { return p->dtype == FLCE_BF16; }
+// bf16 and fp16 inputs run on the tensor cores; fp32 on FFMA kernels.
+bool is_tc(const flce_problem* p) { return p->dtype == FLCE_BF16 || p->dtype == FLCE_F16; }
+
+int tc_type(const flce_problem* p) { return p->dtype == FLCE_F16 ? flce::kTcF16 : flce::kTcBF16; }
 
 bool skips_ignored(const flce_problem* p) {
-  return is_bf16(p) && (p->flags & FLCE_SKIP_IGNORED_ROWS) != 0;
+  return is_tc(p) && (p->flags & FLCE_SKIP_IGNORED_ROWS) != 0;
 }
 
 // Appends the compaction items at `off`; returns the new end.
@@ -221,8 +227,8 @@ flce_status check_problem(const flce_problem* p) {
   const int64_t lim = int64_t(1) << 30;
   if (p->n >= lim || p->h >= lim || p->v >= lim)
     return fail(FLCE_ERR_UNSUPPORTED, "n, h and v must each be below 2^30");
-  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16)
-    return fail(FLCE_ERR_INVALID_ARG, "dtype must be FLCE_F32 or FLCE_BF16");
+  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16 && p->dtype != FLCE_F16)
+    return fail(FLCE_ERR_INVALID_ARG, "dtype must be FLCE_F32, FLCE_BF16 or FLCE_F16");
   if (p->has_bias != 0 && p->has_bias != 1)
     return fail(FLCE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
   if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_MEAN)
@@ -236,10 +242,10 @@ flce_status check_problem(const flce_problem* p) {
   if (p->vocab_chunk < 0) return fail(FLCE_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
   if ((p->flags & ~FLCE_SKIP_IGNORED_ROWS) != 0 || p->reserved != 0)
     return fail(FLCE_ERR_INVALID_ARG, "unknown flags or non-zero reserved field");
-  if (is_bf16(p) && p->h % 8 != 0)
-    return fail(FLCE_ERR_UNSUPPORTED, "bf16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld",
-                (long long)p->h);
-  if (is_bf16(p)) {
+  if (is_tc(p) && p->h % 8 != 0)
+    return fail(FLCE_ERR_UNSUPPORTED,
+                "bf16/fp16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld", (long long)p->h);
+  if (is_tc(p)) {
     const int64_t m_tiles = cdiv(p->n, flce::kBM), n_tiles = cdiv(p->v, flce::kBM);
     if (m_tiles * n_tiles >= (int64_t(1) << 31))
       return fail(FLCE_ERR_UNSUPPORTED, "too many tiles");
@@ -251,7 +257,7 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 
 FwdPlan plan_forward(const flce_problem* p) {
   FwdPlan f;
-  f.n_vt = cdiv(p->v, is_bf16(p) ? flce::kBN : flce::kSimtTileV);
+  f.n_vt = cdiv(p->v, is_tc(p) ? flce::kBN : flce::kSimtTileV);
   size_t off = 0;
   f.partials = off;
   off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 16);
@@ -268,7 +274,7 @@ FwdPlan plan_forward(const flce_problem* p) {
 
 BwdPlan plan_backward(const flce_problem* p) {
   BwdPlan b;
-  const int64_t elem = is_bf16(p) ? 2 : 4;
+  const int64_t elem = is_tc(p) ? 2 : 4;
   const int64_t v_round = cdiv(p->v, 256) * 256;
   int64_t c = p->vocab_chunk;
   if (c > 0) {
@@ -281,8 +287,8 @@ BwdPlan plan_backward(const flce_problem* p) {
   if (c > v_round) c = v_round;
   b.chunk = c;
   b.n_chunks = cdiv(p->v, c);
-  b.use_acc = is_bf16(p) && b.n_chunks > 1;
-  b.gb_parts = p->has_bias ? cdiv(p->n, is_bf16(p) ? flce::kBM : flce::kSimtTileN) : 0;
+  b.use_acc = is_tc(p) && b.n_chunks > 1;
+  b.gb_parts = p->has_bias ? cdiv(p->n, is_tc(p) ? flce::kBM : flce::kSimtTileN) : 0;
   size_t off = 0;
   b.d = off;
   off = align_up(off + static_cast<size_t>(p->n) * c * elem);
@@ -290,6 +296,8 @@ BwdPlan plan_backward(const flce_problem* p) {
   if (b.use_acc) off = align_up(off + static_cast<size_t>(p->n) * p->h * 4);
   b.gb = off;
   if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
+  b.scales = off;
+  if (p->dtype == FLCE_F16) off = align_up(off + 2 * sizeof(float));
   off = plan_compaction(p, true, off, &b.cp);
   b.total = off;
   return b;
@@ -447,8 +455,10 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
   g_err[0] = 0;
   flce_status st = check_problem(p);
   if (st != FLCE_OK) return st;
-  const bool bf16 = is_bf16(p);
+  const bool bf16 = is_tc(p);  // tensor-core path (bf16 or fp16)
   const size_t in_align = bf16 ? 16 : 4;
+  g_map_type = p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (weight == nullptr) return fail(FLCE_ERR_INVALID_ARG, "weight is NULL");
   if (n_valid == nullptr) return fail(FLCE_ERR_INVALID_ARG, "n_valid is NULL");
   if (p->reduction != FLCE_RED_NONE && loss_out == nullptr)
@@ -502,13 +512,13 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       cp.correct_rows = correct_rows;
       cp.entropy_rows = entropy_rows;
       flce::GatherParams gp{};
-      gp.hidden = static_cast<const __nv_bfloat16*>(hidden);
+      gp.hidden = hidden;
       gp.n = p->n;
       gp.h = p->h;
       gp.row_map = row_map;
       gp.n_kept = n_kept;
       gp.pad_rows = flce::kTileRowsTC;
-      gp.hidden_c = reinterpret_cast<__nv_bfloat16*>(ws + plan.cp.hidden_c);
+      gp.hidden_c = ws + plan.cp.hidden_c;
       gp.targets = targets;
       gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
       gp.ignore_index = p->ignore_index;
@@ -539,7 +549,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       g.dyn_axis = 0;
       g.err_word = err_word;
       flce::FwdStatsParams fp{};
-      fp.bias = static_cast<const __nv_bfloat16*>(bias);
+      fp.bias = bias;
       fp.targets = rows_targets;
       fp.partials = partials;
       fp.zt = zt;
@@ -549,7 +559,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.n_vt = plan.n_vt;
       fp.xf = xf;
       ProfScope ps("fwd_stats", s);
-      e = flce::launch_tc_fwd_stats(tm_h, tm_w, g, fp, dev.sms, s);
+      e = flce::launch_tc_fwd_stats(tc_type(p), tm_h, tm_w, g, fp, dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
     } else {
       flce::SimtFwdParams fp{};
@@ -618,8 +628,10 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   g_err[0] = 0;
   flce_status st = check_problem(p);
   if (st != FLCE_OK) return st;
-  const bool bf16 = is_bf16(p);
+  const bool bf16 = is_tc(p);  // tensor-core path (bf16 or fp16)
   const size_t in_align = bf16 ? 16 : 4;
+  g_map_type = p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (weight == nullptr || grad_weight == nullptr)
     return fail(FLCE_ERR_INVALID_ARG, "weight and grad_weight are required");
   if (p->has_bias && (bias == nullptr || grad_bias == nullptr))
@@ -661,8 +673,17 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   float* gb_partial = p->has_bias ? reinterpret_cast<float*>(ws + plan.gb) : nullptr;
 
   if (bf16) {
-    __nv_bfloat16* dbuf = reinterpret_cast<__nv_bfloat16*>(ws + plan.d);
+    void* dbuf = ws + plan.d;
     float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
+    const int type = tc_type(p);
+    // fp16: D is stored times a power of two, undone by the gradient GEMMs
+    float* scales = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + plan.scales) : nullptr;
+    if (scales != nullptr) {
+      ProfScope ps("dlogits_scale", s);
+      e = flce::launch_dlogits_scale(grad_out, n_valid, targets, p->n, p->ignore_index,
+                                     p->reduction, p->logit_scale, scales, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits scale kernel");
+    }
     // valid-row compaction: rows of hidden, targets, lse and per-row
     // upstream gradients are gathered; grad_hidden is scattered back
     const bool compact = plan.cp.on;
@@ -680,13 +701,13 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       cp.row_map = row_map;
       cp.n_kept = n_kept;
       flce::GatherParams gp{};
-      gp.hidden = static_cast<const __nv_bfloat16*>(hidden);
+      gp.hidden = hidden;
       gp.n = p->n;
       gp.h = p->h;
       gp.row_map = row_map;
       gp.n_kept = n_kept;
       gp.pad_rows = flce::kTileRowsTC;
-      gp.hidden_c = reinterpret_cast<__nv_bfloat16*>(ws + plan.cp.hidden_c);
+      gp.hidden_c = ws + plan.cp.hidden_c;
       gp.targets = targets;
       gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
       gp.ignore_index = p->ignore_index;
@@ -708,8 +729,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
       {
         ProfScope ps("zero_ignored_rows", s);
-        e = flce::launch_zero_ignored_rows(targets, p->n, p->ignore_index,
-                                           static_cast<__nv_bfloat16*>(grad_hidden), p->h, s);
+        e = flce::launch_zero_ignored_rows(targets, p->n, p->ignore_index, grad_hidden, p->h,
+                                           s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "grad_hidden zero kernel");
       rows_src = gp.hidden_c;
@@ -743,13 +764,14 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g1.dyn_axis = 0;
       g1.err_word = err_word;
       flce::DlogitsParams dp{};
-      dp.bias = static_cast<const __nv_bfloat16*>(bias);
+      dp.bias = bias;
       dp.targets = rows_targets;
       dp.lse = rows_lse;
       dp.grad_out = rows_grad;
       dp.n_valid = n_valid;
       dp.d = dbuf;
       dp.ldd = plan.chunk;
+      dp.dscale = scales;
       dp.gb_partial = gb_partial;
       dp.gb_ld = p->v;
       dp.n_rows = p->n;
@@ -762,7 +784,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.xf = xf;
       {
         ProfScope ps("bwd_dlogits", s);
-        e = flce::launch_tc_dlogits(tm_h_k, tm_w_k, g1, dp, dev.sms, s);
+        e = flce::launch_tc_dlogits(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
 
@@ -778,13 +800,14 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       flce::StoreRowsParams sp{};
       sp.out = grad_weight;
       sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
+      sp.out_scale = scales != nullptr ? scales + 1 : nullptr;
       sp.ld = p->h;
       sp.rows = width;
       sp.row0 = c0;
       sp.cols = static_cast<int>(p->h);
       {
         ProfScope ps("bwd_grad_weight", s);
-        e = flce::launch_tc_grad_weight(tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
+        e = flce::launch_tc_grad_weight(type, tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
 
@@ -800,7 +823,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g3.err_word = err_word;
       flce::AccRowsParams ap{};
       ap.acc = acc;
-      ap.out = static_cast<__nv_bfloat16*>(grad_hidden);
+      ap.out = grad_hidden;
+      ap.out_scale = scales != nullptr ? scales + 1 : nullptr;
       if (plan.n_chunks == 1)
         ap.mode = flce::kAccStoreOut;
       else if (c == 0)
@@ -816,7 +840,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       ap.cols = static_cast<int>(p->h);
       {
         ProfScope ps("bwd_grad_hidden", s);
-        e = flce::launch_tc_grad_hidden(tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
+        e = flce::launch_tc_grad_hidden(type, tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
     }
@@ -872,8 +896,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
     ProfScope ps("bwd_bias_reduce", s);
     const int32_t* n_dyn =
         plan.cp.on ? reinterpret_cast<const int32_t*>(ws + plan.cp.n_kept) : nullptr;
-    e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias, bf16 ? 1 : 0,
-                                 n_dyn, flce::kBM, s);
+    e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias,
+                                 bf16 ? tc_type(p) : 0, n_dyn, flce::kBM, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
   }
   return FLCE_OK;

@@ -25,8 +25,11 @@ constexpr int kBLoadRowsTC = kBN / kPairCG;
 constexpr int kSimtTileV = 128;
 constexpr int kSimtTileN = 32;
 
+// Input element types of the tensor-core path (FLCE_BF16, FLCE_F16).
+enum TcType { kTcBF16 = 1, kTcF16 = 2 };
+
 struct FwdStatsParams {
-  const __nv_bfloat16* bias;  // [V] or null
+  const void* bias;           // [V] in the input type, or null
   const int64_t* targets;     // [N]
   float4* partials;           // [N][n_vt] (m, s, t, argmax)
   float* zt;                  // [N] target logit
@@ -38,13 +41,14 @@ struct FwdStatsParams {
 };
 
 struct DlogitsParams {
-  const __nv_bfloat16* bias;
+  const void* bias;
   const int64_t* targets;
   const float* lse;
   const float* grad_out;
   const int32_t* n_valid;
-  __nv_bfloat16* d;  // [N][ldd] dlogits of this chunk
+  void* d;  // [N][ldd] dlogits of this chunk, input type, times *dscale
   int64_t ldd;
+  const float* dscale;  // device scalar multiplying the stored D, or null (1)
   float* gb_partial;  // [m_tiles][gb_ld] or null
   int64_t gb_ld;
   int64_t n_rows;             // rows of the buffers
@@ -58,8 +62,9 @@ struct DlogitsParams {
 };
 
 struct StoreRowsParams {
-  void* out;
+  void* out;  // input type, or fp32 when out_f32
   int out_f32;
+  const float* out_scale;  // device scalar multiplying the results, or null (1)
   int64_t ld;
   int64_t rows;
   int64_t row0;
@@ -70,7 +75,8 @@ enum AccMode { kAccStore = 0, kAccAdd = 1, kAccAddOut = 2, kAccStoreOut = 3 };
 
 struct AccRowsParams {
   float* acc;
-  __nv_bfloat16* out;
+  void* out;  // input type
+  const float* out_scale;  // device scalar multiplying the results, or null (1)
   int mode;
   int64_t ld;
   int64_t rows;
@@ -80,17 +86,29 @@ struct AccRowsParams {
 };
 
 // ---------------------------------------------------------------- launchers
-cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                                const GemmGeom& g, const FwdStatsParams& p, int sms,
-                                cudaStream_t s);
-cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                              const GemmGeom& g, const DlogitsParams& p, int sms, cudaStream_t s);
-cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
-                                  const GemmGeom& g, const StoreRowsParams& p, int sms,
-                                  cudaStream_t s);
-cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
-                                  const GemmGeom& g, const AccRowsParams& p, int sms,
-                                  cudaStream_t s);
+// `type` is a TcType; every launcher runs the CTA-pair GEMM of that type.
+cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
+                                const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                                const FwdStatsParams& p, int sms, cudaStream_t s);
+cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
+                              const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                              const DlogitsParams& p, int sms, cudaStream_t s);
+cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,
+                                  const CUtensorMap& tm_hidden_mn, const GemmGeom& g,
+                                  const StoreRowsParams& p, int sms, cudaStream_t s);
+cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
+                                  const CUtensorMap& tm_weight_mn, const GemmGeom& g,
+                                  const AccRowsParams& p, int sms, cudaStream_t s);
+
+// fp16 backward: D is stored as D * dscale with dscale = 2^k chosen so that
+// |D * dscale| < 16384 (the row upstream gradient times logit_scale bounds
+// |D|; fp16's largest finite value is 65504) and entries down to ~1e-8 of
+// the largest stay normal; out_scale = 1 / dscale exactly. Writes both to
+// `scales` [2].
+cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
+                                 const int64_t* targets, int64_t n, int64_t ignore_index,
+                                 int reduction, float logit_scale, float* scales,
+                                 cudaStream_t s);
 
 // fp32 (SIMT) path
 struct SimtFwdParams {
@@ -160,10 +178,11 @@ struct FinalizeParams {
 };
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 
-// out[j] = sum_{r < n_parts} part[r*ld + j] (fixed order), cast to bf16 or f32.
+// out[j] = sum_{r < n_parts} part[r*ld + j] (fixed order), cast to the output
+// type (out_type: 0 fp32, 1 bf16, 2 fp16).
 // With n_dyn, n_parts = ceil(*n_dyn / rows_per_part) (at most the static one).
 cudaError_t launch_bias_reduce(const float* part, int64_t n_parts, int64_t ld, int64_t v,
-                               void* out, int out_bf16, const int32_t* n_dyn,
+                               void* out, int out_type, const int32_t* n_dyn,
                                int rows_per_part, cudaStream_t s);
 
 // ---- valid-row compaction (FLCE_SKIP_IGNORED_ROWS)
@@ -183,12 +202,12 @@ struct CompactParams {
 cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t s);
 
 struct GatherParams {
-  const __nv_bfloat16* hidden;
+  const void* hidden;  // 16-bit elements
   int64_t n, h;
   const int32_t* row_map;
   const int32_t* n_kept;
   int pad_rows;  // rows [n_kept, roundup(n_kept, pad_rows)) are zero-filled
-  __nv_bfloat16* hidden_c;
+  void* hidden_c;
   const int64_t* targets;
   int64_t* targets_c;
   int64_t ignore_index;
@@ -199,9 +218,9 @@ struct GatherParams {
 };
 cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s);
 
-// grad_hidden rows of ignored targets := 0 (bf16 [N, h]).
+// grad_hidden rows of ignored targets := 0 (16-bit elements, [N, h]).
 cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,
-                                     __nv_bfloat16* out, int64_t h, cudaStream_t s);
+                                     void* out, int64_t h, cudaStream_t s);
 
 
 }  // namespace flce

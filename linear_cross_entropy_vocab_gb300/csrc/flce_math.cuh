@@ -20,6 +20,7 @@
 #include <cfloat>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "tc_ptx.cuh"
 
@@ -143,5 +144,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+
+// The 16-bit input types: conversion and the tcgen05 operand-format code.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr uint32_t kFormat = 1;
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    return pack_bf16x2(lo, hi);
+  }
+  __device__ __forceinline__ static __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
+  __device__ __forceinline__ static float lo(uint32_t w) {
+    return __low2float(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+  __device__ __forceinline__ static float hi(uint32_t w) {
+    return __high2float(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+  __device__ __forceinline__ static float to(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr uint32_t kFormat = 0;
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static __half from(float x) { return __float2half_rn(x); }
+  __device__ __forceinline__ static float lo(uint32_t w) {
+    return __low2float(*reinterpret_cast<const __half2*>(&w));
+  }
+  __device__ __forceinline__ static float hi(uint32_t w) {
+    return __high2float(*reinterpret_cast<const __half2*>(&w));
+  }
+  __device__ __forceinline__ static float to(__half x) { return __half2float(x); }
+};
 
 }  // namespace flce

@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "flce_internal.h"
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 
 __global__ void __launch_bounds__(256)
     bias_reduce_kernel(const float* __restrict__ part, int64_t n_parts, int64_t ld, int64_t v,
-                       void* out, int out_bf16, const int32_t* n_dyn, int rows_per_part) {
+                       void* out, int out_type, const int32_t* n_dyn, int rows_per_part) {
   const int64_t j = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   if (j >= v) return;
   if (n_dyn != nullptr) {
@@ -114,11 +115,53 @@ __global__ void __launch_bounds__(256)
   }
   float acc = 0.0f;
   for (int64_t r = 0; r < n_parts; ++r) acc += part[r * ld + j];
-  if (out_bf16) {
+  if (out_type == kTcBF16) {
     static_cast<__nv_bfloat16*>(out)[j] = __float2bfloat16_rn(acc);
+  } else if (out_type == kTcF16) {
+    static_cast<__half*>(out)[j] = __float2half_rn(acc);
   } else {
     static_cast<float*>(out)[j] = acc;
   }
+}
+
+// scales[0] = 2^k with |g_ref * logit_scale * 2^k| in [8192, 16384), scales[1]
+// = 2^-k; g_ref is the largest row upstream gradient (grad_out/n_valid,
+// grad_out, or max |grad_out[i]| over non-ignored rows). 1 and 1 when g_ref
+// is zero or not finite.
+__global__ void __launch_bounds__(1024)
+    dlogits_scale_kernel(const float* grad_out, const int32_t* n_valid, const int64_t* targets,
+                         int64_t n, int64_t ignore_index, int reduction, float logit_scale,
+                         float* scales) {
+  __shared__ float red[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float g = 0.0f;
+  if (reduction == 0) {
+    for (int64_t i = tid; i < n; i += 1024)
+      if (targets[i] != ignore_index) g = fmaxf(g, fabsf(grad_out[i]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, off));
+    if (lane == 0) red[warp] = g;
+    __syncthreads();
+    if (warp == 0) {
+      g = red[lane];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, off));
+    }
+  } else if (tid == 0) {
+    g = fabsf(grad_out[0]);
+    if (reduction == 2) g = n_valid[0] > 0 ? g / static_cast<float>(n_valid[0]) : 0.0f;
+  }
+  if (tid != 0) return;
+  const float gs = g * fabsf(logit_scale);
+  float up = 1.0f, down = 1.0f;
+  if (gs > 0.0f && isfinite(gs)) {
+    int e = 0;
+    frexpf(gs, &e);  // gs in [2^(e-1), 2^e)
+    up = ldexpf(1.0f, 14 - e);
+    down = ldexpf(1.0f, e - 14);
+  }
+  scales[0] = up;
+  scales[1] = down;
 }
 
 // Stable compaction of the rows whose target is not ignore_index: one block
@@ -178,11 +221,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
   const int64_t kept = *p.n_kept;
   const int64_t pad = (kept + p.pad_rows - 1) / p.pad_rows * p.pad_rows;
   if (j >= pad || j >= p.n) return;
-  const int64_t vecs = p.h / 8;  // 8 bf16 per 16-byte vector (h % 8 == 0)
-  uint4* dst = reinterpret_cast<uint4*>(p.hidden_c + j * p.h);
+  const int64_t vecs = p.h / 8;  // 8 16-bit elements per 16-byte vector (h % 8 == 0)
+  uint4* dst = reinterpret_cast<uint4*>(p.hidden_c) + j * vecs;
   if (j < kept) {
     const int64_t src_row = p.row_map[j];
-    const uint4* src = reinterpret_cast<const uint4*>(p.hidden + src_row * p.h);
+    const uint4* src = reinterpret_cast<const uint4*>(p.hidden) + src_row * vecs;
     for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = __ldg(src + q);
     if (threadIdx.x == 0) {
       p.targets_c[j] = p.targets[src_row];
@@ -201,10 +244,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
 
 __global__ void __launch_bounds__(kGatherThreads)
     zero_ignored_rows_kernel(const int64_t* __restrict__ targets, int64_t ignore_index,
-                             __nv_bfloat16* out, int64_t h) {
+                             void* out, int64_t h) {
   const int64_t i = blockIdx.x;
   if (targets[i] != ignore_index) return;
-  uint4* dst = reinterpret_cast<uint4*>(out + i * h);
+  uint4* dst = reinterpret_cast<uint4*>(out) + i * (h / 8);
   for (int64_t q = threadIdx.x; q < h / 8; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
 }
 
@@ -221,8 +264,17 @@ cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
+                                 const int64_t* targets, int64_t n, int64_t ignore_index,
+                                 int reduction, float logit_scale, float* scales,
+                                 cudaStream_t s) {
+  dlogits_scale_kernel<<<1, 1024, 0, s>>>(grad_out, n_valid, targets, n, ignore_index, reduction,
+                                          logit_scale, scales);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,
-                                     __nv_bfloat16* out, int64_t h, cudaStream_t s) {
+                                     void* out, int64_t h, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   zero_ignored_rows_kernel<<<static_cast<unsigned>(n), kGatherThreads, 0, s>>>(targets,
                                                                                 ignore_index, out, h);
@@ -241,10 +293,10 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_bias_reduce(const float* part, int64_t n_parts, int64_t ld, int64_t v,
-                               void* out, int out_bf16, const int32_t* n_dyn,
+                               void* out, int out_type, const int32_t* n_dyn,
                                int rows_per_part, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>((v + 255) / 256);
-  bias_reduce_kernel<<<grid, 256, 0, s>>>(part, n_parts, ld, v, out, out_bf16, n_dyn,
+  bias_reduce_kernel<<<grid, 256, 0, s>>>(part, n_parts, ld, v, out, out_type, n_dyn,
                                           rows_per_part);
   return cudaGetLastError();
 }

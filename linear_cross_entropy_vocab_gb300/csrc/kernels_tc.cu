@@ -10,7 +10,11 @@
 //   grad_weight grad_W[chunk] = D^T @ hidden (K = tokens, fp32 in TMEM,
 //               written once).
 //   grad_hidden grad_h += D @ W[chunk] (K = chunk width), accumulated in an
-//               fp32 buffer across chunks; the last chunk writes bf16.
+//               fp32 buffer across chunks; the last chunk writes the input type.
+// Each is instantiated for bf16 and for fp16 inputs (tcgen05 kind::f16 takes
+// both, with A and B of one type). For fp16, D is stored scaled by a power of
+// two so that its small entries stay in fp16's normal range; the two gradient
+// GEMMs undo the scale in their epilogues.
 #include <cfloat>
 #include <cstdint>
 #include <cuda.h>
@@ -26,8 +30,10 @@ namespace flce {
 namespace {
 
 // 32 bias values of columns [c, c+32) (fewer when nv < 32; the rest are 0).
-__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int64_t c, int nv,
+template <typename T>
+__device__ __forceinline__ void load_bias32(const void* bias_v, int64_t c, int nv,
                                             float (&b)[32]) {
+  const T* bias = static_cast<const T*>(bias_v);
   if (bias == nullptr) {
 #pragma unroll
     for (int k = 0; k < 32; ++k) b[k] = 0.0f;
@@ -41,14 +47,33 @@ __device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int64_t c
       const uint32_t parts[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&parts[h]);
-        b[q * 8 + 2 * h] = __low2float(pr);
-        b[q * 8 + 2 * h + 1] = __high2float(pr);
+        b[q * 8 + 2 * h] = Elem<T>::lo(parts[h]);
+        b[q * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
       }
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) b[k] = (k < nv) ? __bfloat162float(bias[c + k]) : 0.0f;
+    for (int k = 0; k < 32; ++k) b[k] = (k < nv) ? Elem<T>::to(bias[c + k]) : 0.0f;
+  }
+}
+
+// 32 values rounded to T and stored with four 16-byte stores (dst 16-byte
+// aligned), or element by element when only nv < 32 are in range.
+template <typename T>
+__device__ __forceinline__ void store32(T* dst, const float (&v)[32], int nv, float scale) {
+  if (nv == 32) {
+    uint4* dv = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dv[q] = make_uint4(Elem<T>::pack2(v[q * 8 + 0] * scale, v[q * 8 + 1] * scale),
+                         Elem<T>::pack2(v[q * 8 + 2] * scale, v[q * 8 + 3] * scale),
+                         Elem<T>::pack2(v[q * 8 + 4] * scale, v[q * 8 + 5] * scale),
+                         Elem<T>::pack2(v[q * 8 + 6] * scale, v[q * 8 + 7] * scale));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k < nv) dst[k] = Elem<T>::from(v[k] * scale);
   }
 }
 
@@ -93,7 +118,9 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 }  // namespace
 
 // ------------------------------------------------------------------ forward
+template <typename T>
 struct EpiFwdStats {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = FwdStatsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
                               bool acc_zero, int row_in_tile, int /*quarter*/, int /*lane*/,
@@ -114,7 +141,7 @@ struct EpiFwdStats {
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
-      load_bias32(p.bias, cb, nv, b);
+      load_bias32<T>(p.bias, cb, nv, b);
 #pragma unroll
       for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
       if (nv == 32) {
@@ -139,7 +166,9 @@ struct EpiFwdStats {
 };
 
 // ------------------------------------------------------------------ dlogits
+template <typename T>
 struct EpiDlogits {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = DlogitsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
                               bool acc_zero, int row_in_tile, int quarter, int lane,
@@ -154,6 +183,7 @@ struct EpiDlogits {
     const float lse2 = row_ok ? __ldg(p.lse + row) * kLog2e : 0.0f;
     const int64_t tl = t - p.c0;  // target column within this chunk
     const int col0 = n_tile * kBN;
+    const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = col0 + ch * 32;
@@ -161,7 +191,7 @@ struct EpiDlogits {
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
-      load_bias32(p.bias, p.c0 + cb, nv, b);
+      load_bias32<T>(p.bias, p.c0 + cb, nv, b);
       float d[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
@@ -180,22 +210,7 @@ struct EpiDlogits {
         d[k] = row_ok ? d[k] * gs * p.xf.dz_du(z[k]) : 0.0f;
       }
       if (row < p.n_rows) {  // rows past the present ones get zeros (d = 0 there)
-        __nv_bfloat16* dst = p.d + row * p.ldd + cb;
-        if (nv == 32) {
-          uint4* dv = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dv[q] = make_uint4(pack_bf16x2(d[q * 8 + 0], d[q * 8 + 1]),
-                               pack_bf16x2(d[q * 8 + 2], d[q * 8 + 3]),
-                               pack_bf16x2(d[q * 8 + 4], d[q * 8 + 5]),
-                               pack_bf16x2(d[q * 8 + 6], d[q * 8 + 7]));
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (k < nv) dst[k] = __float2bfloat16_rn(d[k]);
-          }
-        }
+        store32<T>(static_cast<T*>(p.d) + row * p.ldd + cb, d, nv, dscale);
       }
       if (p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff) {
         // column sums of D over this tile's 128 rows, in a fixed order
@@ -214,12 +229,15 @@ struct EpiDlogits {
 };
 
 // ------------------------------------------------------------ grad_weight
+template <typename T>
 struct EpiStoreRows {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = StoreRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
                               bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < p.rows;
+    const float scale = p.out_scale != nullptr ? *p.out_scale : 1.0f;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = n_tile * kBN + ch * 32;
@@ -235,34 +253,24 @@ struct EpiStoreRows {
           float4* dv = reinterpret_cast<float4*>(dst);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dv[q] = make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
+            dv[q] = make_float4(z[4 * q] * scale, z[4 * q + 1] * scale, z[4 * q + 2] * scale,
+                                z[4 * q + 3] * scale);
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            if (k < nv) dst[k] = z[k];
+            if (k < nv) dst[k] = z[k] * scale;
         }
       } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + off;
-        if (nv == 32) {
-          uint4* dv = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dv[q] = make_uint4(pack_bf16x2(z[q * 8 + 0], z[q * 8 + 1]),
-                               pack_bf16x2(z[q * 8 + 2], z[q * 8 + 3]),
-                               pack_bf16x2(z[q * 8 + 4], z[q * 8 + 5]),
-                               pack_bf16x2(z[q * 8 + 6], z[q * 8 + 7]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k < nv) dst[k] = __float2bfloat16_rn(z[k]);
-        }
+        store32<T>(static_cast<T*>(p.out) + off, z, nv, scale);
       }
     }
   }
 };
 
 // ------------------------------------------------------------ grad_hidden
+template <typename T>
 struct EpiAccRows {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = AccRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
                               bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
@@ -272,6 +280,7 @@ struct EpiAccRows {
     // accumulator rows are in the (possibly compacted) row order; the final
     // output goes to row_map[row]
     const int64_t out_row = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
+    const float scale = p.out_scale != nullptr ? *p.out_scale : 1.0f;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = n_tile * kBN + ch * 32;
@@ -282,6 +291,10 @@ struct EpiAccRows {
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = row * p.ld + cb;
       const int64_t out_off = out_row * p.ld + cb;
+      if (p.out_scale != nullptr) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) z[k] *= scale;
+      }
       if (p.mode == kAccAdd || p.mode == kAccAddOut) {
         const float* src = p.acc + off;
         if (nv == 32) {
@@ -313,20 +326,7 @@ struct EpiAccRows {
             if (k < nv) dst[k] = z[k];
         }
       } else {
-        __nv_bfloat16* dst = p.out + out_off;
-        if (nv == 32) {
-          uint4* dv = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dv[q] = make_uint4(pack_bf16x2(z[q * 8 + 0], z[q * 8 + 1]),
-                               pack_bf16x2(z[q * 8 + 2], z[q * 8 + 3]),
-                               pack_bf16x2(z[q * 8 + 4], z[q * 8 + 5]),
-                               pack_bf16x2(z[q * 8 + 6], z[q * 8 + 7]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k < nv) dst[k] = __float2bfloat16_rn(z[k]);
-        }
+        store32<T>(static_cast<T*>(p.out) + out_off, z, nv, 1.0f);
       }
     }
   }
@@ -382,28 +382,44 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
 
 }  // namespace
 
-cudaError_t launch_tc_fwd_stats(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                                const GemmGeom& g, const FwdStatsParams& p, int sms,
-                                cudaStream_t s) {
-  return launch_gemm<kPairCG, false, false, EpiFwdStats>(tm_hidden_k, tm_weight_k, g, p, sms, s);
+cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
+                                const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                                const FwdStatsParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, false, false, EpiFwdStats<__half>>(tm_hidden_k, tm_weight_k, g,
+                                                                    p, sms, s);
+  return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
+                                                                         g, p, sms, s);
 }
 
-cudaError_t launch_tc_dlogits(const CUtensorMap& tm_hidden_k, const CUtensorMap& tm_weight_k,
-                              const GemmGeom& g, const DlogitsParams& p, int sms,
-                              cudaStream_t s) {
-  return launch_gemm<kPairCG, false, false, EpiDlogits>(tm_hidden_k, tm_weight_k, g, p, sms, s);
+cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
+                              const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                              const DlogitsParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, false, false, EpiDlogits<__half>>(tm_hidden_k, tm_weight_k, g, p,
+                                                                   sms, s);
+  return launch_gemm<kPairCG, false, false, EpiDlogits<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
+                                                                        g, p, sms, s);
 }
 
-cudaError_t launch_tc_grad_weight(const CUtensorMap& tm_d_mn, const CUtensorMap& tm_hidden_mn,
-                                  const GemmGeom& g, const StoreRowsParams& p, int sms,
-                                  cudaStream_t s) {
-  return launch_gemm<kPairCG, true, true, EpiStoreRows>(tm_d_mn, tm_hidden_mn, g, p, sms, s);
+cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,
+                                  const CUtensorMap& tm_hidden_mn, const GemmGeom& g,
+                                  const StoreRowsParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, true, true, EpiStoreRows<__half>>(tm_d_mn, tm_hidden_mn, g, p,
+                                                                   sms, s);
+  return launch_gemm<kPairCG, true, true, EpiStoreRows<__nv_bfloat16>>(tm_d_mn, tm_hidden_mn, g,
+                                                                        p, sms, s);
 }
 
-cudaError_t launch_tc_grad_hidden(const CUtensorMap& tm_d_k, const CUtensorMap& tm_weight_mn,
-                                  const GemmGeom& g, const AccRowsParams& p, int sms,
-                                  cudaStream_t s) {
-  return launch_gemm<kPairCG, false, true, EpiAccRows>(tm_d_k, tm_weight_mn, g, p, sms, s);
+cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
+                                  const CUtensorMap& tm_weight_mn, const GemmGeom& g,
+                                  const AccRowsParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, false, true, EpiAccRows<__half>>(tm_d_k, tm_weight_mn, g, p, sms,
+                                                                  s);
+  return launch_gemm<kPairCG, false, true, EpiAccRows<__nv_bfloat16>>(tm_d_k, tm_weight_mn, g, p,
+                                                                        sms, s);
 }
 
 }  // namespace flce

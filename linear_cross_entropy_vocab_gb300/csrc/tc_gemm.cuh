@@ -180,6 +180,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 }
 
 // Epi must provide:
+//   static constexpr uint32_t kABFormat;  // operand type: 1 bf16, 0 fp16
 //   struct Params;
 //   static __device__ void tile(const Params&, int m_block, int n_tile,
 //                               uint32_t taddr, bool acc_zero, int row_in_tile,
@@ -300,7 +301,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      constexpr uint32_t idesc =
+          idesc_f16kind_f32(kBM * CG, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0, Epi::kABFormat);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;

@@ -226,12 +226,14 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
       : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// shape M x N, each operand K-major (0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn, int b_mn) {
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D: A and B both
+// bf16 (ab_format 1) or both fp16 (ab_format 0), shape M x N, each operand
+// K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int m, int n, int a_mn, int b_mn,
+                                                         uint32_t ab_format) {
   return (1u << 4)                              // D format: f32
-         | (1u << 7)                            // A format: bf16
-         | (1u << 10)                           // B format: bf16
+         | (ab_format << 7)                     // A format
+         | (ab_format << 10)                    // B format
          | (static_cast<uint32_t>(a_mn) << 15)  // A major-ness
          | (static_cast<uint32_t>(b_mn) << 16)  // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8

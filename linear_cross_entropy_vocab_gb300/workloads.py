@@ -39,7 +39,7 @@ class Workload:
     n: int
     h: int
     v: int
-    dtype: str  # "f32" or "bf16"
+    dtype: str  # "f32", "bf16" or "f16"
     hidden_var: float = 1.0
     weight_var: Optional[float] = None  # None: 1/H
     bias_var: Optional[float] = None  # None: no bias
@@ -64,7 +64,7 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
 
 
 WORKLOADS = {

@@ -31,6 +31,10 @@ TOL = {
     "f32": dict(loss_rel=1e-5, g_atol=1e-5, g_rtol=1e-4, g_norm=1e-4, ent_rel=1e-4),
     "bf16": dict(loss_rel=2e-3, g_atol=5e-5, g_rtol=5e-2, g_norm=1e-2, ent_rel=1e-3),
 }
+# fp16 inputs: the pages state no fp16 bar. fp16 rounds more finely than bf16
+# (2^-11 against 2^-8 relative) in every place the bf16 path rounds (D and the
+# outputs), so the bf16 bars bound the fp16 path.
+TOL["f16"] = dict(TOL["bf16"])
 
 
 def to_dev(x: dict) -> dict:

@@ -57,7 +57,7 @@ def _check_case(w, vocab_chunk=0, grad_weight_dtype=None, skip_ignored=False):
     assert out["err_word"] == 0
     ref = oracle.forward(*oracle_args(x, w))
     tol = TOL[w.dtype]
-    check_forward(out, ref, w, tol, skipped=skip_ignored and w.dtype == "bf16")
+    check_forward(out, ref, w, tol, skipped=skip_ignored and w.dtype != "f32")
     gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"])
     check_backward(out, gref, tol, x["bias"] is not None, grad_scale(w.reduction, ref["n_valid"]))
 
@@ -183,3 +183,32 @@ def test_skip_ignored_all_rows_ignored():
     assert torch.all(out["loss_rows"] == 0)
     for k in ("grad_hidden", "grad_weight", "grad_bias"):
         assert torch.count_nonzero(out[k]) == 0, k
+
+
+F16_CASES = [
+    _case("f16_tails_cap_sum", 300, 136, 1000, dtype="f16", bias_var=0.02, softcap=30.0,
+          logit_scale=0.5, hidden_var=2.0, ignore_frac=0.3, reduction="sum"),
+    _case("f16_mean_v32003", 512, 256, 32003, dtype="f16", ignore_frac=0.05),
+    _case("f16_none", 700, 264, 3333, dtype="f16", bias_var=0.02, ignore_frac=0.1,
+          reduction="none"),
+    _case("f16_peaked_mean", 1024, 512, 8192, dtype="f16", peaked_frac=0.01, ignore_frac=0.05),
+]
+
+
+@pytest.mark.parametrize("w", F16_CASES, ids=[w.name for w in F16_CASES])
+def test_parity_f16(w):
+    """fp16 inputs on the tensor cores (the kernel card's signature lists
+    float16); D is stored in fp16 times a power-of-two scale."""
+    _check_case(w)
+
+
+def test_parity_f16_skip_ignored_chunks():
+    w = _case("f16_skip_chunks", 900, 200, 5000, dtype="f16", bias_var=0.02, softcap=20.0,
+              ignore_frac=0.3)
+    _check_case(w, vocab_chunk=1024, skip_ignored=True)
+
+
+def test_f16_mean_workload_shape():
+    """The mid workload's shape and recipe with fp16 inputs (N=4096, H=2048,
+    V=32000, bias, Zipf targets, 10% ignored, mean)."""
+    _check_case(WORKLOADS["mid_bf16"].with_shape(dtype="f16"))
