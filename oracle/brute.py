@@ -51,8 +51,14 @@ def logits(hidden, weight, bias, logit_scale=1.0, softcap=None) -> List[List[flo
 
 
 def per_row(hidden, weight, targets, bias=None, ignore_index=-100,
-            logit_scale=1.0, softcap=None) -> List[dict]:
-    """Per-row loss, entropy, argmax and validity by explicit softmax."""
+            logit_scale=1.0, softcap=None, label_smoothing=0.0,
+            z_loss=0.0) -> List[dict]:
+    """Per-row loss, entropy, argmax and validity by explicit softmax.
+
+    With label smoothing eps the loss is the cross-entropy against the target
+    distribution q = (1-eps)*onehot + eps/V, -sum_j q_j log p_j; with z_loss
+    lam, lam * (log sum_j e^{z_j})^2 is added (the options named in the
+    CuTe-DSL FLCE pull request's feature list)."""
     z_all = logits(hidden, weight, bias, logit_scale, softcap)
     v = len(weight)
     rows = []
@@ -73,7 +79,13 @@ def per_row(hidden, weight, targets, bias=None, ignore_index=-100,
         if not valid:
             loss = 0.0
         elif 0 <= t < v:
-            loss = -math.log(p[t])
+            loss = 0.0
+            for j in range(v):
+                q = (1.0 - label_smoothing) * (1.0 if j == t else 0.0) + label_smoothing / v
+                if q != 0.0:
+                    loss -= q * math.log(p[j])
+            if z_loss != 0.0:
+                loss += z_loss * math.log(tot) ** 2
         else:
             loss = float("nan")
         rows.append({"loss": loss, "entropy": ent, "argmax": best,
@@ -83,12 +95,13 @@ def per_row(hidden, weight, targets, bias=None, ignore_index=-100,
 
 
 def loss(hidden, weight, targets, bias=None, ignore_index=-100,
-         logit_scale=1.0, softcap=None, reduction="mean", row_grads=None):
+         logit_scale=1.0, softcap=None, reduction="mean", row_grads=None,
+         label_smoothing=0.0, z_loss=0.0):
     """Reduced loss. For reduction 'none' the per-row losses are combined with
     ``row_grads`` (a scalar objective sum_i row_grads[i] * loss_i) so that
     finite differences can probe the per-row upstream-gradient path."""
     rows = per_row(hidden, weight, targets, bias, ignore_index, logit_scale,
-                   softcap)
+                   softcap, label_smoothing, z_loss)
     n_valid = sum(1 for r in rows if r["valid"])
     tot = sum(r["loss"] for r in rows)
     if reduction == "sum":

@@ -39,6 +39,15 @@ design notes):
     go to the lowest vocabulary index.
   * A target outside [0, V) that is not ignore_index counts as non-ignored,
     gets a NaN loss, is never "correct", and contributes no gradient.
+
+Two options from the feature list of the CuTe-DSL FLCE pull request
+(Liger-Kernel #1287, §Summary: "z-loss, softcap, label smoothing, ..."),
+which names them without defining them; the readings taken:
+  * label_smoothing eps: the target distribution is (1-eps)*onehot + eps/V,
+    so loss_i = (1-eps)*(lse_i - z_{i,t_i}) + eps*(lse_i - mean_j z_ij);
+  * z_loss lam: lam * lse_i^2 is added to each non-ignored row's loss;
+and the gradient with respect to z_ij is
+    g_i * [p_ij*(1 + 2*lam*lse_i) - (1-eps)*[j == t_i] - eps/V].
 """
 from __future__ import annotations
 
@@ -99,7 +108,8 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
             bias: Optional[torch.Tensor] = None, ignore_index: int = -100,
             logit_scale: float = 1.0, softcap: Optional[float] = None,
             reduction: str = "mean",
-            rows: Optional[Sequence[int]] = None) -> dict:
+            rows: Optional[Sequence[int]] = None,
+            label_smoothing: float = 0.0, z_loss: float = 0.0) -> dict:
     """Forward of the loss in fp64.
 
     Returns per-row ``loss``, ``lse``, ``argmax``, ``entropy``,
@@ -141,6 +151,11 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
         zt = torch.full((ri.numel(),), float("nan"), dtype=_F64)
         zt[ok] = z[torch.nonzero(ok).flatten(), t[ok]]
         loss = lse - zt
+        if label_smoothing != 0.0:
+            # cross-entropy against (1-eps)*onehot + eps/V
+            loss = (1.0 - label_smoothing) * loss + label_smoothing * (lse - z.mean(dim=1))
+        if z_loss != 0.0:
+            loss = loss + z_loss * lse * lse
         vm = valid_mask(t, ignore_index)
         loss = torch.where(vm, loss, torch.zeros_like(loss))
         if v >= 2:
@@ -204,16 +219,23 @@ def row_weights(targets: torch.Tensor, v: int, ignore_index: int,
 
 def _dlogits(z: torch.Tensor, u: torch.Tensor, lse: torch.Tensor,
              pos: torch.Tensor, g: torch.Tensor, logit_scale: float,
-             softcap: Optional[float]) -> torch.Tensor:
-    """d loss / d lin for a block: g_i * (p_ij - [j == t_i]) * dz/dlin.
+             softcap: Optional[float], label_smoothing: float = 0.0,
+             z_loss: float = 0.0, v_total: int = 0) -> torch.Tensor:
+    """d loss / d lin for a block:
+    g_i * (p_ij*(1 + 2*z_loss*lse_i) - (1-eps)*[j == t_i] - eps/V) * dz/dlin
+    (eps = label_smoothing; with both options off, g_i * (p_ij - [j == t_i])).
 
     ``pos[i]`` is the column of row i's target within ``z`` (or -1 when the
     target is not among these columns). dz/dlin = logit_scale * (1 -
     tanh(u/c)^2) with a softcap, else logit_scale.
     """
     d = torch.exp(z - lse[:, None])
+    if z_loss != 0.0:
+        d *= (1.0 + 2.0 * z_loss * lse)[:, None]
     hit = pos >= 0
-    d[torch.nonzero(hit).flatten(), pos[hit]] -= 1.0
+    d[torch.nonzero(hit).flatten(), pos[hit]] -= 1.0 - label_smoothing
+    if label_smoothing != 0.0:
+        d -= label_smoothing / v_total
     d *= g[:, None]
     d *= logit_scale
     if _softcap_on(softcap):
@@ -228,7 +250,8 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
              lse: Optional[torch.Tensor] = None,
              rows: Optional[Sequence[int]] = None,
              vocab_rows: Optional[Sequence[int]] = None,
-             want_hidden: bool = True, want_weight: bool = True) -> dict:
+             want_hidden: bool = True, want_weight: bool = True,
+             label_smoothing: float = 0.0, z_loss: float = 0.0) -> dict:
     """Gradients of the loss in fp64 (§Algorithm: grad_hidden = (p - onehot)
     @ weight, grad_weight = (p - onehot).T @ hidden; bias gets the column
     sums), with the chain factor of logit_scale and softcap.
@@ -260,14 +283,15 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                 lse_b = lse[ri].to(_F64)
             t = targets[ri]
             pos = torch.where(_in_range(t, v), t, torch.full_like(t, -1))
-            d = _dlogits(z, u, lse_b, pos, g_all[ri], logit_scale, softcap)
+            d = _dlogits(z, u, lse_b, pos, g_all[ri], logit_scale, softcap,
+                         label_smoothing, z_loss, v)
             gh[s:s + blk] = d @ w64
         out["grad_hidden"] = gh
         out["rows"] = idx
     if want_weight:
         if lse is None:
             lse = forward(hidden, weight, targets, bias, ignore_index,
-                          logit_scale, softcap, reduction)["lse"]
+                          logit_scale, softcap, reduction)["lse"]  # lse needs no options
         jdx = torch.arange(v) if vocab_rows is None else torch.as_tensor(list(vocab_rows), dtype=torch.int64)
         # column of each vocabulary id among the selected rows, -1 if absent
         col_of = torch.full((v,), -1, dtype=torch.int64)
@@ -288,7 +312,7 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
             ok = _in_range(t, v)
             pos[ok] = col_of[t[ok]]
             d = _dlogits(z, u, lse[ri].to(_F64), pos, g_all[ri], logit_scale,
-                         softcap)
+                         softcap, label_smoothing, z_loss, v)
             gw += d.T @ hidden[ri].to(_F64)
             gb += d.sum(dim=0)
         out["grad_weight"] = gw

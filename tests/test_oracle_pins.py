@@ -77,7 +77,8 @@ def test_brute_force_forward(case):
     assert f["entropy_mean"] == pytest.approx(ent, rel=1e-12)
 
 
-def _fd_check(case, n_probe=6, step=1e-5, seed=1, mod=flce_oracle):
+def _fd_check(case, n_probe=6, step=1e-5, seed=1, mod=flce_oracle, label_smoothing=0.0,
+              z_loss=0.0):
     """Central differences of the brute-force loss against the oracle's
     analytic gradients, at randomly chosen entries of hidden, weight, bias."""
     x = _inputs(*case[1:])
@@ -90,14 +91,16 @@ def _fd_check(case, n_probe=6, step=1e-5, seed=1, mod=flce_oracle):
         row_g = (torch.rand(n, generator=gen, dtype=F64) + 0.5)
         grad_out = row_g
     g = mod.backward(x["hidden"], x["weight"], x["targets"], x["bias"], -100,
-                     o["logit_scale"], o["softcap"], o["reduction"], grad_out)
+                     o["logit_scale"], o["softcap"], o["reduction"], grad_out,
+                     label_smoothing=label_smoothing, z_loss=z_loss)
     scale = 1.0 if o["reduction"] == "none" else 0.7
 
     def L(hh, ww, bb):
         b = None if bb is None else bb.tolist()
         val = brute.loss(hh.tolist(), ww.tolist(), x["targets"].tolist(), b, -100,
                          o["logit_scale"], o["softcap"], o["reduction"],
-                         None if row_g is None else row_g.tolist())
+                         None if row_g is None else row_g.tolist(),
+                         label_smoothing=label_smoothing, z_loss=z_loss)
         return scale * val
 
     worst = 0.0
@@ -127,6 +130,81 @@ def _fd_check(case, n_probe=6, step=1e-5, seed=1, mod=flce_oracle):
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_finite_differences(case):
     assert _fd_check(case) < 1e-6
+
+
+# label smoothing / z-loss: (case, eps, lam)
+OPT_CASES = [
+    (CASES[1], 0.1, 0.0),
+    (CASES[2], 0.0, 1e-2),
+    (CASES[3], 0.2, 5e-3),
+    (CASES[4], 0.05, 1e-3),
+]
+
+
+@pytest.mark.parametrize("case,eps,lam", OPT_CASES, ids=[f"{c[0]}-ls{e}-z{z}" for c, e, z in OPT_CASES])
+def test_smoothing_zloss_brute_force_and_fd(case, eps, lam):
+    """Label smoothing and z-loss: the oracle's per-row loss against the brute
+    force's cross-entropy against (1-eps)*onehot + eps/V plus lam*lse^2, and
+    its gradients against central differences of that brute-force loss."""
+    x = _inputs(*case[1:])
+    o = _opts(case)
+    f = oracle.forward(x["hidden"], x["weight"], x["targets"], x["bias"], -100,
+                       o["logit_scale"], o["softcap"], o["reduction"],
+                       label_smoothing=eps, z_loss=lam)
+    h, w, t, b = _lists(x)
+    rows = brute.per_row(h, w, t, b, -100, o["logit_scale"], o["softcap"], eps, lam)
+    for i, r in enumerate(rows):
+        assert f["loss"][i].item() == pytest.approx(r["loss"], rel=1e-12, abs=1e-14)
+    assert _fd_check(case, label_smoothing=eps, z_loss=lam) < 1e-6
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_torch_label_smoothing_and_zloss(reduction):
+    """Library cross-check of label smoothing: torch cross_entropy with
+    label_smoothing (its own ignore_index handling) plus the z-loss term, with
+    autograd for the gradients."""
+    eps, lam = 0.15, 2e-3
+    x = _inputs(16, 8, 27, True, 2.5, 0.7, 0.25, reduction)
+    hid = x["hidden"].clone().requires_grad_(True)
+    wt = x["weight"].clone().requires_grad_(True)
+    bs = x["bias"].clone().requires_grad_(True)
+    logits = 2.5 * torch.tanh(0.7 * torch.nn.functional.linear(hid, wt, bs) / 2.5)
+    ce = torch.nn.functional.cross_entropy(logits, x["targets"], ignore_index=-100,
+                                           reduction="none", label_smoothing=eps)
+    valid = (x["targets"] != -100).to(F64)
+    rows = ce + lam * torch.logsumexp(logits, dim=1) ** 2 * valid
+    if reduction == "mean":
+        ref = rows.sum() / valid.sum()
+    elif reduction == "sum":
+        ref = rows.sum()
+    else:
+        ref = rows
+    gen = torch.Generator().manual_seed(3)
+    go = torch.rand(16, generator=gen, dtype=F64) if reduction == "none" else 1.0
+    (ref * go).sum().backward() if reduction == "none" else ref.backward()
+    args = (x["hidden"], x["weight"], x["targets"], x["bias"], -100, 0.7, 2.5, reduction)
+    f = oracle.forward(*args, label_smoothing=eps, z_loss=lam)
+    if reduction == "none":
+        assert torch.allclose(f["loss_out"], ref.detach(), rtol=1e-12, atol=1e-14)
+    else:
+        assert f["loss_out"] == pytest.approx(ref.item(), rel=1e-12)
+    g = oracle.backward(*args, go, label_smoothing=eps, z_loss=lam)
+    assert torch.allclose(g["grad_hidden"], hid.grad, rtol=1e-11, atol=1e-15)
+    assert torch.allclose(g["grad_weight"], wt.grad, rtol=1e-11, atol=1e-15)
+    assert torch.allclose(g["grad_bias"], bs.grad, rtol=1e-11, atol=1e-15)
+
+
+def test_closed_form_zero_weight_with_options():
+    """W = 0, b = 0: lse = ln V and every logit is 0, so with any label
+    smoothing the loss is ln V, plus lam * (ln V)^2 from the z-loss."""
+    n, h, v = 9, 5, 41
+    x = _inputs(n, h, v, False, None, 1.0, 0.0, "mean")
+    w0 = torch.zeros(v, h, dtype=F64)
+    for eps, lam in ((0.3, 0.0), (0.0, 0.01), (0.1, 0.02)):
+        f = oracle.forward(x["hidden"], w0, x["targets"], None, -100, 1.0, None, "mean",
+                           label_smoothing=eps, z_loss=lam)
+        lnv = math.log(v)
+        assert f["loss_out"] == pytest.approx(lnv + lam * lnv * lnv, rel=1e-14)
 
 
 def test_closed_form_zero_weight():
@@ -357,20 +435,37 @@ def _mut_transposed(h, w, b, s, c):
     return flce_oracle_orig_final_logits(h, torch.flip(w, [0]), b, s, c)
 
 
-def _mut_dlogits_no_cap(z, u, lse, pos, g, s, c):
-    return flce_oracle_orig_dlogits(z, u, lse, pos, g, s, None)
+def _mut_dlogits_no_cap(z, u, lse, pos, g, s, c, *opts):
+    return flce_oracle_orig_dlogits(z, u, lse, pos, g, s, None, *opts)
 
 
-def _mut_dlogits_sign(z, u, lse, pos, g, s, c):
-    return -flce_oracle_orig_dlogits(z, u, lse, pos, g, s, c)
+def _mut_dlogits_sign(z, u, lse, pos, g, s, c, *opts):
+    return -flce_oracle_orig_dlogits(z, u, lse, pos, g, s, c, *opts)
 
 
-def _mut_dlogits_no_onehot(z, u, lse, pos, g, s, c):
-    return flce_oracle_orig_dlogits(z, u, lse, torch.full_like(pos, -1), g, s, c)
+def _mut_dlogits_no_onehot(z, u, lse, pos, g, s, c, *opts):
+    return flce_oracle_orig_dlogits(z, u, lse, torch.full_like(pos, -1), g, s, c, *opts)
 
 
-def _mut_dlogits_no_scale(z, u, lse, pos, g, s, c):
-    return flce_oracle_orig_dlogits(z, u, lse, pos, g, 1.0, c)
+def _mut_dlogits_no_scale(z, u, lse, pos, g, s, c, *opts):
+    return flce_oracle_orig_dlogits(z, u, lse, pos, g, 1.0, c, *opts)
+
+
+def _mut_dlogits_no_zloss_term(z, u, lse, pos, g, s, c, eps=0.0, lam=0.0, v=0):
+    return flce_oracle_orig_dlogits(z, u, lse, pos, g, s, c, eps, 0.0, v)
+
+
+def _mut_dlogits_no_uniform_term(z, u, lse, pos, g, s, c, eps=0.0, lam=0.0, v=0):
+    d = flce_oracle_orig_dlogits(z, u, lse, pos, g, s, c, eps, lam, v)
+    return d + (eps / v) * g[:, None] * s if v else d
+
+
+def _mut_dlogits_full_onehot(z, u, lse, pos, g, s, c, eps=0.0, lam=0.0, v=0):
+    # uses 1 instead of 1 - eps on the target
+    d = flce_oracle_orig_dlogits(z, u, lse, pos, g, s, c, eps, lam, v)
+    hit = pos >= 0
+    d[torch.nonzero(hit).flatten(), pos[hit]] -= eps * g[hit] * s
+    return d
 
 
 flce_oracle_orig_final_logits = flce_oracle.final_logits
@@ -384,6 +479,9 @@ MUTANTS = [
     ("_dlogits", _mut_dlogits_sign),
     ("_dlogits", _mut_dlogits_no_onehot),
     ("_dlogits", _mut_dlogits_no_scale),
+    ("_dlogits", _mut_dlogits_no_zloss_term),
+    ("_dlogits", _mut_dlogits_no_uniform_term),
+    ("_dlogits", _mut_dlogits_full_onehot),
 ]
 
 
@@ -392,6 +490,9 @@ def _pins_pass():
         for case in CASES:
             test_brute_force_forward(case)
             if _fd_check(case, n_probe=3) >= 1e-6:
+                return False
+        for case, eps, lam in OPT_CASES:
+            if _fd_check(case, n_probe=3, label_smoothing=eps, z_loss=lam) >= 1e-6:
                 return False
     except AssertionError:
         return False
