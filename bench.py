@@ -81,6 +81,8 @@ def workload_of(args):
         w = w.with_shape(dtype=args.dtype)
     if args.forward_only and w.name == "long_bf16":
         w = w.with_shape(reduction="none")  # this workload's forward-only phase
+    if args.label_smoothing or args.z_loss:
+        w = w.with_shape(label_smoothing=args.label_smoothing, z_loss=args.z_loss)
     return w
 
 
@@ -92,6 +94,8 @@ def describe(w) -> str:
         parts.append(f"logit_scale={w.logit_scale} softcap={w.softcap}")
     if w.peaked_frac:
         parts.append(f"{round(100 * w.peaked_frac)}% weight rows x{w.peaked_factor:g}")
+    if w.label_smoothing or w.z_loss:
+        parts.append(f"label_smoothing={w.label_smoothing:g} z_loss={w.z_loss:g}")
     parts.append(w.reduction + (", return_metrics" if w.return_metrics else ""))
     return ", ".join(parts)
 
@@ -164,7 +168,8 @@ class Step:
                 torch.float32: abi.FLCE_F32}[x["hidden"].dtype]
         self.prob = abi.make_problem(n, h, v, code, x["bias"] is not None, w.ignore_index,
                                      w.logit_scale, w.softcap, w.reduction,
-                                     skip_ignored=skip_ignored)
+                                     skip_ignored=skip_ignored,
+                                     label_smoothing=w.label_smoothing, z_loss=w.z_loss)
         f32 = dict(dtype=torch.float32, device=dev)
         self.loss_rows = torch.empty(n, **f32)
         self.lse_rows = torch.empty(n, **f32)
@@ -461,6 +466,8 @@ def main():
                     help="run the workload with this input type (default: the workload's)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time flce_forward alone (the long workload uses reduction none)")
+    ap.add_argument("--label-smoothing", type=float, default=0.0)
+    ap.add_argument("--z-loss", type=float, default=0.0)
     ap.add_argument("--all-rows", action="store_true",
                     help="run ignored rows through the GEMMs too (FLCE_SKIP_IGNORED_ROWS off)")
     args = ap.parse_args()

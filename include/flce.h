@@ -96,7 +96,15 @@ typedef enum flce_reduction {
  *                      (the chunk's N x chunk dlogits buffer is the largest
  *                      workspace item); rounded up to a multiple of 256
  *   flags              OR of FLCE_SKIP_IGNORED_ROWS; 0 for none
+ *   label_smoothing    eps in [0, 1]: cross-entropy against the target
+ *                      distribution (1-eps)*onehot + eps/V, i.e.
+ *                      loss_i = (1-eps)(lse_i - z_{i,t_i}) + eps(lse_i - mean_j z_ij)
+ *   z_loss             lam >= 0: lam * lse_i^2 is added to each non-ignored row
  *   reserved           must be 0
+ * With label smoothing and z-loss the logit gradient is
+ *   g_i (p_ij (1 + 2 lam lse_i) - (1-eps)[j == t_i] - eps/V).
+ * Both options are named in the CuTe-DSL FLCE pull request's feature list
+ * (Liger-Kernel #1287, Summary); the forms above are the plain readings.
  */
 typedef struct flce_problem {
   int64_t n, h, v;
@@ -109,6 +117,8 @@ typedef struct flce_problem {
   int32_t grad_weight_dtype;
   int64_t vocab_chunk;
   int32_t flags;
+  float label_smoothing;
+  float z_loss;
   int32_t reserved;
 } flce_problem;
 
@@ -125,7 +135,8 @@ typedef struct flce_problem {
 /* Bytes of device workspace flce_forward() needs for `p` (0 if `p` is
  * invalid). Cite: §Algorithm ("tiles over the vocabulary ... merges the tile
  * into a running log-sum-exp"): the workspace holds the per-(row, vocabulary
- * tile) statistics the merge combines, about N * ceil(V/256) * 16 bytes. */
+ * tile) statistics the merge combines, about N * ceil(V/256) * 16 bytes
+ * (20 with label smoothing). */
 size_t flce_forward_workspace_size(const flce_problem* p);
 
 /* Forward pass. Cite: §Algorithm (forward), §Metrics for free.

@@ -68,6 +68,8 @@ class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
         ("grad_weight_dtype", ctypes.c_int32),
         ("vocab_chunk", ctypes.c_int64),
         ("flags", ctypes.c_int32),
+        ("label_smoothing", ctypes.c_float),
+        ("z_loss", ctypes.c_float),
         ("reserved", ctypes.c_int32),
     ]
 
@@ -146,7 +148,8 @@ def _check(status: int, call: str):
 
 def make_problem(n, h, v, dtype, has_bias, ignore_index=-100, logit_scale=1.0,
                  softcap=None, reduction="mean", grad_weight_dtype=None,
-                 vocab_chunk=0, skip_ignored=False) -> flce_problem:
+                 vocab_chunk=0, skip_ignored=False, label_smoothing=0.0,
+                 z_loss=0.0) -> flce_problem:
     p = flce_problem()
     p.n, p.h, p.v = int(n), int(h), int(v)
     p.dtype = int(dtype)
@@ -158,6 +161,8 @@ def make_problem(n, h, v, dtype, has_bias, ignore_index=-100, logit_scale=1.0,
     p.grad_weight_dtype = int(dtype if grad_weight_dtype is None else grad_weight_dtype)
     p.vocab_chunk = int(vocab_chunk)
     p.flags = FLCE_SKIP_IGNORED_ROWS if skip_ignored else 0
+    p.label_smoothing = float(label_smoothing)
+    p.z_loss = float(z_loss)
     p.reserved = 0
     return p
 

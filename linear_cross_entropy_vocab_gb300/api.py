@@ -62,7 +62,8 @@ def _check_inputs(hidden, weight, targets, bias):
 def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
                          logit_scale=1.0, softcap=None, reduction="mean",
                          return_metrics=False, row_metrics=False, err_word=None,
-                         vocab_chunk=0, skip_ignored=False) -> dict:
+                         vocab_chunk=0, skip_ignored=False, label_smoothing=0.0,
+                         z_loss=0.0) -> dict:
     """Run flce_forward; returns a dict of freshly allocated output tensors:
     loss (0-d, or [N] for 'none'), loss_rows, lse_rows, n_valid (0-d int32),
     metrics ([2] or None), correct_rows / entropy_rows (when row_metrics).
@@ -74,7 +75,8 @@ def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
     dev = hidden.device
     prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
                             logit_scale, softcap, reduction, vocab_chunk=vocab_chunk,
-                            skip_ignored=skip_ignored)
+                            skip_ignored=skip_ignored, label_smoothing=label_smoothing,
+                            z_loss=z_loss)
     f32 = dict(dtype=torch.float32, device=dev)
     loss_rows = torch.empty(n, **f32)
     lse_rows = torch.empty(n, **f32)
@@ -105,7 +107,8 @@ def flce_forward_tensors(hidden, weight, targets, bias=None, ignore_index=-100,
 def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, bias=None,
                           ignore_index=-100, logit_scale=1.0, softcap=None,
                           reduction="mean", grad_weight_dtype=None, err_word=None,
-                          vocab_chunk=0, skip_ignored=False):
+                          vocab_chunk=0, skip_ignored=False, label_smoothing=0.0,
+                          z_loss=0.0):
     """Run flce_backward; returns (grad_hidden, grad_weight, grad_bias).
     ``grad_out`` is a 0-d fp32 tensor ('sum'/'mean') or [N] ('none').
     ``grad_weight_dtype`` torch.float32 keeps grad_weight in fp32.
@@ -118,7 +121,8 @@ def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, 
     gw_code = abi.FLCE_F32 if gw_dtype == torch.float32 else _dtype_code(hidden)
     prob = abi.make_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
                             logit_scale, softcap, reduction, grad_weight_dtype=gw_code,
-                            vocab_chunk=vocab_chunk, skip_ignored=skip_ignored)
+                            vocab_chunk=vocab_chunk, skip_ignored=skip_ignored,
+                            label_smoothing=label_smoothing, z_loss=z_loss)
     grad_out = grad_out.to(device=dev, dtype=torch.float32).contiguous()
     grad_hidden = torch.empty_like(hidden)
     grad_weight = torch.empty(v, h, dtype=gw_dtype, device=dev)
@@ -137,12 +141,13 @@ def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, ignore_index, logit_scale, softcap,
-                reduction, return_metrics):
+                reduction, return_metrics, label_smoothing, z_loss):
         # ignored rows contribute nothing, so they are left out of the GEMMs
         out = flce_forward_tensors(hidden, weight, targets, bias, ignore_index, logit_scale,
-                                   softcap, reduction, return_metrics, skip_ignored=True)
+                                   softcap, reduction, return_metrics, skip_ignored=True,
+                                   label_smoothing=label_smoothing, z_loss=z_loss)
         ctx.save_for_backward(hidden, weight, bias, targets, out["lse_rows"], out["n_valid"])
-        ctx.opts = (ignore_index, logit_scale, softcap, reduction)
+        ctx.opts = (ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss)
         metrics = out["metrics"]
         if metrics is None:
             metrics = torch.empty(0, dtype=torch.float32, device=hidden.device)
@@ -152,27 +157,32 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_loss, _grad_metrics):
         hidden, weight, bias, targets, lse_rows, n_valid = ctx.saved_tensors
-        ignore_index, logit_scale, softcap, reduction = ctx.opts
+        ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss = ctx.opts
         gh, gw, gb = flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid,
                                            grad_loss, bias, ignore_index, logit_scale,
-                                           softcap, reduction, skip_ignored=True)
+                                           softcap, reduction, skip_ignored=True,
+                                           label_smoothing=label_smoothing, z_loss=z_loss)
         need = ctx.needs_input_grad
         return (gh if need[0] else None, gw if need[1] else None,
                 gb if (bias is not None and need[2]) else None,
-                None, None, None, None, None, None)
+                None, None, None, None, None, None, None, None)
 
 
 def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
                                targets: torch.Tensor, bias: Optional[torch.Tensor] = None,
                                ignore_index: int = -100, logit_scale: float = 1.0,
                                softcap: Optional[float] = None, reduction: str = "mean",
-                               return_metrics: bool = False):
+                               return_metrics: bool = False, *,
+                               label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Cross-entropy of softcap(logit_scale * (hidden @ weight.T + bias))
     against targets, without materialising the (N, V) logits.
 
     Returns the loss (0-d for 'mean'/'sum', (N,) for 'none'), or with
     return_metrics ``(loss, {"mean_token_accuracy": 0-d, "entropy": 0-d})``;
     metrics are over non-ignored positions, entropy in nats.
+
+    Keyword-only extras: ``label_smoothing`` eps (cross-entropy against
+    (1-eps)*onehot + eps/V) and ``z_loss`` lam (adds lam * lse^2 per row).
     """
     if reduction not in abi.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(abi.REDUCTIONS)}")
@@ -182,7 +192,8 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
     bias = None if bias is None else bias.contiguous()
     loss, metrics = _FusedLinearCrossEntropy.apply(hidden, weight, bias, targets,
                                                    int(ignore_index), float(logit_scale),
-                                                   softcap, reduction, bool(return_metrics))
+                                                   softcap, reduction, bool(return_metrics),
+                                                   float(label_smoothing), float(z_loss))
     if not return_metrics:
         return loss
     return loss, {"mean_token_accuracy": metrics[0], "entropy": metrics[1]}

@@ -177,7 +177,8 @@ struct CompactPlan {
 
 struct FwdPlan {
   int64_t n_vt = 0;
-  size_t partials = 0, zt = 0, correct = 0, entropy = 0, total = 0;
+  size_t partials = 0, zsum = 0, zt = 0, correct = 0, entropy = 0, total = 0;
+  bool has_zsum = false;
   CompactPlan cp;
 };
 
@@ -242,6 +243,10 @@ flce_status check_problem(const flce_problem* p) {
   if (p->vocab_chunk < 0) return fail(FLCE_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
   if ((p->flags & ~FLCE_SKIP_IGNORED_ROWS) != 0 || p->reserved != 0)
     return fail(FLCE_ERR_INVALID_ARG, "unknown flags or non-zero reserved field");
+  if (!(p->label_smoothing >= 0.0f && p->label_smoothing <= 1.0f))
+    return fail(FLCE_ERR_INVALID_ARG, "label_smoothing must be in [0, 1]");
+  if (!std::isfinite(p->z_loss) || p->z_loss < 0.0f)
+    return fail(FLCE_ERR_INVALID_ARG, "z_loss must be finite and >= 0");
   if (is_tc(p) && p->h % 8 != 0)
     return fail(FLCE_ERR_UNSUPPORTED,
                 "bf16/fp16 inputs need h %% 8 == 0 (16-byte row pitch); h=%lld", (long long)p->h);
@@ -261,6 +266,9 @@ FwdPlan plan_forward(const flce_problem* p) {
   size_t off = 0;
   f.partials = off;
   off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 16);
+  f.has_zsum = p->label_smoothing != 0.0f;
+  f.zsum = off;
+  if (f.has_zsum) off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 4);
   f.zt = off;
   off = align_up(off + static_cast<size_t>(p->n) * 4);
   f.correct = off;
@@ -485,6 +493,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float4* partials = reinterpret_cast<float4*>(ws + plan.partials);
+  float* zsum = plan.has_zsum ? reinterpret_cast<float*>(ws + plan.zsum) : nullptr;
   float* zt = reinterpret_cast<float*>(ws + plan.zt);
   int32_t* correct_ws = reinterpret_cast<int32_t*>(ws + plan.correct);
   float* entropy_ws = reinterpret_cast<float*>(ws + plan.entropy);
@@ -552,6 +561,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.bias = bias;
       fp.targets = rows_targets;
       fp.partials = partials;
+      fp.zsum = zsum;
       fp.zt = zt;
       fp.n_rows = p->n;
       fp.n_rows_dyn = n_kept;
@@ -568,6 +578,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.bias = static_cast<const float*>(bias);
       fp.targets = targets;
       fp.partials = partials;
+      fp.zsum = zsum;
       fp.zt = zt;
       fp.n = p->n;
       fp.h = p->h;
@@ -580,6 +591,9 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
     }
     flce::MergeParams mp{};
     mp.partials = partials;
+    mp.zsum = zsum;
+    mp.label_smoothing = p->label_smoothing;
+    mp.z_loss = p->z_loss;
     mp.zt = zt;
     mp.targets = rows_targets;
     mp.row_map = row_map;
@@ -681,7 +695,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
     if (scales != nullptr) {
       ProfScope ps("dlogits_scale", s);
       e = flce::launch_dlogits_scale(grad_out, n_valid, targets, p->n, p->ignore_index,
-                                     p->reduction, p->logit_scale, scales, s);
+                                     p->reduction, p->logit_scale, p->z_loss, lse_rows, scales,
+                                     s);
       if (e != cudaSuccess) return cuda_fail(e, "dlogits scale kernel");
     }
     // valid-row compaction: rows of hidden, targets, lse and per-row
@@ -781,6 +796,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.c0 = static_cast<int>(c0);
       dp.width = static_cast<int>(width);
       dp.reduction = p->reduction;
+      dp.label_smoothing = p->label_smoothing;
+      dp.z_loss = p->z_loss;
       dp.xf = xf;
       {
         ProfScope ps("bwd_dlogits", s);
@@ -868,6 +885,8 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       dp.c0 = c0;
       dp.width = width;
       dp.reduction = p->reduction;
+      dp.label_smoothing = p->label_smoothing;
+      dp.z_loss = p->z_loss;
       dp.xf = xf;
       {
         ProfScope ps("bwd_dlogits_f32", s);

@@ -32,6 +32,7 @@ struct FwdStatsParams {
   const void* bias;           // [V] in the input type, or null
   const int64_t* targets;     // [N]
   float4* partials;           // [N][n_vt] (m, s, t, argmax)
+  float* zsum;                // [N][n_vt] sum of the tile's logits (label smoothing) or null
   float* zt;                  // [N] target logit
   int64_t n_rows;             // rows of the buffers
   const int32_t* n_rows_dyn;  // rows actually present (device count) or null
@@ -58,6 +59,8 @@ struct DlogitsParams {
   int c0;     // first vocabulary column of the chunk
   int width;  // columns in the chunk
   int reduction;
+  float label_smoothing;
+  float z_loss;
   LogitXform xf;
 };
 
@@ -107,8 +110,8 @@ cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
 // `scales` [2].
 cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
                                  const int64_t* targets, int64_t n, int64_t ignore_index,
-                                 int reduction, float logit_scale, float* scales,
-                                 cudaStream_t s);
+                                 int reduction, float logit_scale, float z_loss,
+                                 const float* lse_rows, float* scales, cudaStream_t s);
 
 // fp32 (SIMT) path
 struct SimtFwdParams {
@@ -117,6 +120,7 @@ struct SimtFwdParams {
   const float* bias;
   const int64_t* targets;
   float4* partials;
+  float* zsum;
   float* zt;
   int64_t n, h, v, n_vt;
   LogitXform xf;
@@ -138,6 +142,8 @@ struct SimtDlogitsParams {
   int64_t n, h, v, ignore_index;
   int64_t c0, width;
   int reduction;
+  float label_smoothing;
+  float z_loss;
   LogitXform xf;
 };
 cudaError_t launch_simt_dlogits(const SimtDlogitsParams& p, cudaStream_t s);
@@ -150,6 +156,9 @@ cudaError_t launch_simt_gemm(int64_t m, int64_t n, int64_t k, const float* a, in
 // row kernels
 struct MergeParams {
   const float4* partials;
+  const float* zsum;          // per-tile logit sums (label smoothing) or null
+  float label_smoothing;
+  float z_loss;
   const float* zt;
   const int64_t* targets;     // of the (possibly compacted) rows
   const int32_t* row_map;     // original row of each compacted row, or null

@@ -32,6 +32,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
   for (int64_t u = lane; u < p.n_vt; u += 32) st = merge_stats(st, RowStats::unpack(part[u]));
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) st = merge_stats(st, shfl_xor_stats(st, off));
+  float zsum = 0.0f;  // sum of the row's logits (label smoothing)
+  if (p.zsum != nullptr) {
+    const float* zp = p.zsum + row * p.n_vt;
+    for (int64_t u = lane; u < p.n_vt; u += 32) zsum += zp[u];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
+  }
   if (lane != 0) return;
   const float log_s = logf(st.s);
   const float lse = st.m + log_s;
@@ -42,6 +49,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
   if (t != p.ignore_index) {
     if (t >= 0 && t < p.v) {
       loss = lse - p.zt[row];
+      if (p.zsum != nullptr) {
+        // cross-entropy against (1 - eps) onehot + eps / V
+        const float eps = p.label_smoothing;
+        loss = fmaf(1.0f - eps, loss, eps * (lse - zsum / static_cast<float>(p.v)));
+      }
+      if (p.z_loss != 0.0f) loss = fmaf(p.z_loss * lse, lse, loss);
       correct = (static_cast<int64_t>(st.a) == t) ? 1 : 0;
     } else {
       loss = __int_as_float(0x7fc00000);  // NaN
@@ -131,9 +144,23 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(1024)
     dlogits_scale_kernel(const float* grad_out, const int32_t* n_valid, const int64_t* targets,
                          int64_t n, int64_t ignore_index, int reduction, float logit_scale,
-                         float* scales) {
+                         float z_loss, const float* lse_rows, float* scales) {
   __shared__ float red[32];
+  __shared__ float lse_red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // with z-loss, |D| <= g * s * (1 + 2 |z_loss| max |lse|)
+  float lm = 0.0f;
+  if (z_loss != 0.0f) {
+    for (int64_t i = tid; i < n; i += 1024)
+      if (targets[i] != ignore_index) lm = fmaxf(lm, fabsf(lse_rows[i]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+    if (lane == 0) lse_red[warp] = lm;
+    __syncthreads();
+    lm = lse_red[lane];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+  }
   float g = 0.0f;
   if (reduction == 0) {
     for (int64_t i = tid; i < n; i += 1024)
@@ -152,7 +179,7 @@ __global__ void __launch_bounds__(1024)
     if (reduction == 2) g = n_valid[0] > 0 ? g / static_cast<float>(n_valid[0]) : 0.0f;
   }
   if (tid != 0) return;
-  const float gs = g * fabsf(logit_scale);
+  const float gs = g * fabsf(logit_scale) * fmaf(2.0f * fabsf(z_loss), lm, 1.0f);
   float up = 1.0f, down = 1.0f;
   if (gs > 0.0f && isfinite(gs)) {
     int e = 0;
@@ -266,10 +293,10 @@ cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s) {
 
 cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
                                  const int64_t* targets, int64_t n, int64_t ignore_index,
-                                 int reduction, float logit_scale, float* scales,
-                                 cudaStream_t s) {
+                                 int reduction, float logit_scale, float z_loss,
+                                 const float* lse_rows, float* scales, cudaStream_t s) {
   dlogits_scale_kernel<<<1, 1024, 0, s>>>(grad_out, n_valid, targets, n, ignore_index, reduction,
-                                          logit_scale, scales);
+                                          logit_scale, z_loss, lse_rows, scales);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const SimtFwdParams p) {
     if (row >= p.n) break;  // warp-uniform
     RowStats st;
     st.init();
+    float zsum = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int cl = lane + 32 * j;
@@ -97,12 +98,17 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const SimtFwdParams p) {
           st.rebase(z);
         }
         st.add(z);
+        zsum += z;
       }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) st = merge_stats(st, shfl_xor_stats(st, off));
+    for (int off = 16; off >= 1; off >>= 1) {
+      st = merge_stats(st, shfl_xor_stats(st, off));
+      zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
+    }
     if (lane == 0) {
       p.partials[row * p.n_vt + blockIdx.y] = st.pack();
+      if (p.zsum != nullptr) p.zsum[row * p.n_vt + blockIdx.y] = zsum;
       const int64_t t = p.targets[row];
       if (t >= col0 && t < col0 + TV && t < p.v) p.zt[row] = zs[rl][t - col0];
     }
@@ -129,6 +135,8 @@ __global__ void __launch_bounds__(256) simt_dlogits_kernel(const SimtDlogitsPara
     const float g =
         row_ok ? row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row) : 0.0f;
     const float lse = row_ok ? p.lse[row] : 0.0f;
+    const float pz = fmaf(2.0f * p.z_loss, lse, 1.0f);
+    const float eps_v = p.label_smoothing / static_cast<float>(p.v);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int cl = tx + 32 * j;
@@ -137,8 +145,8 @@ __global__ void __launch_bounds__(256) simt_dlogits_kernel(const SimtDlogitsPara
       if (row_ok && c < vend) {
         const float b = (p.bias != nullptr) ? p.bias[c] : 0.0f;
         const float z = p.xf(acc[i][j], b);
-        d = ex2_approx((z - lse) * kLog2e);
-        if (c == t) d -= 1.0f;
+        d = fmaf(ex2_approx((z - lse) * kLog2e), pz, -eps_v);
+        if (c == t) d -= 1.0f - p.label_smoothing;
         d *= g * p.xf.scale * p.xf.dz_du(z);
         p.d[row * p.ldd + (c - p.c0)] = d;
       }

@@ -133,6 +133,7 @@ struct EpiFwdStats {
     RowStats st;
     st.init();
     float zt = 0.0f;
+    float zs = 0.0f;  // sum of this tile's logits (used for label smoothing)
     bool has_zt = false;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
@@ -149,6 +150,11 @@ struct EpiFwdStats {
       } else {
         fold_chunk<false>(st, z, nv, static_cast<int>(cb));
       }
+      if (p.zsum != nullptr) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (k < nv) zs += z[k];
+      }
       const int64_t tk = t - cb;
       if (tk >= 0 && tk < nv) {
 #pragma unroll
@@ -160,6 +166,7 @@ struct EpiFwdStats {
     }
     if (row_ok) {
       p.partials[row * p.n_vt + n_tile] = st.pack();
+      if (p.zsum != nullptr) p.zsum[row * p.n_vt + n_tile] = zs;
       if (has_zt) p.zt[row] = zt;
     }
   }
@@ -180,7 +187,12 @@ struct EpiDlogits {
     const float g = row_ok ? row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row)
                            : 0.0f;
     const float gs = g * p.xf.scale;
-    const float lse2 = row_ok ? __ldg(p.lse + row) * kLog2e : 0.0f;
+    const float lse_r = row_ok ? __ldg(p.lse + row) : 0.0f;
+    const float lse2 = lse_r * kLog2e;
+    // D/(g * dz/dlin) = p * (1 + 2 z_loss lse) - (1 - eps) [target] - eps / V
+    const float pz = fmaf(2.0f * p.z_loss, lse_r, 1.0f);
+    const float eps_v = p.label_smoothing / static_cast<float>(p.v);
+    const float on_target = 1.0f - p.label_smoothing;
     const int64_t tl = t - p.c0;  // target column within this chunk
     const int col0 = n_tile * kBN;
     const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
@@ -196,13 +208,13 @@ struct EpiDlogits {
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         z[k] = p.xf(z[k], b[k]);
-        d[k] = ex2_approx(fmaf(z[k], kLog2e, -lse2));
+        d[k] = fmaf(ex2_approx(fmaf(z[k], kLog2e, -lse2)), pz, -eps_v);
       }
       const int64_t tk = tl - cb;
       if (tk >= 0 && tk < nv) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          if (k == tk) d[k] -= 1.0f;
+          if (k == tk) d[k] -= on_target;
         }
       }
 #pragma unroll

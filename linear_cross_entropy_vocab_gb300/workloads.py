@@ -54,6 +54,8 @@ class Workload:
     peaked_frac: float = 0.0
     peaked_factor: float = 8.0
     seed: int = 0
+    label_smoothing: float = 0.0
+    z_loss: float = 0.0
 
     def with_shape(self, n: Optional[int] = None, h: Optional[int] = None,
                    v: Optional[int] = None, **kw) -> "Workload":

@@ -48,7 +48,8 @@ def run_gpu(xd: dict, w, grad_out=1.0, row_metrics=True, vocab_chunk=0,
     f = api.flce_forward_tensors(xd["hidden"], xd["weight"], xd["targets"], xd["bias"],
                                  w.ignore_index, w.logit_scale, w.softcap, w.reduction,
                                  return_metrics=True, row_metrics=row_metrics, err_word=err,
-                                 skip_ignored=skip_ignored)
+                                 skip_ignored=skip_ignored, label_smoothing=w.label_smoothing,
+                                 z_loss=w.z_loss)
     out = {k: (None if t is None else t.detach().cpu()) for k, t in f.items()}
     if backward:
         if w.reduction == "none":
@@ -59,7 +60,7 @@ def run_gpu(xd: dict, w, grad_out=1.0, row_metrics=True, vocab_chunk=0,
             xd["hidden"], xd["weight"], xd["targets"], f["lse_rows"], f["n_valid"], go,
             xd["bias"], w.ignore_index, w.logit_scale, w.softcap, w.reduction,
             grad_weight_dtype=grad_weight_dtype, err_word=err, vocab_chunk=vocab_chunk,
-            skip_ignored=skip_ignored)
+            skip_ignored=skip_ignored, label_smoothing=w.label_smoothing, z_loss=w.z_loss)
         out["grad_hidden"] = gh.cpu()
         out["grad_weight"] = gw.cpu()
         out["grad_bias"] = None if gb is None else gb.cpu()
@@ -71,6 +72,10 @@ def run_gpu(xd: dict, w, grad_out=1.0, row_metrics=True, vocab_chunk=0,
 def oracle_args(x: dict, w):
     return (x["hidden"], x["weight"], x["targets"], x["bias"], w.ignore_index,
             w.logit_scale, w.softcap, w.reduction)
+
+
+def oracle_opts(w) -> dict:
+    return dict(label_smoothing=w.label_smoothing, z_loss=w.z_loss)
 
 
 def assert_rows_close(name, got, ref, rel, valid=None):

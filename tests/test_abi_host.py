@@ -35,12 +35,14 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_matches_header():
     # int64 n,h,v; int32 dtype,has_bias; int64 ignore_index; float scale, softcap;
-    # int32 reduction, grad_weight_dtype; int64 vocab_chunk; int32 flags, reserved
-    assert ctypes.sizeof(abi.flce_problem) == 72
+    # int32 reduction, grad_weight_dtype; int64 vocab_chunk; int32 flags;
+    # float label_smoothing, z_loss; int32 reserved
+    assert ctypes.sizeof(abi.flce_problem) == 80
     assert abi.flce_problem.ignore_index.offset == 32
     assert abi.flce_problem.logit_scale.offset == 40
     assert abi.flce_problem.vocab_chunk.offset == 56
     assert abi.flce_problem.flags.offset == 64
+    assert abi.flce_problem.z_loss.offset == 72
 
 
 def test_status_strings(lib):
@@ -105,6 +107,10 @@ def test_validation_statuses(lib):
     assert _fwd(cap) == abi.FLCE_ERR_INVALID_ARG
     gw = abi.make_problem(64, 64, 100, abi.FLCE_F32, False, grad_weight_dtype=abi.FLCE_BF16)
     assert _fwd(gw) == abi.FLCE_ERR_INVALID_ARG
+    ls = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False, label_smoothing=1.5)
+    assert _fwd(ls) == abi.FLCE_ERR_INVALID_ARG
+    zl = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False, z_loss=float("inf"))
+    assert _fwd(zl) == abi.FLCE_ERR_INVALID_ARG
     none = abi.make_problem(64, 64, 100, abi.FLCE_BF16, False, reduction="none")
     assert _fwd(none, loss_out=None, workspace_bytes=8) == abi.FLCE_ERR_WORKSPACE
     bias = abi.make_problem(64, 64, 100, abi.FLCE_BF16, True)

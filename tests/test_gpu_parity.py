@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import oracle
-from _parity import TOL, check_backward, check_forward, grad_scale, oracle_args, run_gpu, to_dev
+from _parity import (TOL, check_backward, check_forward, grad_scale, oracle_args, oracle_opts,
+                     run_gpu, to_dev)
 from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -55,10 +56,10 @@ def _check_case(w, vocab_chunk=0, grad_weight_dtype=None, skip_ignored=False):
                   vocab_chunk=vocab_chunk, grad_weight_dtype=grad_weight_dtype,
                   skip_ignored=skip_ignored)
     assert out["err_word"] == 0
-    ref = oracle.forward(*oracle_args(x, w))
+    ref = oracle.forward(*oracle_args(x, w), **oracle_opts(w))
     tol = TOL[w.dtype]
     check_forward(out, ref, w, tol, skipped=skip_ignored and w.dtype != "f32")
-    gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"])
+    gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"], **oracle_opts(w))
     check_backward(out, gref, tol, x["bias"] is not None, grad_scale(w.reduction, ref["n_valid"]))
 
 
@@ -212,3 +213,28 @@ def test_f16_mean_workload_shape():
     """The mid workload's shape and recipe with fp16 inputs (N=4096, H=2048,
     V=32000, bias, Zipf targets, 10% ignored, mean)."""
     _check_case(WORKLOADS["mid_bf16"].with_shape(dtype="f16"))
+
+
+OPT_CASES = [
+    _case("ls_bf16_mean", 520, 256, 5000, bias_var=0.02, ignore_frac=0.1, label_smoothing=0.1),
+    _case("zl_bf16_sum_cap", 300, 136, 1000, softcap=30.0, logit_scale=0.5, hidden_var=2.0,
+          ignore_frac=0.3, reduction="sum", z_loss=1e-3),
+    _case("ls_zl_bf16_none", 700, 264, 3333, bias_var=0.02, ignore_frac=0.1, reduction="none",
+          label_smoothing=0.2, z_loss=1e-4),
+    _case("ls_zl_f16_peaked", 1024, 512, 8192, dtype="f16", peaked_frac=0.01, ignore_frac=0.05,
+          label_smoothing=0.05, z_loss=1e-3),
+    _case("ls_zl_f32", 257, 96, 2100, dtype="f32", bias_var=0.5, reduction="sum",
+          label_smoothing=0.1, z_loss=1e-3),
+]
+
+
+@pytest.mark.parametrize("w", OPT_CASES, ids=[w.name for w in OPT_CASES])
+def test_parity_label_smoothing_zloss(w):
+    """Label smoothing and z-loss (the CuTe-DSL FLCE pull request's options)."""
+    _check_case(w)
+
+
+def test_parity_label_smoothing_zloss_skip_chunks():
+    w = _case("ls_zl_skip_chunks", 777, 200, 5000, bias_var=0.02, softcap=20.0, ignore_frac=0.3,
+              label_smoothing=0.1, z_loss=1e-3)
+    _check_case(w, vocab_chunk=1024, skip_ignored=True)
