@@ -169,6 +169,16 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kDefaultDlogitsBudget = int64_t(512) << 20;  // bytes of one dlogits chunk
 
+// Tile bands (GemmGeom::group) of the row-tile-fastest GEMMs. With bands of
+// 16 pair row tiles (4096 rows) the forward and dlogits kernels re-read
+// hidden far less (measured at the Llama-3 head shape: forward DRAM reads
+// 6.5 -> 2.7-4.2 GB, dlogits 7.0 -> 3.1-3.4 GB per step); grad_hidden does
+// best with 8 (19.7 -> 11.6-13.5 GB). grad_weight is fastest along H and is
+// left unbanded (banding it raised its reads).
+constexpr int kBandForward = 16;
+constexpr int kBandDlogits = 16;
+constexpr int kBandGradHidden = 8;
+
 // Workspace items of valid-row compaction (FLCE_SKIP_IGNORED_ROWS).
 struct CompactPlan {
   bool on = false;
@@ -554,6 +564,7 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
       g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g.m_fastest = 1;
+      g.group = kBandForward;
       g.dyn_rows = n_kept;
       g.dyn_axis = 0;
       g.err_word = err_word;
@@ -774,6 +785,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
       g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
       g1.m_fastest = 1;
+      g1.group = kBandDlogits;
       g1.b_mn0 = static_cast<int>(c0);
       g1.dyn_rows = n_kept;
       g1.dyn_axis = 0;
@@ -834,6 +846,7 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
       g3.n_tiles = h_tiles;
       g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
       g3.m_fastest = 1;
+      g3.group = kBandGradHidden;
       g3.b_k0 = static_cast<int>(c0);
       g3.dyn_rows = n_kept;
       g3.dyn_axis = 0;

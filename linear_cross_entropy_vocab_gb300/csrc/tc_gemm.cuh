@@ -82,17 +82,41 @@ struct GemmGeom {
   // read at kernel start, so the host needs no synchronisation to learn it.
   const int32_t* dyn_rows;
   int dyn_axis;
+  // When > 0, tiles are taken in bands: with m_fastest, bands of `group`
+  // M-tiles (all N-tiles of a band before the next band); otherwise bands of
+  // `group` N-tiles (all M-tiles of a band before the next). The
+  // tiles in flight then share fewer rows of the operand that every tile of
+  // the other axis reuses, which keeps it in L2.
+  int group;
   int* err_word;
 };
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int m_tiles, int u, int& m,
                                             int& n) {
   if (g.m_fastest) {
-    m = u % m_tiles;
-    n = u / m_tiles;
+    if (g.group > 0 && g.group < m_tiles) {
+      const int band = g.group * g.n_tiles;
+      const int first = (u / band) * g.group;
+      const int rows = m_tiles - first < g.group ? m_tiles - first : g.group;
+      const int r = u % band;
+      m = first + r % rows;
+      n = r / rows;
+    } else {
+      m = u % m_tiles;
+      n = u / m_tiles;
+    }
   } else {
-    n = u % g.n_tiles;
-    m = u / g.n_tiles;
+    if (g.group > 0 && g.group < g.n_tiles) {
+      const int band = g.group * m_tiles;
+      const int first = (u / band) * g.group;
+      const int cols = g.n_tiles - first < g.group ? g.n_tiles - first : g.group;
+      const int r = u % band;
+      n = first + r % cols;
+      m = r / cols;
+    } else {
+      n = u % g.n_tiles;
+      m = u / g.n_tiles;
+    }
   }
 }
 
