@@ -126,3 +126,41 @@ def metrics(hidden, weight, targets, bias=None, ignore_index=-100,
     acc = sum(1 for r in val if r["correct"]) / len(val)
     ent = sum(r["entropy"] for r in val) / len(val)
     return acc, ent
+
+
+def kl_per_row(hidden, weight, target_probs, bias=None, labels=None, ignore_index=-100,
+               temperature=1.0, eps=1e-10):
+    """Per-row KL(Q || P) by explicit softmax of the logits / T:
+    sum_j q_j (log max(q_j, eps) - log p_j), 0 for ignored rows (the fused
+    linear KL divergence of Liger-Kernel pull request #1423)."""
+    z_all = logits(hidden, weight, bias, 1.0 / temperature, None)
+    out = []
+    for i, (z, q) in enumerate(zip(z_all, target_probs)):
+        if labels is not None and int(labels[i]) == ignore_index:
+            out.append(0.0)
+            continue
+        e = [math.exp(x) for x in z]
+        tot = sum(e)
+        acc = 0.0
+        for qj, ej in zip(q, e):
+            qj = float(qj)
+            acc += qj * (math.log(max(qj, eps)) - math.log(ej / tot))
+        out.append(acc)
+    return out
+
+
+def kl_loss(hidden, weight, target_probs, bias=None, labels=None, ignore_index=-100,
+            temperature=1.0, eps=1e-10, reduction="batchmean", row_grads=None):
+    rows = kl_per_row(hidden, weight, target_probs, bias, labels, ignore_index, temperature,
+                      eps)
+    n_counted = len(rows) if labels is None else sum(1 for t in labels if int(t) != ignore_index)
+    tot = sum(rows)
+    if reduction == "sum":
+        return tot
+    if reduction == "batchmean":
+        return tot / n_counted
+    if reduction == "mean":
+        return tot / (n_counted * len(weight))
+    if reduction == "none":
+        return sum(g * r for g, r in zip(row_grads, rows))
+    raise ValueError(reduction)
