@@ -221,6 +221,87 @@ flce_status flce_backward(const flce_problem* p, const void* hidden,
                           size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused linear KL divergence (FusedLinearKLDivLoss pull request, Liger-Kernel
+ * #1423, Summary and Details): the vocabulary projection followed by
+ * KL(Q || P) against an explicit target distribution Q (teacher
+ * probabilities), without materialising the N x V logits:
+ *
+ *   z_ij   = (hidden_i . weight_j + bias_j) / temperature
+ *   loss_i = sum_j q_ij (log max(q_ij, eps) - (z_ij - lse_i))     (counted rows)
+ *          = sum_j q_ij (log max(q_ij, eps) - z_ij) + lse_i * sum_j q_ij
+ *   D_ij   = g_i (p_ij * sum_k q_ik - q_ij) / temperature          (d loss / d lin)
+ *
+ * Rows whose label equals ignore_index are not counted (labels may be NULL:
+ * every row counts). Reductions follow torch.nn.KLDivLoss: batchmean divides
+ * the sum by the counted rows, mean by counted rows * V; none returns the
+ * per-row losses and takes per-row upstream gradients. The same kernels as
+ * the cross-entropy run underneath; conventions are those of flce_forward /
+ * flce_backward above.
+ */
+typedef enum flce_kl_reduction {
+  FLCE_KL_NONE = 0,
+  FLCE_KL_SUM = 1,
+  FLCE_KL_BATCHMEAN = 2,
+  FLCE_KL_MEAN = 3
+} flce_kl_reduction;
+
+/*   n, h, v, dtype, has_bias, grad_weight_dtype, vocab_chunk, flags
+ *                      as in flce_problem (target_probs has the input dtype)
+ *   ignore_index       label value of rows left out (used only with labels)
+ *   temperature        > 0: the student logits are divided by it
+ *   eps                > 0: clamp inside log q (so that 0 * log 0 adds 0)
+ *   reduction          flce_kl_reduction
+ *   reserved           must be 0 */
+typedef struct flce_kl_problem {
+  int64_t n, h, v;
+  int32_t dtype;
+  int32_t has_bias;
+  int64_t ignore_index;
+  float temperature;
+  float eps;
+  int32_t reduction;
+  int32_t grad_weight_dtype;
+  int64_t vocab_chunk;
+  int32_t flags;
+  int32_t reserved;
+} flce_kl_problem;
+
+/* Bytes of device workspace flce_kl_forward() needs (0 if `p` is invalid). */
+size_t flce_kl_forward_workspace_size(const flce_kl_problem* p);
+
+/* KL forward. target_probs [N,V] (input dtype), labels [N] int64 (nullable).
+ *   loss_rows [N] fp32 out (0 on uncounted rows)                     required
+ *   lse_rows  [N] fp32 out: log-sum-exp of z, kept for the backward   required
+ *   qsum_rows [N] fp32 out: sum_j q_ij, kept for the backward         required
+ *   loss_out  scalar fp32 out (not written for FLCE_KL_NONE)
+ *   n_counted scalar int32 out: rows counted                          required
+ * With FLCE_SKIP_IGNORED_ROWS and labels, uncounted rows are left out of
+ * the contractions (their lse and qsum are then NaN). */
+flce_status flce_kl_forward(const flce_kl_problem* p, const void* hidden,
+                            const void* weight, const void* bias,
+                            const void* target_probs, const int64_t* labels,
+                            float* loss_rows, float* lse_rows, float* qsum_rows,
+                            float* loss_out, int32_t* n_counted,
+                            int32_t* err_word, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace flce_kl_backward() needs (0 if `p` is invalid). */
+size_t flce_kl_backward_workspace_size(const flce_kl_problem* p);
+
+/* KL backward: grad_hidden, grad_weight, grad_bias as in flce_backward, from
+ * the forward's lse_rows, qsum_rows and n_counted; grad_out is a scalar, or
+ * [N] for FLCE_KL_NONE. */
+flce_status flce_kl_backward(const flce_kl_problem* p, const void* hidden,
+                             const void* weight, const void* bias,
+                             const void* target_probs, const int64_t* labels,
+                             const float* lse_rows, const float* qsum_rows,
+                             const int32_t* n_counted, const float* grad_out,
+                             void* grad_hidden, void* grad_weight,
+                             void* grad_bias, int32_t* err_word,
+                             void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-kernel timing, for measurement tools (not part of the method; the
  * pages describe no profiler). While enabled, every kernel launch made by
  * flce_forward / flce_backward on the calling process is bracketed by two

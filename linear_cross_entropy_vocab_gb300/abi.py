@@ -36,6 +36,14 @@ FLCE_DEVERR_TIMEOUT = 2
 
 REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
 
+FLCE_KL_NONE = 0
+FLCE_KL_SUM = 1
+FLCE_KL_BATCHMEAN = 2
+FLCE_KL_MEAN = 3
+
+KL_REDUCTIONS = {"none": FLCE_KL_NONE, "sum": FLCE_KL_SUM, "batchmean": FLCE_KL_BATCHMEAN,
+                 "mean": FLCE_KL_MEAN}
+
 # Every symbol include/flce.h declares.
 EXPORTS = (
     "flce_forward_workspace_size",
@@ -43,6 +51,10 @@ EXPORTS = (
     "flce_forward_noalloc",
     "flce_backward_workspace_size",
     "flce_backward",
+    "flce_kl_forward_workspace_size",
+    "flce_kl_forward",
+    "flce_kl_backward_workspace_size",
+    "flce_kl_backward",
     "flce_status_string",
     "flce_last_error",
     "flce_device_supported",
@@ -74,6 +86,24 @@ class flce_problem(ctypes.Structure):  # noqa: N801  (C name)
     ]
 
 
+class flce_kl_problem(ctypes.Structure):  # noqa: N801  (C name)
+    _fields_ = [
+        ("n", ctypes.c_int64),
+        ("h", ctypes.c_int64),
+        ("v", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("has_bias", ctypes.c_int32),
+        ("ignore_index", ctypes.c_int64),
+        ("temperature", ctypes.c_float),
+        ("eps", ctypes.c_float),
+        ("reduction", ctypes.c_int32),
+        ("grad_weight_dtype", ctypes.c_int32),
+        ("vocab_chunk", ctypes.c_int64),
+        ("flags", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
 class flce_kernel_time(ctypes.Structure):  # noqa: N801  (C name)
     _fields_ = [
         ("name", ctypes.c_char * FLCE_PROFILE_NAME_LEN),
@@ -93,6 +123,7 @@ _lib = None
 
 _P = ctypes.c_void_p
 _PROB = ctypes.POINTER(flce_problem)
+_KLPROB = ctypes.POINTER(flce_kl_problem)
 
 
 def library_path() -> str:
@@ -123,6 +154,16 @@ def load() -> ctypes.CDLL:
         lib.flce_backward.argtypes = [_PROB] + [_P] * 14
         lib.flce_backward.argtypes[-2] = ctypes.c_size_t
         lib.flce_backward.restype = ctypes.c_int
+        lib.flce_kl_forward_workspace_size.argtypes = [_KLPROB]
+        lib.flce_kl_forward_workspace_size.restype = ctypes.c_size_t
+        lib.flce_kl_backward_workspace_size.argtypes = [_KLPROB]
+        lib.flce_kl_backward_workspace_size.restype = ctypes.c_size_t
+        lib.flce_kl_forward.argtypes = [_KLPROB] + [_P] * 14
+        lib.flce_kl_forward.argtypes[-2] = ctypes.c_size_t
+        lib.flce_kl_forward.restype = ctypes.c_int
+        lib.flce_kl_backward.argtypes = [_KLPROB] + [_P] * 16
+        lib.flce_kl_backward.argtypes[-2] = ctypes.c_size_t
+        lib.flce_kl_backward.restype = ctypes.c_int
         lib.flce_status_string.argtypes = [ctypes.c_int]
         lib.flce_status_string.restype = ctypes.c_char_p
         lib.flce_last_error.argtypes = []
@@ -207,6 +248,55 @@ def flce_backward(p, hidden, weight, bias, targets, lse_rows, n_valid, grad_out,
                               err_word, workspace, workspace_bytes, stream)
     if check:
         _check(st, "flce_backward")
+    return st
+
+
+def make_kl_problem(n, h, v, dtype, has_bias, ignore_index=-100, temperature=1.0, eps=1e-10,
+                    reduction="batchmean", grad_weight_dtype=None, vocab_chunk=0,
+                    skip_ignored=False) -> flce_kl_problem:
+    p = flce_kl_problem()
+    p.n, p.h, p.v = int(n), int(h), int(v)
+    p.dtype = int(dtype)
+    p.has_bias = 1 if has_bias else 0
+    p.ignore_index = int(ignore_index)
+    p.temperature = float(temperature)
+    p.eps = float(eps)
+    p.reduction = KL_REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
+    p.grad_weight_dtype = int(dtype if grad_weight_dtype is None else grad_weight_dtype)
+    p.vocab_chunk = int(vocab_chunk)
+    p.flags = FLCE_SKIP_IGNORED_ROWS if skip_ignored else 0
+    p.reserved = 0
+    return p
+
+
+def flce_kl_forward_workspace_size(p: flce_kl_problem) -> int:
+    return load().flce_kl_forward_workspace_size(ctypes.byref(p))
+
+
+def flce_kl_backward_workspace_size(p: flce_kl_problem) -> int:
+    return load().flce_kl_backward_workspace_size(ctypes.byref(p))
+
+
+def flce_kl_forward(p, hidden, weight, bias, target_probs, labels, loss_rows, lse_rows,
+                    qsum_rows, loss_out, n_counted, err_word, workspace, workspace_bytes,
+                    stream, check=True) -> int:
+    st = load().flce_kl_forward(ctypes.byref(p), hidden, weight, bias, target_probs, labels,
+                                loss_rows, lse_rows, qsum_rows, loss_out, n_counted, err_word,
+                                workspace, workspace_bytes, stream)
+    if check:
+        _check(st, "flce_kl_forward")
+    return st
+
+
+def flce_kl_backward(p, hidden, weight, bias, target_probs, labels, lse_rows, qsum_rows,
+                     n_counted, grad_out, grad_hidden, grad_weight, grad_bias, err_word,
+                     workspace, workspace_bytes, stream, check=True) -> int:
+    st = load().flce_kl_backward(ctypes.byref(p), hidden, weight, bias, target_probs, labels,
+                                 lse_rows, qsum_rows, n_counted, grad_out, grad_hidden,
+                                 grad_weight, grad_bias, err_word, workspace, workspace_bytes,
+                                 stream)
+    if check:
+        _check(st, "flce_kl_backward")
     return st
 
 

@@ -20,7 +20,8 @@ import torch
 
 from . import abi
 
-__all__ = ["fused_linear_cross_entropy", "flce_forward_tensors", "flce_backward_tensors"]
+__all__ = ["fused_linear_cross_entropy", "flce_forward_tensors", "flce_backward_tensors",
+           "fused_linear_kl_div", "flce_kl_forward_tensors", "flce_kl_backward_tensors"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -197,3 +198,136 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
     if not return_metrics:
         return loss
     return loss, {"mean_token_accuracy": metrics[0], "entropy": metrics[1]}
+
+
+# ------------------------------------------------------------ KL divergence
+def _check_kl_inputs(hidden, weight, target_probs, labels, bias):
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden must be (N, H) and weight (V, H)")
+    if target_probs.shape != (hidden.shape[0], weight.shape[0]):
+        raise ValueError("target_probs must be (N, V)")
+    if labels is not None:
+        if labels.dim() != 1 or labels.shape[0] != hidden.shape[0]:
+            raise ValueError("labels must be (N,)")
+        if labels.dtype != torch.int64:
+            raise TypeError("labels must be int64")
+    if (weight.dtype != hidden.dtype or target_probs.dtype != hidden.dtype
+            or (bias is not None and bias.dtype != hidden.dtype)):
+        raise TypeError("hidden, weight, target_probs and bias must share one dtype")
+    if bias is not None and (bias.dim() != 1 or bias.shape[0] != weight.shape[0]):
+        raise ValueError("bias must be (V,)")
+    for name, t in (("hidden", hidden), ("weight", weight), ("target_probs", target_probs),
+                    ("labels", labels), ("bias", bias)):
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device != hidden.device:
+            raise ValueError(f"{name} is on {t.device}, hidden on {hidden.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def flce_kl_forward_tensors(hidden, weight, target_probs, labels=None, bias=None,
+                            ignore_index=-100, temperature=1.0, eps=1e-10,
+                            reduction="batchmean", err_word=None, skip_ignored=False) -> dict:
+    """Run flce_kl_forward; returns loss (0-d, or [N] for 'none'), loss_rows,
+    lse_rows, qsum_rows and n_counted (0-d int32)."""
+    _check_kl_inputs(hidden, weight, target_probs, labels, bias)
+    n, h = hidden.shape
+    v = weight.shape[0]
+    dev = hidden.device
+    prob = abi.make_kl_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
+                               temperature, eps, reduction, skip_ignored=skip_ignored)
+    f32 = dict(dtype=torch.float32, device=dev)
+    loss_rows = torch.empty(n, **f32)
+    lse_rows = torch.empty(n, **f32)
+    qsum_rows = torch.empty(n, **f32)
+    n_counted = torch.empty((), dtype=torch.int32, device=dev)
+    loss_out = None if reduction == "none" else torch.empty((), **f32)
+    with torch.cuda.device(dev):
+        ws_bytes = abi.flce_kl_forward_workspace_size(prob)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        abi.flce_kl_forward(prob, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(target_probs),
+                            _ptr(labels), _ptr(loss_rows), _ptr(lse_rows), _ptr(qsum_rows),
+                            _ptr(loss_out), _ptr(n_counted), _ptr(err_word), _ptr(ws), ws_bytes,
+                            stream)
+    return {"loss": loss_rows if reduction == "none" else loss_out, "loss_rows": loss_rows,
+            "lse_rows": lse_rows, "qsum_rows": qsum_rows, "n_counted": n_counted}
+
+
+def flce_kl_backward_tensors(hidden, weight, target_probs, lse_rows, qsum_rows, n_counted,
+                             grad_out, labels=None, bias=None, ignore_index=-100,
+                             temperature=1.0, eps=1e-10, reduction="batchmean",
+                             grad_weight_dtype=None, err_word=None, vocab_chunk=0,
+                             skip_ignored=False):
+    """Run flce_kl_backward; returns (grad_hidden, grad_weight, grad_bias)."""
+    _check_kl_inputs(hidden, weight, target_probs, labels, bias)
+    n, h = hidden.shape
+    v = weight.shape[0]
+    dev = hidden.device
+    gw_dtype = hidden.dtype if grad_weight_dtype is None else grad_weight_dtype
+    gw_code = abi.FLCE_F32 if gw_dtype == torch.float32 else _dtype_code(hidden)
+    prob = abi.make_kl_problem(n, h, v, _dtype_code(hidden), bias is not None, ignore_index,
+                               temperature, eps, reduction, grad_weight_dtype=gw_code,
+                               vocab_chunk=vocab_chunk, skip_ignored=skip_ignored)
+    grad_out = grad_out.to(device=dev, dtype=torch.float32).contiguous()
+    grad_hidden = torch.empty_like(hidden)
+    grad_weight = torch.empty(v, h, dtype=gw_dtype, device=dev)
+    grad_bias = torch.empty_like(bias) if bias is not None else None
+    with torch.cuda.device(dev):
+        ws_bytes = abi.flce_kl_backward_workspace_size(prob)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        abi.flce_kl_backward(prob, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(target_probs),
+                             _ptr(labels), _ptr(lse_rows), _ptr(qsum_rows), _ptr(n_counted),
+                             _ptr(grad_out), _ptr(grad_hidden), _ptr(grad_weight),
+                             _ptr(grad_bias), _ptr(err_word), _ptr(ws), ws_bytes, stream)
+    return grad_hidden, grad_weight, grad_bias
+
+
+class _FusedLinearKLDiv(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, hidden, weight, bias, target_probs, labels, ignore_index, temperature, eps,
+                reduction):
+        out = flce_kl_forward_tensors(hidden, weight, target_probs, labels, bias, ignore_index,
+                                      temperature, eps, reduction, skip_ignored=True)
+        ctx.save_for_backward(hidden, weight, bias, target_probs, labels, out["lse_rows"],
+                              out["qsum_rows"], out["n_counted"])
+        ctx.opts = (ignore_index, temperature, eps, reduction)
+        return out["loss"]
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        hidden, weight, bias, target_probs, labels, lse_rows, qsum_rows, n_counted = \
+            ctx.saved_tensors
+        ignore_index, temperature, eps, reduction = ctx.opts
+        gh, gw, gb = flce_kl_backward_tensors(hidden, weight, target_probs, lse_rows, qsum_rows,
+                                              n_counted, grad_loss, labels, bias, ignore_index,
+                                              temperature, eps, reduction, skip_ignored=True)
+        need = ctx.needs_input_grad
+        return (gh if need[0] else None, gw if need[1] else None,
+                gb if (bias is not None and need[2]) else None,
+                None, None, None, None, None, None)
+
+
+def fused_linear_kl_div(hidden: torch.Tensor, weight: torch.Tensor,
+                        target_probs: torch.Tensor, labels: Optional[torch.Tensor] = None,
+                        bias: Optional[torch.Tensor] = None, ignore_index: int = -100,
+                        temperature: float = 1.0, eps: float = 1e-10,
+                        reduction: str = "batchmean"):
+    """KL(target || softmax((hidden @ weight.T + bias) / temperature)) per row,
+    reduced like torch.nn.KLDivLoss ('batchmean', 'mean', 'sum', 'none'),
+    without materialising the (N, V) logits. Rows whose label equals
+    ignore_index are left out (labels None: every row counts). The teacher
+    probabilities get no gradient."""
+    if reduction not in abi.KL_REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(abi.KL_REDUCTIONS)}")
+    hidden = hidden.contiguous()
+    weight = weight.contiguous()
+    target_probs = target_probs.detach().contiguous()
+    labels = None if labels is None else labels.contiguous()
+    bias = None if bias is None else bias.contiguous()
+    return _FusedLinearKLDiv.apply(hidden, weight, bias, target_probs, labels,
+                                   int(ignore_index), float(temperature), float(eps), reduction)

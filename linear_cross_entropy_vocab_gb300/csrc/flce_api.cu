@@ -182,7 +182,8 @@ constexpr int kBandGradHidden = 8;
 // Workspace items of valid-row compaction (FLCE_SKIP_IGNORED_ROWS).
 struct CompactPlan {
   bool on = false;
-  size_t row_map = 0, n_kept = 0, hidden_c = 0, targets_c = 0, lse_c = 0, grad_c = 0;
+  size_t row_map = 0, n_kept = 0, hidden_c = 0, targets_c = 0, lse_c = 0, grad_c = 0,
+         qsum_c = 0;
 };
 
 struct FwdPlan {
@@ -209,7 +210,8 @@ bool skips_ignored(const flce_problem* p) {
 }
 
 // Appends the compaction items at `off`; returns the new end.
-size_t plan_compaction(const flce_problem* p, bool backward, size_t off, CompactPlan* c) {
+size_t plan_compaction(const flce_problem* p, bool backward, bool kl, size_t off,
+                       CompactPlan* c) {
   c->on = skips_ignored(p);
   if (!c->on) return off;
   const size_t n = static_cast<size_t>(p->n);
@@ -226,6 +228,10 @@ size_t plan_compaction(const flce_problem* p, bool backward, size_t off, Compact
     off = align_up(off + n * 4);
     c->grad_c = off;
     off = align_up(off + n * 4);
+    if (kl) {
+      c->qsum_c = off;
+      off = align_up(off + n * 4);
+    }
   }
   return off;
 }
@@ -285,12 +291,12 @@ FwdPlan plan_forward(const flce_problem* p) {
   off = align_up(off + static_cast<size_t>(p->n) * 4);
   f.entropy = off;
   off = align_up(off + static_cast<size_t>(p->n) * 4);
-  off = plan_compaction(p, false, off, &f.cp);
+  off = plan_compaction(p, false, false, off, &f.cp);
   f.total = off;
   return f;
 }
 
-BwdPlan plan_backward(const flce_problem* p) {
+BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   BwdPlan b;
   const int64_t elem = is_tc(p) ? 2 : 4;
   const int64_t v_round = cdiv(p->v, 256) * 256;
@@ -316,7 +322,7 @@ BwdPlan plan_backward(const flce_problem* p) {
   if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
   b.scales = off;
   if (p->dtype == FLCE_F16) off = align_up(off + 2 * sizeof(float));
-  off = plan_compaction(p, true, off, &b.cp);
+  off = plan_compaction(p, true, kl, off, &b.cp);
   b.total = off;
   return b;
 }
@@ -347,6 +353,411 @@ flce_status check_workspace(void* ws, size_t have, size_t need) {
     return fail(FLCE_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   return FLCE_OK;
 }
+
+// Valid-row compaction (FLCE_SKIP_IGNORED_ROWS): row_map / n_kept from the
+// targets, then the kept rows of hidden (and, through `gp`, of the per-row
+// inputs the caller names) gathered into the workspace. `cp` and `gp` carry
+// the caller's optional outputs; the common fields are filled here.
+flce_status launch_compaction(const flce_problem* p, const CompactPlan& plan, uint8_t* ws,
+                              const void* hidden, const int64_t* targets, flce::CompactParams cp,
+                              flce::GatherParams gp, cudaStream_t s) {
+  int32_t* row_map = reinterpret_cast<int32_t*>(ws + plan.row_map);
+  int32_t* n_kept = reinterpret_cast<int32_t*>(ws + plan.n_kept);
+  cp.targets = targets;
+  cp.n = p->n;
+  cp.ignore_index = p->ignore_index;
+  cp.row_map = row_map;
+  cp.n_kept = n_kept;
+  gp.hidden = hidden;
+  gp.n = p->n;
+  gp.h = p->h;
+  gp.row_map = row_map;
+  gp.n_kept = n_kept;
+  gp.pad_rows = flce::kTileRowsTC;
+  gp.hidden_c = ws + plan.hidden_c;
+  gp.targets = targets;
+  gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.targets_c);
+  gp.ignore_index = p->ignore_index;
+  cudaError_t e;
+  {
+    ProfScope ps("compact_rows", s);
+    e = flce::launch_compact_rows(cp, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "row compaction kernel");
+  {
+    ProfScope ps("gather_rows", s);
+    e = flce::launch_gather_rows(gp, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------ KL problems
+// The KL divergence runs on the cross-entropy's plans and kernels: its
+// problem maps to an flce_problem with logit_scale = 1 / temperature, no
+// softcap, and the reduction code the shared steps understand (none 0,
+// sum 1, batchmean and mean 2: an average over counted rows; "mean" further
+// divides by V where it is applied).
+flce_status check_kl_problem(const flce_kl_problem* k, flce_problem* ce) {
+  if (k == nullptr) return fail(FLCE_ERR_INVALID_ARG, "problem pointer is NULL");
+  if (!(k->temperature > 0.0f) || !std::isfinite(k->temperature) ||
+      !std::isfinite(1.0f / k->temperature))
+    return fail(FLCE_ERR_INVALID_ARG, "temperature must be finite and > 0 (with 1/T finite)");
+  if (!(k->eps > 0.0f) || !std::isfinite(k->eps))
+    return fail(FLCE_ERR_INVALID_ARG, "eps must be finite and > 0");
+  if (k->reduction < FLCE_KL_NONE || k->reduction > FLCE_KL_MEAN)
+    return fail(FLCE_ERR_INVALID_ARG, "reduction must be none, sum, batchmean or mean");
+  if (k->reserved != 0) return fail(FLCE_ERR_INVALID_ARG, "non-zero reserved field");
+  std::memset(ce, 0, sizeof(*ce));
+  ce->n = k->n;
+  ce->h = k->h;
+  ce->v = k->v;
+  ce->dtype = k->dtype;
+  ce->has_bias = k->has_bias;
+  ce->ignore_index = k->ignore_index;
+  ce->logit_scale = 1.0f / k->temperature;
+  ce->softcap = 0.0f;
+  ce->reduction = k->reduction == FLCE_KL_NONE  ? FLCE_RED_NONE
+                  : k->reduction == FLCE_KL_SUM ? FLCE_RED_SUM
+                                                : FLCE_RED_MEAN;
+  ce->grad_weight_dtype = k->grad_weight_dtype;
+  ce->vocab_chunk = k->vocab_chunk;
+  ce->flags = k->flags;
+  return check_problem(ce);
+}
+
+struct KLFwdPlan {
+  int64_t n_vt = 0;
+  size_t partials = 0, total = 0;
+  CompactPlan cp;
+};
+
+KLFwdPlan plan_kl_forward(const flce_problem* ce) {
+  KLFwdPlan f;
+  f.n_vt = cdiv(ce->v, is_tc(ce) ? flce::kBN : flce::kSimtTileV);
+  size_t off = align_up(static_cast<size_t>(ce->n) * f.n_vt * 16);
+  off = plan_compaction(ce, false, true, off, &f.cp);
+  f.total = off;
+  return f;
+}
+
+// KL inputs of the shared backward (null for the cross-entropy).
+struct KLArgs {
+  const void* q;      // teacher probabilities [N][V], input type
+  const float* qsum;  // per-row sum of q
+  int reduction;      // flce_kl_reduction
+};
+
+// The backward of both losses: the cross-entropy (kl == null) and the KL
+// divergence (kl != null: D from the teacher probabilities; targets are the
+// optional labels). `p` has been checked by the caller.
+flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* hidden,
+                          const void* weight, const void* bias, const int64_t* targets,
+                          const float* lse_rows, const int32_t* n_valid, const float* grad_out,
+                          void* grad_hidden, void* grad_weight, void* grad_bias,
+                          int32_t* err_word, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  flce_status st = FLCE_OK;
+  const bool bf16 = is_tc(p);  // tensor-core path (bf16 or fp16)
+  const size_t in_align = bf16 ? 16 : 4;
+  g_map_type = p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (weight == nullptr || grad_weight == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "weight and grad_weight are required");
+  if (p->has_bias && (bias == nullptr || grad_bias == nullptr))
+    return fail(FLCE_ERR_INVALID_ARG, "has_bias needs bias and grad_bias");
+  if (!p->has_bias && (bias != nullptr || grad_bias != nullptr))
+    return fail(FLCE_ERR_INVALID_ARG, "bias/grad_bias given but has_bias is 0");
+  if (p->n > 0) {
+    if (hidden == nullptr || lse_rows == nullptr || n_valid == nullptr || grad_out == nullptr ||
+        grad_hidden == nullptr)
+      return fail(FLCE_ERR_INVALID_ARG,
+                  "hidden, lse_rows, n_valid, grad_out and grad_hidden are required");
+    if (!aligned(hidden, in_align) || !aligned(grad_hidden, in_align))
+      return fail(FLCE_ERR_UNSUPPORTED, "hidden or grad_hidden is misaligned");
+    if (targets != nullptr && !aligned(targets, 8))
+      return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
+  }
+  if (!aligned(weight, in_align) || !aligned(grad_weight, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "weight or grad_weight is misaligned");
+  if (bias != nullptr && !aligned(bias, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
+  const BwdPlan plan = plan_backward(p, kl != nullptr);
+  st = check_workspace(workspace, workspace_bytes, plan.total);
+  if (st != FLCE_OK) return st;
+  DeviceInfo dev;
+  st = check_device(&dev);
+  if (st != FLCE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t gw_elem = p->grad_weight_dtype == FLCE_F32 ? 4 : 2;
+  cudaError_t e;
+  if (p->n == 0) {
+    e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(p->v) * p->h * gw_elem, s);
+    if (e == cudaSuccess && grad_bias != nullptr)
+      e = cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(p->v) * (bf16 ? 2 : 4), s);
+    return e == cudaSuccess ? FLCE_OK : cuda_fail(e, "cudaMemsetAsync");
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const flce::LogitXform xf = make_xform(p);
+  float* gb_partial = p->has_bias ? reinterpret_cast<float*>(ws + plan.gb) : nullptr;
+  // valid-row compaction (rows come from the targets, so none without them)
+  const bool compact = plan.cp.on && targets != nullptr;
+
+  if (bf16) {
+    void* dbuf = ws + plan.d;
+    float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
+    const int type = tc_type(p);
+    // fp16: D is stored times a power of two, undone by the gradient GEMMs
+    float* scales = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + plan.scales) : nullptr;
+    if (scales != nullptr) {
+      ProfScope ps("dlogits_scale", s);
+      // KL: |p Q - q| <= Q bounds D per row; "mean" also divides by V
+      const float extra_div =
+          (kl != nullptr && kl->reduction == FLCE_KL_MEAN) ? static_cast<float>(p->v) : 1.0f;
+      e = flce::launch_dlogits_scale(grad_out, n_valid, targets, p->n, p->ignore_index,
+                                     p->reduction, p->logit_scale, p->z_loss, lse_rows,
+                                     kl != nullptr ? kl->qsum : nullptr, extra_div, scales, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits scale kernel");
+    }
+    // valid-row compaction: rows of hidden, targets, lse, per-row upstream
+    // gradients (and KL row sums of q) are gathered; grad_hidden is
+    // scattered back
+    int32_t* row_map = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.row_map) : nullptr;
+    int32_t* n_kept = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.n_kept) : nullptr;
+    const void* rows_src = hidden;
+    const int64_t* rows_targets = targets;
+    const float* rows_lse = lse_rows;
+    const float* rows_grad = grad_out;
+    const float* rows_qsum = kl != nullptr ? kl->qsum : nullptr;
+    if (compact) {
+      flce::GatherParams gp{};
+      gp.lse = lse_rows;
+      gp.lse_c = reinterpret_cast<float*>(ws + plan.cp.lse_c);
+      if (p->reduction == FLCE_RED_NONE) {
+        gp.grad_rows = grad_out;
+        gp.grad_rows_c = reinterpret_cast<float*>(ws + plan.cp.grad_c);
+      }
+      if (kl != nullptr) {
+        gp.qsum = kl->qsum;
+        gp.qsum_c = reinterpret_cast<float*>(ws + plan.cp.qsum_c);
+      }
+      st = launch_compaction(p, plan.cp, ws, hidden, targets, flce::CompactParams{}, gp, s);
+      if (st != FLCE_OK) return st;
+      {
+        ProfScope ps("zero_ignored_rows", s);
+        e = flce::launch_zero_ignored_rows(targets, p->n, p->ignore_index, grad_hidden, p->h,
+                                           s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden zero kernel");
+      rows_src = ws + plan.cp.hidden_c;
+      rows_targets = reinterpret_cast<const int64_t*>(ws + plan.cp.targets_c);
+      rows_lse = gp.lse_c;
+      if (p->reduction == FLCE_RED_NONE) rows_grad = gp.grad_rows_c;
+      if (kl != nullptr) rows_qsum = gp.qsum_c;
+    }
+    CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
+    if (!make_map(&tm_h_k, "hidden", rows_src, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+        !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC) ||
+        !make_map(&tm_h_mn, "hidden^T", rows_src, p->h, p->n, p->h, 64, flce::kBK) ||
+        !make_map(&tm_w_mn, "weight^T", weight, p->h, p->v, p->h, 64, flce::kBK))
+      return FLCE_ERR_CUDA;
+    const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
+    for (int64_t c = 0; c < plan.n_chunks; ++c) {
+      const int64_t c0 = c * plan.chunk;
+      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
+      CUtensorMap tm_d_k, tm_d_mn;
+      if (!make_map(&tm_d_k, "dlogits", dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
+          !make_map(&tm_d_mn, "dlogits^T", dbuf, width, p->n, plan.chunk, 64, flce::kBK))
+        return FLCE_ERR_CUDA;
+
+      // 1. recompute the chunk's logits and form D
+      GemmGeom g1{};
+      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+      g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
+      g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+      g1.m_fastest = 1;
+      g1.group = kBandDlogits;
+      g1.b_mn0 = static_cast<int>(c0);
+      g1.dyn_rows = n_kept;
+      g1.dyn_axis = 0;
+      g1.err_word = err_word;
+      if (kl != nullptr) {
+        flce::DlogitsKLParams dp{};
+        dp.bias = bias;
+        dp.q = kl->q;
+        dp.q_vec = (p->v % 8 == 0 && aligned(kl->q, 16)) ? 1 : 0;
+        dp.row_map = row_map;
+        dp.labels = rows_targets;
+        dp.lse = rows_lse;
+        dp.qsum = rows_qsum;
+        dp.grad_out = rows_grad;
+        dp.n_counted = n_valid;
+        dp.d = dbuf;
+        dp.ldd = plan.chunk;
+        dp.dscale = scales;
+        dp.gb_partial = gb_partial;
+        dp.gb_ld = p->v;
+        dp.n_rows = p->n;
+        dp.n_rows_dyn = n_kept;
+        dp.v = p->v;
+        dp.ignore_index = p->ignore_index;
+        dp.c0 = static_cast<int>(c0);
+        dp.width = static_cast<int>(width);
+        dp.reduction = kl->reduction;
+        dp.xf = xf;
+        ProfScope ps("bwd_dlogits_kl", s);
+        e = flce::launch_tc_dlogits_kl(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
+      } else {
+        flce::DlogitsParams dp{};
+        dp.bias = bias;
+        dp.targets = rows_targets;
+        dp.lse = rows_lse;
+        dp.grad_out = rows_grad;
+        dp.n_valid = n_valid;
+        dp.d = dbuf;
+        dp.ldd = plan.chunk;
+        dp.dscale = scales;
+        dp.gb_partial = gb_partial;
+        dp.gb_ld = p->v;
+        dp.n_rows = p->n;
+        dp.n_rows_dyn = n_kept;
+        dp.v = p->v;
+        dp.ignore_index = p->ignore_index;
+        dp.c0 = static_cast<int>(c0);
+        dp.width = static_cast<int>(width);
+        dp.reduction = p->reduction;
+        dp.label_smoothing = p->label_smoothing;
+        dp.z_loss = p->z_loss;
+        dp.xf = xf;
+        {
+          ProfScope ps("bwd_dlogits", s);
+          e = flce::launch_tc_dlogits(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
+        }
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
+
+      // 2. grad_weight[c0 : c0+width] = D^T @ hidden
+      GemmGeom g2{};
+      g2.m_tiles = static_cast<int>(cdiv(width, flce::kTileRowsTC));
+      g2.n_tiles = h_tiles;
+      g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
+      g2.m_fastest = 0;
+      g2.dyn_rows = n_kept;  // the contraction runs over the kept rows
+      g2.dyn_axis = 1;
+      g2.err_word = err_word;
+      flce::StoreRowsParams sp{};
+      sp.out = grad_weight;
+      sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
+      sp.out_scale = scales != nullptr ? scales + 1 : nullptr;
+      sp.ld = p->h;
+      sp.rows = width;
+      sp.row0 = c0;
+      sp.cols = static_cast<int>(p->h);
+      {
+        ProfScope ps("bwd_grad_weight", s);
+        e = flce::launch_tc_grad_weight(type, tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
+
+      // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
+      GemmGeom g3{};
+      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+      g3.n_tiles = h_tiles;
+      g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
+      g3.m_fastest = 1;
+      g3.group = kBandGradHidden;
+      g3.b_k0 = static_cast<int>(c0);
+      g3.dyn_rows = n_kept;
+      g3.dyn_axis = 0;
+      g3.err_word = err_word;
+      flce::AccRowsParams ap{};
+      ap.acc = acc;
+      ap.out = grad_hidden;
+      ap.out_scale = scales != nullptr ? scales + 1 : nullptr;
+      if (plan.n_chunks == 1)
+        ap.mode = flce::kAccStoreOut;
+      else if (c == 0)
+        ap.mode = flce::kAccStore;
+      else if (c == plan.n_chunks - 1)
+        ap.mode = flce::kAccAddOut;
+      else
+        ap.mode = flce::kAccAdd;
+      ap.ld = p->h;
+      ap.rows = p->n;
+      ap.rows_dyn = n_kept;
+      ap.row_map = row_map;
+      ap.cols = static_cast<int>(p->h);
+      {
+        ProfScope ps("bwd_grad_hidden", s);
+        e = flce::launch_tc_grad_hidden(type, tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
+    }
+  } else {
+    float* dbuf = reinterpret_cast<float*>(ws + plan.d);
+    for (int64_t c = 0; c < plan.n_chunks; ++c) {
+      const int64_t c0 = c * plan.chunk;
+      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
+      flce::SimtDlogitsParams dp{};
+      dp.hidden = static_cast<const float*>(hidden);
+      dp.weight = static_cast<const float*>(weight);
+      dp.bias = static_cast<const float*>(bias);
+      dp.q = kl != nullptr ? static_cast<const float*>(kl->q) : nullptr;
+      dp.qsum = kl != nullptr ? kl->qsum : nullptr;
+      dp.targets = targets;
+      dp.lse = lse_rows;
+      dp.grad_out = grad_out;
+      dp.n_valid = n_valid;
+      dp.d = dbuf;
+      dp.ldd = plan.chunk;
+      dp.gb_partial = gb_partial;
+      dp.gb_ld = p->v;
+      dp.n = p->n;
+      dp.h = p->h;
+      dp.v = p->v;
+      dp.ignore_index = p->ignore_index;
+      dp.c0 = c0;
+      dp.width = width;
+      dp.reduction = kl != nullptr ? kl->reduction : p->reduction;
+      dp.label_smoothing = p->label_smoothing;
+      dp.z_loss = p->z_loss;
+      dp.xf = xf;
+      {
+        ProfScope ps("bwd_dlogits_f32", s);
+        e = flce::launch_simt_dlogits(dp, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 dlogits kernel");
+      // grad_weight rows [c0, c0+width) = D^T @ hidden
+      {
+        ProfScope ps("bwd_grad_weight_f32", s);
+        e = flce::launch_simt_gemm(width, p->h, p->n, dbuf, 1, plan.chunk,
+                                 static_cast<const float*>(hidden), p->h, 1,
+                                   static_cast<float*>(grad_weight) + c0 * p->h, p->h, 0, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_weight kernel");
+      // grad_hidden (+)= D @ weight[c0 : c0+width]
+      {
+        ProfScope ps("bwd_grad_hidden_f32", s);
+        e = flce::launch_simt_gemm(p->n, p->h, width, dbuf, plan.chunk, 1,
+                                 static_cast<const float*>(weight) + c0 * p->h, p->h, 1,
+                                   static_cast<float*>(grad_hidden), p->h, c > 0 ? 1 : 0, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_hidden kernel");
+    }
+  }
+  if (p->has_bias) {
+    ProfScope ps("bwd_bias_reduce", s);
+    const int32_t* n_dyn =
+        compact ? reinterpret_cast<const int32_t*>(ws + plan.cp.n_kept) : nullptr;
+    e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias,
+                                 bf16 ? tc_type(p) : 0, n_dyn, flce::kBM, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
+  }
+  return FLCE_OK;
+}
+
 
 }  // namespace
 
@@ -519,40 +930,16 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
     const int64_t* rows_targets = targets;
     if (compact) {
       flce::CompactParams cp{};
-      cp.targets = targets;
-      cp.n = p->n;
-      cp.ignore_index = p->ignore_index;
-      cp.row_map = row_map;
-      cp.n_kept = n_kept;
       cp.loss_rows = loss_rows;
       cp.lse_rows = lse_rows;
       cp.correct_ws = correct_ws;
       cp.entropy_ws = entropy_ws;
       cp.correct_rows = correct_rows;
       cp.entropy_rows = entropy_rows;
-      flce::GatherParams gp{};
-      gp.hidden = hidden;
-      gp.n = p->n;
-      gp.h = p->h;
-      gp.row_map = row_map;
-      gp.n_kept = n_kept;
-      gp.pad_rows = flce::kTileRowsTC;
-      gp.hidden_c = ws + plan.cp.hidden_c;
-      gp.targets = targets;
-      gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
-      gp.ignore_index = p->ignore_index;
-      {
-        ProfScope ps("compact_rows", s);
-        e = flce::launch_compact_rows(cp, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "row compaction kernel");
-      {
-        ProfScope ps("gather_rows", s);
-        e = flce::launch_gather_rows(gp, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
-      rows_src = gp.hidden_c;
-      rows_targets = gp.targets_c;
+      st = launch_compaction(p, plan.cp, ws, hidden, targets, cp, flce::GatherParams{}, s);
+      if (st != FLCE_OK) return st;
+      rows_src = ws + plan.cp.hidden_c;
+      rows_targets = reinterpret_cast<const int64_t*>(ws + plan.cp.targets_c);
     }
     if (bf16) {
       CUtensorMap tm_h, tm_w;
@@ -653,30 +1040,62 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   g_err[0] = 0;
   flce_status st = check_problem(p);
   if (st != FLCE_OK) return st;
-  const bool bf16 = is_tc(p);  // tensor-core path (bf16 or fp16)
-  const size_t in_align = bf16 ? 16 : 4;
+  if (p->n > 0 && targets == nullptr) return fail(FLCE_ERR_INVALID_ARG, "targets is NULL");
+  return backward_impl(p, nullptr, hidden, weight, bias, targets, lse_rows, n_valid, grad_out,
+                       grad_hidden, grad_weight, grad_bias, err_word, workspace, workspace_bytes,
+                       stream);
+}
+
+// ---------------------------------------------------------------- KL
+size_t flce_kl_forward_workspace_size(const flce_kl_problem* p) {
+  flce_problem ce;
+  if (check_kl_problem(p, &ce) != FLCE_OK) return 0;
+  return plan_kl_forward(&ce).total;
+}
+
+size_t flce_kl_backward_workspace_size(const flce_kl_problem* p) {
+  flce_problem ce;
+  if (check_kl_problem(p, &ce) != FLCE_OK) return 0;
+  return plan_backward(&ce, true).total;
+}
+
+flce_status flce_kl_forward(const flce_kl_problem* k, const void* hidden, const void* weight,
+                            const void* bias, const void* target_probs, const int64_t* labels,
+                            float* loss_rows, float* lse_rows, float* qsum_rows, float* loss_out,
+                            int32_t* n_counted, int32_t* err_word, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  flce_problem ce;
+  flce_problem* p = &ce;
+  flce_status st = check_kl_problem(k, p);
+  if (st != FLCE_OK) return st;
+  const bool tc = is_tc(p);
+  const size_t in_align = tc ? 16 : 4;
+  const size_t elem = tc ? 2 : 4;
   g_map_type = p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (weight == nullptr || grad_weight == nullptr)
-    return fail(FLCE_ERR_INVALID_ARG, "weight and grad_weight are required");
-  if (p->has_bias && (bias == nullptr || grad_bias == nullptr))
-    return fail(FLCE_ERR_INVALID_ARG, "has_bias needs bias and grad_bias");
-  if (!p->has_bias && (bias != nullptr || grad_bias != nullptr))
-    return fail(FLCE_ERR_INVALID_ARG, "bias/grad_bias given but has_bias is 0");
+  if (weight == nullptr) return fail(FLCE_ERR_INVALID_ARG, "weight is NULL");
+  if (n_counted == nullptr) return fail(FLCE_ERR_INVALID_ARG, "n_counted is NULL");
+  if (k->reduction != FLCE_KL_NONE && loss_out == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "loss_out is NULL (required unless reduction is none)");
+  if (p->has_bias && bias == nullptr) return fail(FLCE_ERR_INVALID_ARG, "has_bias but bias is NULL");
+  if (!p->has_bias && bias != nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "bias given but has_bias is 0");
   if (p->n > 0) {
-    if (hidden == nullptr || targets == nullptr || lse_rows == nullptr || n_valid == nullptr ||
-        grad_out == nullptr || grad_hidden == nullptr)
+    if (hidden == nullptr || target_probs == nullptr || loss_rows == nullptr ||
+        lse_rows == nullptr || qsum_rows == nullptr)
       return fail(FLCE_ERR_INVALID_ARG,
-                  "hidden, targets, lse_rows, n_valid, grad_out and grad_hidden are required");
-    if (!aligned(hidden, in_align) || !aligned(grad_hidden, in_align))
-      return fail(FLCE_ERR_UNSUPPORTED, "hidden or grad_hidden is misaligned");
-    if (!aligned(targets, 8)) return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
+                  "hidden, target_probs, loss_rows, lse_rows and qsum_rows are required");
+    if (!aligned(hidden, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "hidden is misaligned");
+    if (!aligned(target_probs, elem))
+      return fail(FLCE_ERR_UNSUPPORTED, "target_probs is misaligned");
+    if (labels != nullptr && !aligned(labels, 8))
+      return fail(FLCE_ERR_UNSUPPORTED, "labels is misaligned");
   }
-  if (!aligned(weight, in_align) || !aligned(grad_weight, in_align))
-    return fail(FLCE_ERR_UNSUPPORTED, "weight or grad_weight is misaligned");
+  if (!aligned(weight, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "weight is misaligned");
   if (bias != nullptr && !aligned(bias, in_align))
     return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
-  const BwdPlan plan = plan_backward(p);
+  const KLFwdPlan plan = plan_kl_forward(p);
   st = check_workspace(workspace, workspace_bytes, plan.total);
   if (st != FLCE_OK) return st;
   DeviceInfo dev;
@@ -684,255 +1103,126 @@ flce_status flce_backward(const flce_problem* p, const void* hidden, const void*
   if (st != FLCE_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t gw_elem = p->grad_weight_dtype == FLCE_F32 ? 4 : 2;
-  cudaError_t e;
-  if (p->n == 0) {
-    e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(p->v) * p->h * gw_elem, s);
-    if (e == cudaSuccess && grad_bias != nullptr)
-      e = cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(p->v) * (bf16 ? 2 : 4), s);
-    return e == cudaSuccess ? FLCE_OK : cuda_fail(e, "cudaMemsetAsync");
-  }
-
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float4* partials = reinterpret_cast<float4*>(ws + plan.partials);
   const flce::LogitXform xf = make_xform(p);
-  float* gb_partial = p->has_bias ? reinterpret_cast<float*>(ws + plan.gb) : nullptr;
-
-  if (bf16) {
-    void* dbuf = ws + plan.d;
-    float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
-    const int type = tc_type(p);
-    // fp16: D is stored times a power of two, undone by the gradient GEMMs
-    float* scales = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + plan.scales) : nullptr;
-    if (scales != nullptr) {
-      ProfScope ps("dlogits_scale", s);
-      e = flce::launch_dlogits_scale(grad_out, n_valid, targets, p->n, p->ignore_index,
-                                     p->reduction, p->logit_scale, p->z_loss, lse_rows, scales,
-                                     s);
-      if (e != cudaSuccess) return cuda_fail(e, "dlogits scale kernel");
-    }
-    // valid-row compaction: rows of hidden, targets, lse and per-row
-    // upstream gradients are gathered; grad_hidden is scattered back
-    const bool compact = plan.cp.on;
+  cudaError_t e;
+  if (p->n > 0) {
+    const bool compact = plan.cp.on && labels != nullptr;
     int32_t* row_map = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.row_map) : nullptr;
     int32_t* n_kept = compact ? reinterpret_cast<int32_t*>(ws + plan.cp.n_kept) : nullptr;
     const void* rows_src = hidden;
-    const int64_t* rows_targets = targets;
-    const float* rows_lse = lse_rows;
-    const float* rows_grad = grad_out;
+    const int64_t* rows_labels = labels;
     if (compact) {
       flce::CompactParams cp{};
-      cp.targets = targets;
-      cp.n = p->n;
-      cp.ignore_index = p->ignore_index;
-      cp.row_map = row_map;
-      cp.n_kept = n_kept;
-      flce::GatherParams gp{};
-      gp.hidden = hidden;
-      gp.n = p->n;
-      gp.h = p->h;
-      gp.row_map = row_map;
-      gp.n_kept = n_kept;
-      gp.pad_rows = flce::kTileRowsTC;
-      gp.hidden_c = ws + plan.cp.hidden_c;
-      gp.targets = targets;
-      gp.targets_c = reinterpret_cast<int64_t*>(ws + plan.cp.targets_c);
-      gp.ignore_index = p->ignore_index;
-      gp.lse = lse_rows;
-      gp.lse_c = reinterpret_cast<float*>(ws + plan.cp.lse_c);
-      if (p->reduction == FLCE_RED_NONE) {
-        gp.grad_rows = grad_out;
-        gp.grad_rows_c = reinterpret_cast<float*>(ws + plan.cp.grad_c);
-      }
-      {
-        ProfScope ps("compact_rows", s);
-        e = flce::launch_compact_rows(cp, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "row compaction kernel");
-      {
-        ProfScope ps("gather_rows", s);
-        e = flce::launch_gather_rows(gp, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "row gather kernel");
-      {
-        ProfScope ps("zero_ignored_rows", s);
-        e = flce::launch_zero_ignored_rows(targets, p->n, p->ignore_index, grad_hidden, p->h,
-                                           s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden zero kernel");
-      rows_src = gp.hidden_c;
-      rows_targets = gp.targets_c;
-      rows_lse = gp.lse_c;
-      if (p->reduction == FLCE_RED_NONE) rows_grad = gp.grad_rows_c;
+      cp.loss_rows = loss_rows;
+      cp.lse_rows = lse_rows;
+      cp.qsum_rows = qsum_rows;
+      st = launch_compaction(p, plan.cp, ws, hidden, labels, cp, flce::GatherParams{}, s);
+      if (st != FLCE_OK) return st;
+      rows_src = ws + plan.cp.hidden_c;
+      rows_labels = reinterpret_cast<const int64_t*>(ws + plan.cp.targets_c);
     }
-    CUtensorMap tm_h_k, tm_w_k, tm_h_mn, tm_w_mn;
-    if (!make_map(&tm_h_k, "hidden", rows_src, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
-        !make_map(&tm_w_k, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC) ||
-        !make_map(&tm_h_mn, "hidden^T", rows_src, p->h, p->n, p->h, 64, flce::kBK) ||
-        !make_map(&tm_w_mn, "weight^T", weight, p->h, p->v, p->h, 64, flce::kBK))
-      return FLCE_ERR_CUDA;
-    const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
-    for (int64_t c = 0; c < plan.n_chunks; ++c) {
-      const int64_t c0 = c * plan.chunk;
-      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
-      CUtensorMap tm_d_k, tm_d_mn;
-      if (!make_map(&tm_d_k, "dlogits", dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
-          !make_map(&tm_d_mn, "dlogits^T", dbuf, width, p->n, plan.chunk, 64, flce::kBK))
+    if (tc) {
+      CUtensorMap tm_h, tm_w;
+      if (!make_map(&tm_h, "hidden", rows_src, p->h, p->n, p->h, flce::kBK, flce::kBM) ||
+          !make_map(&tm_w, "weight", weight, p->h, p->v, p->h, flce::kBK, flce::kBLoadRowsTC))
         return FLCE_ERR_CUDA;
-
-      // 1. recompute the chunk's logits and form D
-      GemmGeom g1{};
-      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
-      g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
-      g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
-      g1.m_fastest = 1;
-      g1.group = kBandDlogits;
-      g1.b_mn0 = static_cast<int>(c0);
-      g1.dyn_rows = n_kept;
-      g1.dyn_axis = 0;
-      g1.err_word = err_word;
-      flce::DlogitsParams dp{};
-      dp.bias = bias;
-      dp.targets = rows_targets;
-      dp.lse = rows_lse;
-      dp.grad_out = rows_grad;
-      dp.n_valid = n_valid;
-      dp.d = dbuf;
-      dp.ldd = plan.chunk;
-      dp.dscale = scales;
-      dp.gb_partial = gb_partial;
-      dp.gb_ld = p->v;
-      dp.n_rows = p->n;
-      dp.n_rows_dyn = n_kept;
-      dp.v = p->v;
-      dp.ignore_index = p->ignore_index;
-      dp.c0 = static_cast<int>(c0);
-      dp.width = static_cast<int>(width);
-      dp.reduction = p->reduction;
-      dp.label_smoothing = p->label_smoothing;
-      dp.z_loss = p->z_loss;
-      dp.xf = xf;
-      {
-        ProfScope ps("bwd_dlogits", s);
-        e = flce::launch_tc_dlogits(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
-
-      // 2. grad_weight[c0 : c0+width] = D^T @ hidden
-      GemmGeom g2{};
-      g2.m_tiles = static_cast<int>(cdiv(width, flce::kTileRowsTC));
-      g2.n_tiles = h_tiles;
-      g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
-      g2.m_fastest = 0;
-      g2.dyn_rows = n_kept;  // the contraction runs over the kept rows
-      g2.dyn_axis = 1;
-      g2.err_word = err_word;
-      flce::StoreRowsParams sp{};
-      sp.out = grad_weight;
-      sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
-      sp.out_scale = scales != nullptr ? scales + 1 : nullptr;
-      sp.ld = p->h;
-      sp.rows = width;
-      sp.row0 = c0;
-      sp.cols = static_cast<int>(p->h);
-      {
-        ProfScope ps("bwd_grad_weight", s);
-        e = flce::launch_tc_grad_weight(type, tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
-
-      // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
-      GemmGeom g3{};
-      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
-      g3.n_tiles = h_tiles;
-      g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
-      g3.m_fastest = 1;
-      g3.group = kBandGradHidden;
-      g3.b_k0 = static_cast<int>(c0);
-      g3.dyn_rows = n_kept;
-      g3.dyn_axis = 0;
-      g3.err_word = err_word;
-      flce::AccRowsParams ap{};
-      ap.acc = acc;
-      ap.out = grad_hidden;
-      ap.out_scale = scales != nullptr ? scales + 1 : nullptr;
-      if (plan.n_chunks == 1)
-        ap.mode = flce::kAccStoreOut;
-      else if (c == 0)
-        ap.mode = flce::kAccStore;
-      else if (c == plan.n_chunks - 1)
-        ap.mode = flce::kAccAddOut;
-      else
-        ap.mode = flce::kAccAdd;
-      ap.ld = p->h;
-      ap.rows = p->n;
-      ap.rows_dyn = n_kept;
-      ap.row_map = row_map;
-      ap.cols = static_cast<int>(p->h);
-      {
-        ProfScope ps("bwd_grad_hidden", s);
-        e = flce::launch_tc_grad_hidden(type, tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
+      GemmGeom g{};
+      g.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+      g.n_tiles = static_cast<int>(cdiv(p->v, flce::kBN));
+      g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+      g.m_fastest = 1;
+      g.group = kBandForward;
+      g.dyn_rows = n_kept;
+      g.dyn_axis = 0;
+      g.err_word = err_word;
+      flce::FwdKLParams fp{};
+      fp.bias = bias;
+      fp.q = target_probs;
+      fp.q_vec = (p->v % 8 == 0 && aligned(target_probs, 16)) ? 1 : 0;
+      fp.row_map = row_map;
+      fp.partials = partials;
+      fp.n_rows = p->n;
+      fp.n_rows_dyn = n_kept;
+      fp.v = p->v;
+      fp.n_vt = plan.n_vt;
+      fp.eps = k->eps;
+      fp.xf = xf;
+      ProfScope ps("fwd_kl", s);
+      e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, dev.sms, s);
+      if (e != cudaSuccess) return cuda_fail(e, "KL forward kernel");
+    } else {
+      flce::SimtFwdParams fp{};
+      fp.hidden = static_cast<const float*>(hidden);
+      fp.weight = static_cast<const float*>(weight);
+      fp.bias = static_cast<const float*>(bias);
+      fp.q = static_cast<const float*>(target_probs);
+      fp.eps = k->eps;
+      fp.partials = partials;
+      fp.n = p->n;
+      fp.h = p->h;
+      fp.v = p->v;
+      fp.n_vt = plan.n_vt;
+      fp.xf = xf;
+      ProfScope ps("fwd_kl_f32", s);
+      e = flce::launch_simt_fwd(fp, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 KL forward kernel");
     }
-  } else {
-    float* dbuf = reinterpret_cast<float*>(ws + plan.d);
-    for (int64_t c = 0; c < plan.n_chunks; ++c) {
-      const int64_t c0 = c * plan.chunk;
-      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
-      flce::SimtDlogitsParams dp{};
-      dp.hidden = static_cast<const float*>(hidden);
-      dp.weight = static_cast<const float*>(weight);
-      dp.bias = static_cast<const float*>(bias);
-      dp.targets = targets;
-      dp.lse = lse_rows;
-      dp.grad_out = grad_out;
-      dp.n_valid = n_valid;
-      dp.d = dbuf;
-      dp.ldd = plan.chunk;
-      dp.gb_partial = gb_partial;
-      dp.gb_ld = p->v;
-      dp.n = p->n;
-      dp.h = p->h;
-      dp.v = p->v;
-      dp.ignore_index = p->ignore_index;
-      dp.c0 = c0;
-      dp.width = width;
-      dp.reduction = p->reduction;
-      dp.label_smoothing = p->label_smoothing;
-      dp.z_loss = p->z_loss;
-      dp.xf = xf;
-      {
-        ProfScope ps("bwd_dlogits_f32", s);
-        e = flce::launch_simt_dlogits(dp, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "fp32 dlogits kernel");
-      // grad_weight rows [c0, c0+width) = D^T @ hidden
-      {
-        ProfScope ps("bwd_grad_weight_f32", s);
-        e = flce::launch_simt_gemm(width, p->h, p->n, dbuf, 1, plan.chunk,
-                                 static_cast<const float*>(hidden), p->h, 1,
-                                   static_cast<float*>(grad_weight) + c0 * p->h, p->h, 0, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_weight kernel");
-      // grad_hidden (+)= D @ weight[c0 : c0+width]
-      {
-        ProfScope ps("bwd_grad_hidden_f32", s);
-        e = flce::launch_simt_gemm(p->n, p->h, width, dbuf, plan.chunk, 1,
-                                 static_cast<const float*>(weight) + c0 * p->h, p->h, 1,
-                                   static_cast<float*>(grad_hidden), p->h, c > 0 ? 1 : 0, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "fp32 grad_hidden kernel");
+    flce::MergeKLParams mp{};
+    mp.partials = partials;
+    mp.labels = rows_labels;
+    mp.row_map = row_map;
+    mp.n_dyn = n_kept;
+    mp.n = p->n;
+    mp.n_vt = plan.n_vt;
+    mp.ignore_index = p->ignore_index;
+    mp.loss_rows = loss_rows;
+    mp.lse_rows = lse_rows;
+    mp.qsum_rows = qsum_rows;
+    {
+      ProfScope ps("merge_kl", s);
+      e = flce::launch_merge_kl(mp, s);
     }
+    if (e != cudaSuccess) return cuda_fail(e, "KL row merge kernel");
   }
-  if (p->has_bias) {
-    ProfScope ps("bwd_bias_reduce", s);
-    const int32_t* n_dyn =
-        plan.cp.on ? reinterpret_cast<const int32_t*>(ws + plan.cp.n_kept) : nullptr;
-    e = flce::launch_bias_reduce(gb_partial, plan.gb_parts, p->v, p->v, grad_bias,
-                                 bf16 ? tc_type(p) : 0, n_dyn, flce::kBM, s);
-    if (e != cudaSuccess) return cuda_fail(e, "grad_bias kernel");
+  flce::FinalizeKLParams fin{};
+  fin.loss_rows = loss_rows;
+  fin.labels = labels;
+  fin.n = p->n;
+  fin.v = p->v;
+  fin.ignore_index = p->ignore_index;
+  fin.reduction = k->reduction;
+  fin.loss_out = k->reduction == FLCE_KL_NONE ? nullptr : loss_out;
+  fin.n_counted = n_counted;
+  {
+    ProfScope ps("finalize_kl", s);
+    e = flce::launch_finalize_kl(fin, s);
   }
+  if (e != cudaSuccess) return cuda_fail(e, "KL finalize kernel");
   return FLCE_OK;
+}
+
+flce_status flce_kl_backward(const flce_kl_problem* k, const void* hidden, const void* weight,
+                             const void* bias, const void* target_probs, const int64_t* labels,
+                             const float* lse_rows, const float* qsum_rows,
+                             const int32_t* n_counted, const float* grad_out, void* grad_hidden,
+                             void* grad_weight, void* grad_bias, int32_t* err_word,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  flce_problem ce;
+  flce_status st = check_kl_problem(k, &ce);
+  if (st != FLCE_OK) return st;
+  if (ce.n > 0) {
+    if (target_probs == nullptr || qsum_rows == nullptr)
+      return fail(FLCE_ERR_INVALID_ARG, "target_probs and qsum_rows are required");
+    if (!aligned(target_probs, is_tc(&ce) ? 2 : 4))
+      return fail(FLCE_ERR_UNSUPPORTED, "target_probs is misaligned");
+  }
+  const KLArgs kl{target_probs, qsum_rows, k->reduction};
+  return backward_impl(&ce, &kl, hidden, weight, bias, labels, lse_rows, n_counted, grad_out,
+                       grad_hidden, grad_weight, grad_bias, err_word, workspace, workspace_bytes,
+                       stream);
 }
 
 // Forward pass for callers that cannot provide a workspace: the same kernels

@@ -64,6 +64,48 @@ struct DlogitsParams {
   LogitXform xf;
 };
 
+// Fused linear KL divergence: forward statistics per (row, vocabulary tile)
+// are (m, s, A, Q): the running max and sum e^{z-m} of z, A = sum q (log
+// max(q, eps) - z) and Q = sum q over the tile's columns.
+struct FwdKLParams {
+  const void* bias;
+  const void* q;              // [N][V] teacher probabilities, input type
+  int q_vec;                  // 1: rows of q are 16-byte aligned (V % 8 == 0)
+  const int32_t* row_map;     // original row of each (compacted) row, or null
+  float4* partials;
+  int64_t n_rows;
+  const int32_t* n_rows_dyn;
+  int64_t v;
+  int64_t n_vt;
+  float eps;
+  LogitXform xf;              // scale = 1 / temperature
+};
+
+struct DlogitsKLParams {
+  const void* bias;
+  const void* q;
+  int q_vec;
+  const int32_t* row_map;
+  const int64_t* labels;      // of the (compacted) rows, or null: every row counts
+  const float* lse;
+  const float* qsum;
+  const float* grad_out;      // scalar, or per (compacted) row for reduction none
+  const int32_t* n_counted;
+  void* d;
+  int64_t ldd;
+  const float* dscale;
+  float* gb_partial;
+  int64_t gb_ld;
+  int64_t n_rows;
+  const int32_t* n_rows_dyn;
+  int64_t v;
+  int64_t ignore_index;
+  int c0;
+  int width;
+  int reduction;              // flce_kl_reduction
+  LogitXform xf;
+};
+
 struct StoreRowsParams {
   void* out;  // input type, or fp32 when out_f32
   int out_f32;
@@ -89,6 +131,13 @@ struct AccRowsParams {
 };
 
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
+                             const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                             const FwdKLParams& p, int sms, cudaStream_t s);
+cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
+                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                                 const DlogitsKLParams& p, int sms, cudaStream_t s);
+
 // `type` is a TcType; every launcher runs the CTA-pair GEMM of that type.
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
@@ -103,21 +152,53 @@ cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
                                   const CUtensorMap& tm_weight_mn, const GemmGeom& g,
                                   const AccRowsParams& p, int sms, cudaStream_t s);
 
+// KL per-row merge and the scalar loss.
+struct MergeKLParams {
+  const float4* partials;
+  const int64_t* labels;  // of the (compacted) rows, or null
+  const int32_t* row_map;
+  const int32_t* n_dyn;
+  int64_t n, n_vt, ignore_index;
+  float* loss_rows;
+  float* lse_rows;
+  float* qsum_rows;
+};
+cudaError_t launch_merge_kl(const MergeKLParams& p, cudaStream_t s);
+
+struct FinalizeKLParams {
+  const float* loss_rows;
+  const int64_t* labels;  // original rows, or null
+  int64_t n, v, ignore_index;
+  int reduction;          // flce_kl_reduction
+  float* loss_out;
+  int32_t* n_counted;
+};
+cudaError_t launch_finalize_kl(const FinalizeKLParams& p, cudaStream_t s);
+
 // fp16 backward: D is stored as D * dscale with dscale = 2^k chosen so that
 // |D * dscale| < 16384 (the row upstream gradient times logit_scale bounds
 // |D|; fp16's largest finite value is 65504) and entries down to ~1e-8 of
 // the largest stay normal; out_scale = 1 / dscale exactly. Writes both to
 // `scales` [2].
+// `reduction` uses the cross-entropy codes (0 none, 1 sum, 2 mean over
+// n_valid); `extra_div` further divides the uniform row gradient (V for the
+// KL "mean"). With `row_bound` (KL: per-row sum of q), |D| is bounded by the
+// row gradient times logit_scale times max row_bound instead of (1 + 2 |z_loss|
+// max |lse|). Rows whose target (label) is ignore_index are skipped; targets
+// may be null (every row counts).
 cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
                                  const int64_t* targets, int64_t n, int64_t ignore_index,
                                  int reduction, float logit_scale, float z_loss,
-                                 const float* lse_rows, float* scales, cudaStream_t s);
+                                 const float* lse_rows, const float* row_bound, float extra_div,
+                                 float* scales, cudaStream_t s);
 
 // fp32 (SIMT) path
 struct SimtFwdParams {
   const float* hidden;
   const float* weight;
   const float* bias;
+  const float* q;  // KL: teacher probabilities [N][V]; null for the cross-entropy
+  float eps;
   const int64_t* targets;
   float4* partials;
   float* zsum;
@@ -131,7 +212,9 @@ struct SimtDlogitsParams {
   const float* hidden;
   const float* weight;
   const float* bias;
-  const int64_t* targets;
+  const float* q;     // KL: teacher probabilities [N][V]; null for the cross-entropy
+  const float* qsum;  // KL: per-row sum of q
+  const int64_t* targets;  // cross-entropy targets, or KL labels (nullable for KL)
   const float* lse;
   const float* grad_out;
   const int32_t* n_valid;
@@ -207,6 +290,7 @@ struct CompactParams {
   float* entropy_ws;
   int32_t* correct_rows;
   float* entropy_rows;
+  float* qsum_rows;  // KL forward (nullable); correct_ws / entropy_ws are nullable too
 };
 cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t s);
 
@@ -224,6 +308,8 @@ struct GatherParams {
   float* lse_c;
   const float* grad_rows;  // backward, reduction none (nullable)
   float* grad_rows_c;
+  const float* qsum;  // KL backward: per-row sum of q (nullable)
+  float* qsum_c;
 };
 cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s);
 

@@ -140,6 +140,18 @@ __device__ __forceinline__ float row_grad(int64_t t, int64_t ignore_index, int64
   return grad_out[0] / static_cast<float>(n_valid[0]);  // mean (n_valid >= 1 here)
 }
 
+// Upstream gradient of row `row`'s KL term (reduction codes: 0 none, 1 sum,
+// 2 batchmean, 3 mean); 0 for rows not counted.
+__device__ __forceinline__ float kl_row_grad(bool counted, int reduction, const float* grad_out,
+                                             const int32_t* n_counted, int64_t v, int64_t row) {
+  if (!counted) return 0.0f;
+  if (reduction == 0) return grad_out[row];
+  float g = grad_out[0];
+  if (reduction >= 2) g /= static_cast<float>(n_counted[0]);  // n_counted >= 1 here
+  if (reduction == 3) g /= static_cast<float>(v);
+  return g;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -6,7 +6,10 @@
 //               entropy with the same rescaling);
 //   finalize    the reduced loss, n_valid and the two scalar metrics, in a
 //               fixed summation order (bitwise repeatable);
-//   bias_reduce grad_bias from per-row-tile column partial sums, fixed order.
+//   bias_reduce grad_bias from per-row-tile column partial sums, fixed order;
+//   merge_kl / finalize_kl  the same two steps for the fused linear KL
+//               divergence (FusedLinearKLDivLoss pull request, Liger-Kernel
+//               #1423, Details: loss = sum q (log q - z) + lse * sum q).
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -117,6 +120,77 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   }
 }
 
+// KL: a row's (m, s) merge as softmax statistics; A = sum q (log max(q,
+// eps) - z) and Q = sum q are plain sums. loss = A + lse * Q on counted rows.
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kl_kernel(const MergeKLParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
+  const int64_t n_rows = p.n_dyn != nullptr ? static_cast<int64_t>(*p.n_dyn) : p.n;
+  if (row >= n_rows) return;  // warp-uniform
+  const float4* part = p.partials + row * p.n_vt;
+  RowStats st;
+  st.init();
+  float a_sum = 0.0f, q_sum = 0.0f;
+  for (int64_t u = lane; u < p.n_vt; u += 32) {
+    const float4 v = part[u];
+    RowStats x;
+    x.m = v.x;
+    x.s = v.y;
+    x.t = 0.0f;
+    x.a = 0;
+    st = merge_stats(st, x);
+    a_sum += v.z;
+    q_sum += v.w;
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    st = merge_stats(st, shfl_xor_stats(st, off));
+    a_sum += __shfl_xor_sync(0xffffffffu, a_sum, off);
+    q_sum += __shfl_xor_sync(0xffffffffu, q_sum, off);
+  }
+  if (lane != 0) return;
+  const float lse = st.m + logf(st.s);
+  const bool counted = p.labels == nullptr || p.labels[row] != p.ignore_index;
+  const int64_t orig = p.row_map != nullptr ? static_cast<int64_t>(p.row_map[row]) : row;
+  p.loss_rows[orig] = counted ? fmaf(lse, q_sum, a_sum) : 0.0f;
+  p.lse_rows[orig] = lse;
+  p.qsum_rows[orig] = q_sum;
+}
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kl_kernel(const FinalizeKLParams p) {
+  __shared__ double s_loss[kFinThreads];
+  __shared__ long long s_nc[kFinThreads];
+  const int tid = threadIdx.x;
+  double ls = 0.0;
+  long long nc = 0;
+  for (int64_t i = tid; i < p.n; i += kFinThreads) {
+    if (p.labels != nullptr && p.labels[i] == p.ignore_index) continue;
+    ++nc;
+    ls += static_cast<double>(p.loss_rows[i]);
+  }
+  s_loss[tid] = ls;
+  s_nc[tid] = nc;
+  __syncthreads();
+  for (int w = kFinThreads / 2; w >= 1; w >>= 1) {
+    if (tid < w) {
+      s_loss[tid] += s_loss[tid + w];
+      s_nc[tid] += s_nc[tid + w];
+    }
+    __syncthreads();
+  }
+  if (tid != 0) return;
+  p.n_counted[0] = static_cast<int32_t>(s_nc[0]);
+  if (p.loss_out == nullptr) return;
+  const double tot = s_loss[0], cnt = static_cast<double>(s_nc[0]);
+  if (p.reduction == 1) {
+    p.loss_out[0] = static_cast<float>(tot);
+  } else if (p.reduction == 2) {
+    p.loss_out[0] = static_cast<float>(tot / cnt);  // 0/0 -> NaN
+  } else if (p.reduction == 3) {
+    p.loss_out[0] = static_cast<float>(tot / (cnt * static_cast<double>(p.v)));
+  }
+}
+
 __global__ void __launch_bounds__(256)
     bias_reduce_kernel(const float* __restrict__ part, int64_t n_parts, int64_t ld, int64_t v,
                        void* out, int out_type, const int32_t* n_dyn, int rows_per_part) {
@@ -137,49 +211,55 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// scales[0] = 2^k with |g_ref * logit_scale * 2^k| in [8192, 16384), scales[1]
-// = 2^-k; g_ref is the largest row upstream gradient (grad_out/n_valid,
-// grad_out, or max |grad_out[i]| over non-ignored rows). 1 and 1 when g_ref
-// is zero or not finite.
+// scales[0] = 2^k with |gs * 2^k| in [8192, 16384), scales[1] = 2^-k; gs
+// bounds |D|: the largest row upstream gradient (grad_out/n_valid/extra_div,
+// grad_out/extra_div, or max |grad_out[i]| over counted rows) times
+// |logit_scale| times either (1 + 2 |z_loss| max |lse|) or, with row_bound,
+// max row_bound over counted rows. 1 and 1 when gs is zero or not finite.
+__device__ __forceinline__ float block_max(float x, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  x = red[lane];
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  __syncthreads();
+  return x;
+}
+
 __global__ void __launch_bounds__(1024)
     dlogits_scale_kernel(const float* grad_out, const int32_t* n_valid, const int64_t* targets,
                          int64_t n, int64_t ignore_index, int reduction, float logit_scale,
-                         float z_loss, const float* lse_rows, float* scales) {
+                         float z_loss, const float* lse_rows, const float* row_bound,
+                         float extra_div, float* scales) {
   __shared__ float red[32];
-  __shared__ float lse_red[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // with z-loss, |D| <= g * s * (1 + 2 |z_loss| max |lse|)
-  float lm = 0.0f;
-  if (z_loss != 0.0f) {
+  const int tid = threadIdx.x;
+  float factor = 1.0f;
+  if (row_bound != nullptr) {
+    float b = 0.0f;
     for (int64_t i = tid; i < n; i += 1024)
-      if (targets[i] != ignore_index) lm = fmaxf(lm, fabsf(lse_rows[i]));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, off));
-    if (lane == 0) lse_red[warp] = lm;
-    __syncthreads();
-    lm = lse_red[lane];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+      if (targets == nullptr || targets[i] != ignore_index) b = fmaxf(b, fabsf(row_bound[i]));
+    factor = block_max(b, red);
+  } else if (z_loss != 0.0f) {
+    float lm = 0.0f;
+    for (int64_t i = tid; i < n; i += 1024)
+      if (targets == nullptr || targets[i] != ignore_index) lm = fmaxf(lm, fabsf(lse_rows[i]));
+    lm = block_max(lm, red);
+    factor = fmaf(2.0f * fabsf(z_loss), lm, 1.0f);
   }
   float g = 0.0f;
   if (reduction == 0) {
     for (int64_t i = tid; i < n; i += 1024)
-      if (targets[i] != ignore_index) g = fmaxf(g, fabsf(grad_out[i]));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, off));
-    if (lane == 0) red[warp] = g;
-    __syncthreads();
-    if (warp == 0) {
-      g = red[lane];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, off));
-    }
-  } else if (tid == 0) {
-    g = fabsf(grad_out[0]);
+      if (targets == nullptr || targets[i] != ignore_index) g = fmaxf(g, fabsf(grad_out[i]));
+    g = block_max(g, red);
+  } else {
+    g = fabsf(grad_out[0]) / extra_div;
     if (reduction == 2) g = n_valid[0] > 0 ? g / static_cast<float>(n_valid[0]) : 0.0f;
   }
   if (tid != 0) return;
-  const float gs = g * fabsf(logit_scale) * fmaf(2.0f * fabsf(z_loss), lm, 1.0f);
+  const float gs = g * fabsf(logit_scale) * factor;
   float up = 1.0f, down = 1.0f;
   if (gs > 0.0f && isfinite(gs)) {
     int e = 0;
@@ -228,10 +308,11 @@ __global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const Com
       const float nan = __int_as_float(0x7fc00000);
       p.loss_rows[i] = 0.0f;
       p.lse_rows[i] = nan;
-      p.correct_ws[i] = 0;
-      p.entropy_ws[i] = nan;
+      if (p.correct_ws) p.correct_ws[i] = 0;
+      if (p.entropy_ws) p.entropy_ws[i] = nan;
       if (p.correct_rows) p.correct_rows[i] = 0;
       if (p.entropy_rows) p.entropy_rows[i] = nan;
+      if (p.qsum_rows) p.qsum_rows[i] = nan;
     }
     carry += chunk_total;
     __syncthreads();
@@ -258,6 +339,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
       p.targets_c[j] = p.targets[src_row];
       if (p.lse_c) p.lse_c[j] = p.lse[src_row];
       if (p.grad_rows_c) p.grad_rows_c[j] = p.grad_rows[src_row];
+      if (p.qsum_c) p.qsum_c[j] = p.qsum[src_row];
     }
   } else {
     for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
@@ -265,6 +347,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
       p.targets_c[j] = p.ignore_index;
       if (p.lse_c) p.lse_c[j] = 0.0f;
       if (p.grad_rows_c) p.grad_rows_c[j] = 0.0f;
+      if (p.qsum_c) p.qsum_c[j] = 0.0f;
     }
   }
 }
@@ -294,9 +377,22 @@ cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s) {
 cudaError_t launch_dlogits_scale(const float* grad_out, const int32_t* n_valid,
                                  const int64_t* targets, int64_t n, int64_t ignore_index,
                                  int reduction, float logit_scale, float z_loss,
-                                 const float* lse_rows, float* scales, cudaStream_t s) {
+                                 const float* lse_rows, const float* row_bound, float extra_div,
+                                 float* scales, cudaStream_t s) {
   dlogits_scale_kernel<<<1, 1024, 0, s>>>(grad_out, n_valid, targets, n, ignore_index, reduction,
-                                          logit_scale, z_loss, lse_rows, scales);
+                                          logit_scale, z_loss, lse_rows, row_bound, extra_div,
+                                          scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_kl(const MergeKLParams& p, cudaStream_t s) {
+  const unsigned grid = static_cast<unsigned>((p.n + kMergeWarps - 1) / kMergeWarps);
+  merge_kl_kernel<<<grid, kMergeWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_kl(const FinalizeKLParams& p, cudaStream_t s) {
+  finalize_kl_kernel<<<1, kFinThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,10 @@
 // that folds each logit tile into per-(row, tile) softmax statistics, and a
 // backward that recomputes the logits of one vocabulary chunk, forms D =
 // g (p - onehot) dz/dlin in fp32 and contracts it with hidden and weight.
+// With teacher probabilities q the same two kernels serve the fused linear KL
+// divergence (FusedLinearKLDivLoss pull request, Liger-Kernel #1423): the
+// forward keeps A = sum q (log max(q, eps) - z) and Q = sum q per tile, the
+// backward forms D = g (p Q - q) / T.
 #include <cfloat>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -86,7 +90,9 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const SimtFwdParams p) {
     if (row >= p.n) break;  // warp-uniform
     RowStats st;
     st.init();
-    float zsum = 0.0f;
+    float zsum = 0.0f;          // cross-entropy: sum z (label smoothing)
+    float a_sum = 0.0f;         // KL: sum q (log max(q, eps) - z)
+    float q_sum = 0.0f;         // KL: sum q
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int cl = lane + 32 * j;
@@ -99,14 +105,25 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(const SimtFwdParams p) {
         }
         st.add(z);
         zsum += z;
+        if (p.q != nullptr) {
+          const float q = p.q[row * p.v + c];
+          a_sum = fmaf(q, logf(fmaxf(q, p.eps)) - z, a_sum);
+          q_sum += q;
+        }
       }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       st = merge_stats(st, shfl_xor_stats(st, off));
       zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
+      a_sum += __shfl_xor_sync(0xffffffffu, a_sum, off);
+      q_sum += __shfl_xor_sync(0xffffffffu, q_sum, off);
     }
     if (lane == 0) {
+      if (p.q != nullptr) {  // KL partials: (m, s, A, Q)
+        p.partials[row * p.n_vt + blockIdx.y] = make_float4(st.m, st.s, a_sum, q_sum);
+        continue;
+      }
       p.partials[row * p.n_vt + blockIdx.y] = st.pack();
       if (p.zsum != nullptr) p.zsum[row * p.n_vt + blockIdx.y] = zsum;
       const int64_t t = p.targets[row];
@@ -131,10 +148,17 @@ __global__ void __launch_bounds__(256) simt_dlogits_kernel(const SimtDlogitsPara
     const int rl = ty * 4 + i;
     const int64_t row = row0 + rl;
     const bool row_ok = row < p.n;
-    const int64_t t = row_ok ? p.targets[row] : p.ignore_index;
-    const float g =
-        row_ok ? row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row) : 0.0f;
+    const bool kl = p.q != nullptr;
+    const int64_t t = (row_ok && p.targets != nullptr) ? p.targets[row] : p.ignore_index;
+    float g = 0.0f;
+    if (kl) {
+      const bool counted = row_ok && (p.targets == nullptr || t != p.ignore_index);
+      g = kl_row_grad(counted, p.reduction, p.grad_out, p.n_valid, p.v, row);
+    } else if (row_ok) {
+      g = row_grad(t, p.ignore_index, p.v, p.reduction, p.grad_out, p.n_valid, row);
+    }
     const float lse = row_ok ? p.lse[row] : 0.0f;
+    const float qs = (kl && row_ok) ? p.qsum[row] : 0.0f;
     const float pz = fmaf(2.0f * p.z_loss, lse, 1.0f);
     const float eps_v = p.label_smoothing / static_cast<float>(p.v);
 #pragma unroll
@@ -145,8 +169,13 @@ __global__ void __launch_bounds__(256) simt_dlogits_kernel(const SimtDlogitsPara
       if (row_ok && c < vend) {
         const float b = (p.bias != nullptr) ? p.bias[c] : 0.0f;
         const float z = p.xf(acc[i][j], b);
-        d = fmaf(ex2_approx((z - lse) * kLog2e), pz, -eps_v);
-        if (c == t) d -= 1.0f - p.label_smoothing;
+        const float pr = ex2_approx((z - lse) * kLog2e);
+        if (kl) {
+          d = fmaf(pr, qs, -p.q[row * p.v + c]);  // p sum q - q
+        } else {
+          d = fmaf(pr, pz, -eps_v);
+          if (c == t) d -= 1.0f - p.label_smoothing;
+        }
         d *= g * p.xf.scale * p.xf.dz_du(z);
         p.d[row * p.ldd + (c - p.c0)] = d;
       }

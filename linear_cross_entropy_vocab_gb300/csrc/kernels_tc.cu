@@ -115,6 +115,53 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Loads q[c .. c+32) of one row (fewer when nv < 32; the rest are 0).
+template <typename T>
+__device__ __forceinline__ void load_row32(const T* row_ptr, int64_t c, int nv, bool vec,
+                                           float (&q)[32]) {
+  if (vec && nv == 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(row_ptr + c);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint4 w = __ldg(src + r);
+      const uint32_t parts[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        q[r * 8 + 2 * h] = Elem<T>::lo(parts[h]);
+        q[r * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) q[k] = (k < nv) ? Elem<T>::to(row_ptr[c + k]) : 0.0f;
+  }
+}
+
+// The tail every dlogits epilogue shares: store the 32 values of D (times
+// dscale, rounded to T) for every buffer row (rows past the present ones hold
+// d = 0), and add the tile's fixed-order fp32 column sums to the grad_bias
+// partials.
+template <typename T>
+__device__ __forceinline__ void emit_dlogits(float (&d)[32], int nv, int64_t row, int64_t buf_rows,
+                                             void* dbuf, int64_t ldd, int cb, float dscale,
+                                             float* gb_partial, int64_t gb_ld, int c0, int width,
+                                             int m_tile, int64_t n_eff, int quarter, int lane,
+                                             GemmCtl* ctl) {
+  if (row < buf_rows) store32<T>(static_cast<T*>(dbuf) + row * ldd + cb, d, nv, dscale);
+  if (gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff) {
+    // column sums of D over this tile's 128 rows, in a fixed order
+    const float colsum = transpose_reduce32(d, lane);
+    ctl->red[quarter][lane] = colsum;
+    named_bar_sync(1, kEpiThreads);
+    if (quarter == 0 && cb + lane < width) {
+      const float tot =
+          ((ctl->red[0][lane] + ctl->red[1][lane]) + ctl->red[2][lane]) + ctl->red[3][lane];
+      gb_partial[static_cast<int64_t>(m_tile) * gb_ld + c0 + cb + lane] = tot;
+    }
+    named_bar_sync(1, kEpiThreads);
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ forward
@@ -221,21 +268,106 @@ struct EpiDlogits {
       for (int k = 0; k < 32; ++k) {
         d[k] = row_ok ? d[k] * gs * p.xf.dz_du(z[k]) : 0.0f;
       }
-      if (row < p.n_rows) {  // rows past the present ones get zeros (d = 0 there)
-        store32<T>(static_cast<T*>(p.d) + row * p.ldd + cb, d, nv, dscale);
+      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, p.gb_partial, p.gb_ld,
+                      p.c0, p.width, m_tile, n_eff, quarter, lane, ctl);
+    }
+  }
+};
+
+// ------------------------------------------------------------ KL forward
+template <typename T>
+struct EpiFwdKL {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  using Params = FwdKLParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*lane*/,
+                              GemmCtl* /*ctl*/) {
+    const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < n_eff;
+    const int64_t orig = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
+    const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v;
+    const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
+    RowStats st;
+    st.init();
+    float a_sum = 0.0f;  // sum q (log max(q, eps) - z)
+    float q_sum = 0.0f;  // sum q
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int64_t cb = col0 + ch * 32;
+      if (cb >= p.v) break;
+      const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
+      float z[32], b[32];
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      load_bias32<T>(p.bias, cb, nv, b);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
+      if (nv == 32) {
+        fold_chunk<true>(st, z, nv, static_cast<int>(cb));
+      } else {
+        fold_chunk<false>(st, z, nv, static_cast<int>(cb));
       }
-      if (p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff) {
-        // column sums of D over this tile's 128 rows, in a fixed order
-        const float colsum = transpose_reduce32(d, lane);
-        ctl->red[quarter][lane] = colsum;
-        named_bar_sync(1, kEpiThreads);
-        if (quarter == 0 && cb + lane < p.width) {
-          const float tot = ((ctl->red[0][lane] + ctl->red[1][lane]) + ctl->red[2][lane]) +
-                            ctl->red[3][lane];
-          p.gb_partial[static_cast<int64_t>(m_tile) * p.gb_ld + p.c0 + cb + lane] = tot;
+      if (row_ok) {
+        float q[32];
+        load_row32<T>(qrow, cb, nv, p.q_vec != 0, q);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k < nv) {
+            a_sum = fmaf(q[k], __logf(fmaxf(q[k], p.eps)) - z[k], a_sum);
+            q_sum += q[k];
+          }
         }
-        named_bar_sync(1, kEpiThreads);
       }
+    }
+    if (row_ok) p.partials[row * p.n_vt + n_tile] = make_float4(st.m, st.s, a_sum, q_sum);
+  }
+};
+
+// ------------------------------------------------------------ KL dlogits
+// D = g (p * sum_k q_k - q) * dz/dlin, with dz/dlin = 1 / temperature.
+template <typename T>
+struct EpiDlogitsKL {
+  static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  using Params = DlogitsKLParams;
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
+                              bool acc_zero, int row_in_tile, int quarter, int lane,
+                              GemmCtl* ctl) {
+    const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
+    const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
+    const bool row_ok = row < n_eff;
+    const bool counted =
+        row_ok && (p.labels == nullptr || __ldg(p.labels + row) != p.ignore_index);
+    const float gs = kl_row_grad(counted, p.reduction, p.grad_out, p.n_counted, p.v, row) *
+                     p.xf.scale;
+    const float lse2 = row_ok ? __ldg(p.lse + row) * kLog2e : 0.0f;
+    const float qs = row_ok ? __ldg(p.qsum + row) : 0.0f;
+    const int64_t orig = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
+    const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v + p.c0;
+    const int col0 = n_tile * kBN;
+    const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int cb = col0 + ch * 32;
+      if (cb >= p.width) break;
+      const int nv = p.width - cb < 32 ? p.width - cb : 32;
+      float z[32], b[32], q[32];
+      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      load_bias32<T>(p.bias, p.c0 + cb, nv, b);
+      if (row_ok) {
+        load_row32<T>(qrow, cb, nv, p.q_vec != 0, q);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) q[k] = 0.0f;
+      }
+      float d[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        z[k] = p.xf(z[k], b[k]);
+        const float pr = ex2_approx(fmaf(z[k], kLog2e, -lse2));
+        d[k] = counted ? fmaf(pr, qs, -q[k]) * gs * p.xf.dz_du(z[k]) : 0.0f;
+      }
+      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, p.gb_partial, p.gb_ld,
+                      p.c0, p.width, m_tile, n_eff, quarter, lane, ctl);
     }
   }
 };
@@ -412,6 +544,27 @@ cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
                                                                    sms, s);
   return launch_gemm<kPairCG, false, false, EpiDlogits<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
                                                                         g, p, sms, s);
+}
+
+cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
+                             const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                             const FwdKLParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, false, false, EpiFwdKL<__half>>(tm_hidden_k, tm_weight_k, g, p,
+                                                                 sms, s);
+  return launch_gemm<kPairCG, false, false, EpiFwdKL<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
+                                                                      g, p, sms, s);
+}
+
+cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
+                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
+                                 const DlogitsKLParams& p, int sms, cudaStream_t s) {
+  if (type == kTcF16)
+    return launch_gemm<kPairCG, false, false, EpiDlogitsKL<__half>>(tm_hidden_k, tm_weight_k, g,
+                                                                     p, sms, s);
+  return launch_gemm<kPairCG, false, false, EpiDlogitsKL<__nv_bfloat16>>(tm_hidden_k,
+                                                                          tm_weight_k, g, p,
+                                                                          sms, s);
 }
 
 cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,

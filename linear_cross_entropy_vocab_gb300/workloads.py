@@ -19,7 +19,8 @@ Readings of the workload notation (stated once, used everywhere):
   * "1% of weight rows scaled x8": ``round(0.01 * V)`` rows chosen by a seeded
     permutation are multiplied by 8 after sampling and before the bf16 cast.
   * Draw order: hidden, weight, bias, ignore permutation, targets, scaled
-    rows; draw ``idx`` uses ``torch.Generator('cpu').manual_seed(seed + idx)``.
+    rows, then (KL divergence only) teacher logits as draw 6; draw ``idx``
+    uses ``torch.Generator('cpu').manual_seed(seed + idx)``.
     Values are drawn in fp32 and cast to bf16 with round-to-nearest-even.
 """
 from __future__ import annotations
@@ -30,7 +31,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "peaked_rows", "gemm_flops"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_teacher_probs", "peaked_rows",
+           "gemm_flops"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -129,6 +131,24 @@ def make_inputs(w: Workload) -> dict:
         "bias": None if bias is None else bias.to(dt),
         "targets": targets,
     }
+
+
+def make_teacher_probs(w: Workload, teacher_std: float = 2.0, keep_top: Optional[int] = None,
+                       idx: int = 6) -> torch.Tensor:
+    """Teacher probabilities [N,V] for the KL divergence, in the workload's
+    dtype: the distribution a teacher model would output, drawn as the
+    softmax (fp32) of N(0, teacher_std**2) teacher logits (draw ``idx``).
+    With ``keep_top`` k, each row keeps only its k largest entries
+    (renormalised; the rest exactly 0), as a top-k truncated teacher does.
+    These are inputs of the method; after the cast a row sums to 1 only up
+    to the dtype's rounding."""
+    t = torch.randn(w.n, w.v, generator=_gen(w.seed, idx), dtype=torch.float32)
+    t.mul_(teacher_std)
+    if keep_top is not None and keep_top < w.v:
+        kth = torch.topk(t, keep_top, dim=1).values[:, -1:]
+        t = t.masked_fill(t < kth, float("-inf"))
+    q = torch.softmax(t, dim=1)
+    return q.to(w.torch_dtype)
 
 
 def peaked_rows(w: Workload) -> torch.Tensor:

@@ -119,3 +119,90 @@ def test_validation_statuses(lib):
     assert _bwd(ok, grad_hidden=FAKE + 4) == abi.FLCE_ERR_UNSUPPORTED
     assert _bwd(ok, workspace_bytes=0) == abi.FLCE_ERR_WORKSPACE
     assert lib.flce_forward(None, *([None] * 13), 0, None) == abi.FLCE_ERR_INVALID_ARG
+
+
+def _c_layout():
+    """sizeof / offsetof of both problem structs as a C compiler lays them
+    out from include/flce.h (gcc on this host)."""
+    import shutil
+    import subprocess
+    import tempfile
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "flce.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(flce_problem), offsetof(flce_problem, ignore_index),
+         offsetof(flce_problem, logit_scale), offsetof(flce_problem, flags),
+         offsetof(flce_problem, z_loss));
+  printf("%zu %zu %zu %zu %zu\n", sizeof(flce_kl_problem),
+         offsetof(flce_kl_problem, ignore_index), offsetof(flce_kl_problem, temperature),
+         offsetof(flce_kl_problem, vocab_chunk), offsetof(flce_kl_problem, reserved));
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe],
+                       check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split("\n")
+    return [int(x) for x in out[0].split()], [int(x) for x in out[1].split()]
+
+
+def test_struct_layouts_match_c_compiler():
+    ce, kl = _c_layout()
+    P, K = abi.flce_problem, abi.flce_kl_problem
+    assert ce == [ctypes.sizeof(P), P.ignore_index.offset, P.logit_scale.offset,
+                  P.flags.offset, P.z_loss.offset]
+    assert kl == [ctypes.sizeof(K), K.ignore_index.offset, K.temperature.offset,
+                  K.vocab_chunk.offset, K.reserved.offset]
+    assert ctypes.sizeof(K) == 72
+
+
+def _kl_fwd(p, **kw):
+    args = dict(hidden=FAKE, weight=FAKE, bias=None, target_probs=FAKE, labels=None,
+                loss_rows=FAKE, lse_rows=FAKE, qsum_rows=FAKE, loss_out=FAKE, n_counted=FAKE,
+                err_word=None, workspace=FAKE, workspace_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return abi.flce_kl_forward(p, check=False, **args)
+
+
+def _kl_bwd(p, **kw):
+    args = dict(hidden=FAKE, weight=FAKE, bias=None, target_probs=FAKE, labels=None,
+                lse_rows=FAKE, qsum_rows=FAKE, n_counted=FAKE, grad_out=FAKE,
+                grad_hidden=FAKE, grad_weight=FAKE, grad_bias=None, err_word=None,
+                workspace=FAKE, workspace_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return abi.flce_kl_backward(p, check=False, **args)
+
+
+def test_kl_validation_and_workspace(lib):
+    ok = abi.make_kl_problem(64, 64, 100, abi.FLCE_BF16, False)
+    assert abi.flce_kl_forward_workspace_size(ok) >= 64 * 1 * 16
+    big = abi.make_kl_problem(8192, 4096, 128256, abi.FLCE_BF16, False)
+    assert abi.flce_kl_backward_workspace_size(big) < 8192 * 128256 * 2
+    for field, bad in (("temperature", 0.0), ("temperature", float("nan")),
+                       ("temperature", -1.0), ("temperature", 1e-39), ("eps", 0.0),
+                       ("eps", float("inf")), ("reduction", 4), ("reserved", 1)):
+        p = abi.make_kl_problem(64, 64, 100, abi.FLCE_BF16, False)
+        setattr(p, field, bad)
+        assert _kl_fwd(p) == abi.FLCE_ERR_INVALID_ARG, field
+        assert abi.flce_kl_forward_workspace_size(p) == 0
+    assert _kl_fwd(ok, target_probs=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_fwd(ok, qsum_rows=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_fwd(ok, n_counted=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_fwd(ok, loss_out=None) == abi.FLCE_ERR_INVALID_ARG  # batchmean needs it
+    assert _kl_fwd(ok, target_probs=FAKE + 1) == abi.FLCE_ERR_UNSUPPORTED
+    assert _kl_fwd(ok, labels=FAKE + 4) == abi.FLCE_ERR_UNSUPPORTED
+    assert _kl_fwd(ok, workspace_bytes=16) == abi.FLCE_ERR_WORKSPACE
+    odd = abi.make_kl_problem(64, 60, 100, abi.FLCE_BF16, False)
+    assert _kl_fwd(odd) == abi.FLCE_ERR_UNSUPPORTED
+    assert _kl_bwd(ok, target_probs=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_bwd(ok, qsum_rows=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_bwd(ok, grad_out=None) == abi.FLCE_ERR_INVALID_ARG
+    assert _kl_bwd(ok, workspace_bytes=0) == abi.FLCE_ERR_WORKSPACE
+    assert lib.flce_kl_forward(None, *([None] * 12), 0, None) == abi.FLCE_ERR_INVALID_ARG

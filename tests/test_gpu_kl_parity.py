@@ -1,0 +1,203 @@
+"""GPU parity of the fused linear KL divergence (FusedLinearKLDivLoss pull
+request, Liger-Kernel #1423): the CUDA path through the C ABI against the
+fp64 KL oracle, element by element, on seeded inputs with ragged tails along
+N, V and H, every reduction, temperature, labels with ignored rows (with and
+without leaving them out of the contractions), bias, top-k truncated teachers
+(exact zeros, so the eps clamp matters), multi-chunk backward passes, and the
+three input dtypes.
+
+Tolerances are those of the cross-entropy (``tests/_parity.py``): loss and
+lse rows rel 2e-3 (16-bit inputs) / 1e-5 (fp32) of max(1, |ref|); per-row
+sums of q rel 1e-5 (a sum of positive fp32 terms); gradients brought to the
+scale of a 'batchmean' loss (divided by n_counted for 'sum' / 'none',
+multiplied by V for 'mean') and held to the elementwise and normwise bars.
+"""
+import math
+
+import pytest
+import torch
+
+from _parity import TOL, assert_grad_close, assert_rows_close, to_dev
+from linear_cross_entropy_vocab_gb300 import api, fused_linear_kl_div
+from linear_cross_entropy_vocab_gb300.workloads import Workload, make_inputs, make_teacher_probs
+from oracle import kl_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(name, n, h, v, dtype="bf16", **kw):
+    return Workload(name, n, h, v, dtype, **kw)
+
+
+# (workload, temperature, reduction, with labels, teacher keep_top, vocab_chunk, skip_ignored)
+CASES = [
+    (_w("tails_bias_bm", 300, 136, 1000, bias_var=0.02, ignore_frac=0.1), 1.0, "batchmean",
+     True, None, 0, False),
+    (_w("v32003_sum", 512, 256, 32003), 2.0, "sum", False, None, 0, False),
+    (_w("n4097_mean", 4097, 512, 4096, ignore_frac=0.1), 0.5, "mean", True, None, 0, False),
+    (_w("topk_none_bias", 640, 192, 5000, bias_var=0.02, ignore_frac=0.2), 1.5, "none", True,
+     20, 512, False),
+    (_w("skip_bm", 300, 136, 1000, bias_var=0.02, ignore_frac=0.3), 1.0, "batchmean", True,
+     None, 0, True),
+    (_w("skip_none_chunks", 1000, 256, 3000, ignore_frac=0.25), 2.0, "none", True, 50, 512,
+     True),
+    (_w("f16_bm", 384, 256, 3000, "f16", ignore_frac=0.05), 1.0, "batchmean", True, None, 0,
+     False),
+    (_w("f16_skip_mean_bias", 500, 128, 2056, "f16", bias_var=0.02, ignore_frac=0.2), 0.7,
+     "mean", True, 10, 1024, True),
+    (_w("f32_bias_bm", 100, 50, 777, "f32", bias_var=0.02, ignore_frac=0.1), 2.0, "batchmean",
+     True, None, 0, False),
+    (_w("f32_none", 257, 96, 2100, "f32"), 1.0, "none", False, 30, 512, False),
+]
+
+
+def _grad_out(reduction, n):
+    if reduction == "none":
+        g = torch.Generator().manual_seed(11)
+        return (torch.rand(n, generator=g, dtype=torch.float64) + 0.5).float()
+    return 0.75
+
+
+def _labels(x, with_labels):
+    return x["targets"] if with_labels else None
+
+
+def run_kl_gpu(xd, q, labels, w, temperature, reduction, grad_out, vocab_chunk=0,
+               skip_ignored=False, backward=True):
+    err = torch.zeros((), dtype=torch.int32, device="cuda")
+    f = api.flce_kl_forward_tensors(xd["hidden"], xd["weight"], q, labels, xd["bias"],
+                                    w.ignore_index, temperature, 1e-10, reduction,
+                                    err_word=err, skip_ignored=skip_ignored)
+    out = {k: (None if t is None else t.detach().cpu()) for k, t in f.items()}
+    if backward:
+        go = (grad_out.cuda() if torch.is_tensor(grad_out)
+              else torch.tensor(float(grad_out), dtype=torch.float32, device="cuda"))
+        gh, gw, gb = api.flce_kl_backward_tensors(
+            xd["hidden"], xd["weight"], q, f["lse_rows"], f["qsum_rows"], f["n_counted"], go,
+            labels, xd["bias"], w.ignore_index, temperature, 1e-10, reduction, err_word=err,
+            vocab_chunk=vocab_chunk, skip_ignored=skip_ignored)
+        out["grad_hidden"], out["grad_weight"] = gh.cpu(), gw.cpu()
+        out["grad_bias"] = None if gb is None else gb.cpu()
+    torch.cuda.synchronize()
+    out["err_word"] = int(err.item())
+    return out
+
+
+def _scale(reduction, n_counted, v):
+    """Brings a gradient to the scale of the 'batchmean' one."""
+    if reduction == "mean":
+        return float(v)
+    if reduction in ("sum", "none") and n_counted > 0:
+        return 1.0 / n_counted
+    return 1.0
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0].name for c in CASES])
+def test_kl_parity(case):
+    w, temp, reduction, with_labels, keep_top, chunk, skip = case
+    x = make_inputs(w)
+    q = make_teacher_probs(w, keep_top=keep_top)
+    labels = _labels(x, with_labels)
+    go = _grad_out(reduction, w.n)
+    xd = to_dev(x)
+    out = run_kl_gpu(xd, q.cuda(), None if labels is None else labels.cuda(), w, temp,
+                     reduction, go, vocab_chunk=chunk, skip_ignored=skip)
+    assert out["err_word"] == 0
+    tol = TOL[w.dtype]
+    ref = kl_oracle.forward(x["hidden"], x["weight"], q, x["bias"], labels, w.ignore_index,
+                            temp, 1e-10, reduction)
+    counted = ref["counted"]
+    assert int(out["n_counted"]) == ref["n_counted"]
+    assert_rows_close("loss_rows", out["loss_rows"], ref["loss"], tol["loss_rel"])
+    assert torch.all(out["loss_rows"][~counted] == 0)
+    stat = counted if (skip and labels is not None) else None
+    assert_rows_close("lse_rows", out["lse_rows"], ref["lse"], tol["loss_rel"], stat)
+    assert_rows_close("qsum_rows", out["qsum_rows"], ref["qsum"], 1e-5, stat)
+    if stat is not None:
+        assert bool(torch.isnan(out["lse_rows"][~counted]).all())
+        assert bool(torch.isnan(out["qsum_rows"][~counted]).all())
+    if reduction != "none":
+        r, g = ref["loss_out"], float(out["loss"])
+        assert abs(g - r) <= tol["loss_rel"] * max(1.0, abs(r)), (g, r)
+    gref = kl_oracle.backward(x["hidden"], x["weight"], q, x["bias"], labels, w.ignore_index,
+                              temp, 1e-10, reduction, go.double() if torch.is_tensor(go) else go)
+    s = _scale(reduction, ref["n_counted"], w.v)
+    assert_grad_close("grad_hidden", out["grad_hidden"], gref["grad_hidden"], tol, s)
+    assert_grad_close("grad_weight", out["grad_weight"], gref["grad_weight"], tol, s)
+    if x["bias"] is not None:
+        assert_grad_close("grad_bias", out["grad_bias"], gref["grad_bias"], tol, s)
+    if labels is not None:
+        assert torch.all(out["grad_hidden"][~counted] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_onehot_teacher_equals_cross_entropy(dtype):
+    """With a one-hot teacher at the targets and T = 1, KL(onehot || p) is the
+    cross-entropy -log p_t, and d/dz is p - onehot: the KL path reproduces the
+    separately pinned cross-entropy path (batchmean = mean over counted rows).
+    Loss rows agree to rounding of the log of 1 in the approximate logarithm;
+    lse rows and the gradients are bitwise equal."""
+    w = _w("onehot", 700, 264, 3333, dtype, bias_var=0.02, ignore_frac=0.1)
+    x = make_inputs(w)
+    t = x["targets"]
+    q = torch.zeros(w.n, w.v, dtype=w.torch_dtype)
+    keep = t != w.ignore_index
+    q[keep, t[keep]] = 1.0
+    xd = to_dev(x)
+    kl = run_kl_gpu(xd, q.cuda(), xd["targets"], w, 1.0, "batchmean", 0.75)
+    ce_f = api.flce_forward_tensors(xd["hidden"], xd["weight"], xd["targets"], xd["bias"],
+                                    w.ignore_index, reduction="mean")
+    go = torch.tensor(0.75, dtype=torch.float32, device="cuda")
+    ce_g = api.flce_backward_tensors(xd["hidden"], xd["weight"], xd["targets"],
+                                     ce_f["lse_rows"], ce_f["n_valid"], go, xd["bias"],
+                                     w.ignore_index, reduction="mean")
+    torch.cuda.synchronize()
+    assert torch.equal(kl["lse_rows"], ce_f["lse_rows"].cpu())
+    assert torch.allclose(kl["loss_rows"], ce_f["loss_rows"].cpu(), rtol=1e-6, atol=1e-6)
+    assert abs(float(kl["loss"]) - float(ce_f["loss"])) <= 1e-6 * max(1.0, abs(float(ce_f["loss"])))
+    assert torch.equal(kl["grad_hidden"], ce_g[0].cpu())
+    assert torch.equal(kl["grad_weight"], ce_g[1].cpu())
+    assert torch.equal(kl["grad_bias"], ce_g[2].cpu())
+
+
+def test_kl_empty_and_all_ignored():
+    w = _w("empty", 0, 64, 1000)
+    x = make_inputs(w)
+    xd = to_dev(x)
+    q = torch.empty(0, w.v, dtype=torch.bfloat16, device="cuda")
+    for reduction, expect in (("batchmean", math.nan), ("sum", 0.0), ("mean", math.nan)):
+        out = run_kl_gpu(xd, q, xd["targets"], w, 1.0, reduction, 1.0)
+        assert int(out["n_counted"]) == 0
+        got = float(out["loss"])
+        assert (math.isnan(got) if math.isnan(expect) else got == expect)
+        assert torch.all(out["grad_weight"] == 0)
+    w = _w("all_ignored", 300, 64, 1000, ignore_frac=1.0)
+    x = make_inputs(w)
+    xd = to_dev(x)
+    q = make_teacher_probs(w).cuda()
+    for skip in (False, True):
+        out = run_kl_gpu(xd, q, xd["targets"], w, 1.0, "sum", 1.0, skip_ignored=skip)
+        assert int(out["n_counted"]) == 0 and float(out["loss"]) == 0.0
+        assert torch.all(out["loss_rows"] == 0)
+        for k in ("grad_hidden", "grad_weight"):
+            assert torch.all(out[k] == 0), k
+
+
+def test_kl_autograd_matches_raw_calls_and_repeats_bitwise():
+    w = _w("autograd", 600, 192, 5000, bias_var=0.02, ignore_frac=0.2)
+    x = make_inputs(w)
+    xd = to_dev(x)
+    q = make_teacher_probs(w, keep_top=100).cuda()
+    raw = run_kl_gpu(xd, q, xd["targets"], w, 1.3, "batchmean", 1.0, skip_ignored=True)
+    again = run_kl_gpu(xd, q, xd["targets"], w, 1.3, "batchmean", 1.0, skip_ignored=True)
+    for k in ("loss", "loss_rows", "grad_hidden", "grad_weight", "grad_bias"):
+        assert torch.equal(raw[k], again[k]), k
+    h = xd["hidden"].clone().requires_grad_(True)
+    wt = xd["weight"].clone().requires_grad_(True)
+    b = xd["bias"].clone().requires_grad_(True)
+    loss = fused_linear_kl_div(h, wt, q, xd["targets"], b, temperature=1.3)
+    loss.backward()
+    assert torch.equal(loss.detach().cpu(), raw["loss"])
+    assert torch.equal(h.grad.cpu(), raw["grad_hidden"])
+    assert torch.equal(wt.grad.cpu(), raw["grad_weight"])
+    assert torch.equal(b.grad.cpu(), raw["grad_bias"])

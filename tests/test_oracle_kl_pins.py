@@ -154,3 +154,52 @@ def test_planted_mistakes(monkeypatch, mutant):
     monkeypatch.setattr(kl_oracle, "backward", mutant)
     worst = max(_fd(red, t, mod=kl_oracle, n_probe=3) for red, t in CASES)
     assert worst > 1e-6, f"{mutant.__name__} went unnoticed"
+
+
+ORIG_FORWARD = kl_oracle.forward
+
+
+def _mut_fwd_no_clamp(hidden, weight, target_probs, bias=None, labels=None, ignore_index=-100,
+                      temperature=1.0, eps=1e-10, reduction="batchmean", rows=None):
+    # log q without the eps clamp: a zero probability gives 0 * log 0 = NaN
+    return ORIG_FORWARD(hidden, weight, target_probs, bias, labels, ignore_index, temperature,
+                        0.0, reduction, rows)
+
+
+def _mut_fwd_mean_as_batchmean(hidden, weight, target_probs, bias=None, labels=None,
+                               ignore_index=-100, temperature=1.0, eps=1e-10,
+                               reduction="batchmean", rows=None):
+    red = "batchmean" if reduction == "mean" else reduction
+    return ORIG_FORWARD(hidden, weight, target_probs, bias, labels, ignore_index, temperature,
+                        eps, red, rows)
+
+
+def _mut_fwd_no_lse(hidden, weight, target_probs, bias=None, labels=None, ignore_index=-100,
+                    temperature=1.0, eps=1e-10, reduction="batchmean", rows=None):
+    # sum q (log q - z): the lse * sum q term dropped
+    r = ORIG_FORWARD(hidden, weight, target_probs, bias, labels, ignore_index, temperature, eps,
+                     reduction, rows)
+    keep = r["counted"].to(F64)
+    r["loss"] = r["loss"] - r["lse"] * r["qsum"] * keep
+    if rows is None and reduction != "none":
+        scale = r["loss_out"] / float(ORIG_FORWARD(hidden, weight, target_probs, bias, labels,
+                                                   ignore_index, temperature, eps, "sum")
+                                      ["loss_out"])
+        r["loss_out"] = float(r["loss"].sum()) * scale
+    return r
+
+
+def _forward_pins():
+    for red, t in CASES:
+        test_brute_force_forward(red, t)
+    test_zero_weight_closed_form()
+    for red in ("batchmean", "sum", "mean"):
+        test_torch_kl_div(red)
+
+
+@pytest.mark.parametrize("mutant", [_mut_fwd_no_clamp, _mut_fwd_mean_as_batchmean,
+                                    _mut_fwd_no_lse])
+def test_planted_forward_mistakes(monkeypatch, mutant):
+    monkeypatch.setattr(kl_oracle, "forward", mutant)
+    with pytest.raises(AssertionError):
+        _forward_pins()
