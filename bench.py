@@ -28,13 +28,16 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, gemm_flops, make_inputs  # noqa: E402
+from linear_cross_entropy_vocab_gb300.workloads import (  # noqa: E402
+    WORKLOADS, gemm_flops, make_inputs, make_teacher_probs)
 
 METRIC = "FLCE fwd+bwd tokens/s at H4096 V128256 bf16; % of dense-BF16 tensor peak"
+KL_METRIC = "fused linear KL fwd+bwd tokens/s at H4096 V128256 bf16; % of dense-BF16 tensor peak"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "llama3_head_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_ROLES = ("fwd_stats", "bwd_dlogits", "bwd_grad_weight", "bwd_grad_hidden")
+GEMM_ROLES = ("fwd_stats", "fwd_kl", "bwd_dlogits", "bwd_dlogits_kl", "bwd_grad_weight",
+              "bwd_grad_hidden")
 
 
 def kernel_sources_sha256() -> str:
@@ -60,9 +63,9 @@ def measured_traffic(kernel: str, workload: str):
         return None
     with open(path) as fh:
         d = json.load(fh)
-    if d.get("workload") != workload or d.get("csrc_sha256") != kernel_sources_sha256():
+    if d.get("csrc_sha256") != kernel_sources_sha256():
         return None
-    return d.get("bytes_per_launch", {}).get(kernel)
+    return d.get("workloads", {}).get(workload, {}).get("bytes_per_launch", {}).get(kernel)
 
 
 def load_peaks():
@@ -98,6 +101,28 @@ def describe(w) -> str:
         parts.append(f"label_smoothing={w.label_smoothing:g} z_loss={w.z_loss:g}")
     parts.append(w.reduction + (", return_metrics" if w.return_metrics else ""))
     return ", ".join(parts)
+
+
+# KL divergence workload: the Llama-3 head shape that the KL pull request
+# benchmarks (8192 x 4096 x 128256, bf16), teacher probabilities from
+# make_teacher_probs, the workload's targets as labels (2% ignored, left out
+# of the contractions), temperature 1, batchmean.
+KL_TEMPERATURE = 1.0
+KL_REDUCTION = "batchmean"
+
+
+def describe_kl(w) -> str:
+    return (f"fused linear KL, {w.name} shape: N={w.n} H={w.h} V={w.v} {w.dtype}, "
+            f"{'bias' if w.bias_var is not None else 'no bias'}, teacher = softmax of "
+            f"N(0, 4) logits, labels with {round(100 * w.ignore_frac)}% ignore_index, "
+            f"T={KL_TEMPERATURE:g}, {KL_REDUCTION}")
+
+
+def make_bench_inputs(w, kl: bool) -> dict:
+    x = make_inputs(w)
+    if kl:
+        x["q"] = make_teacher_probs(w)
+    return x
 
 
 # ----------------------------------------------------------------- clocks
@@ -187,7 +212,7 @@ class Step:
 
     def rebind(self, x: dict) -> "Step":
         """The same step (problem, outputs, workspace) on other input buffers."""
-        other = object.__new__(Step)
+        other = object.__new__(type(self))
         other.__dict__.update(self.__dict__)
         other.x = x
         return other
@@ -207,16 +232,67 @@ class Step:
                         stream)
 
 
+class KLStep:
+    """Preallocated buffers and the two C-ABI calls of one fused linear KL
+    fwd+bwd step."""
+
+    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False):
+        from linear_cross_entropy_vocab_gb300 import abi
+
+        self.abi = abi
+        self.x = x
+        self.w = w
+        self.forward_only = forward_only
+        n, h = x["hidden"].shape
+        v = x["weight"].shape[0]
+        code = {torch.bfloat16: abi.FLCE_BF16, torch.float16: abi.FLCE_F16,
+                torch.float32: abi.FLCE_F32}[x["hidden"].dtype]
+        self.prob = abi.make_kl_problem(n, h, v, code, x["bias"] is not None, w.ignore_index,
+                                        KL_TEMPERATURE, 1e-10, KL_REDUCTION,
+                                        skip_ignored=skip_ignored)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.loss_rows = torch.empty(n, **f32)
+        self.lse_rows = torch.empty(n, **f32)
+        self.qsum_rows = torch.empty(n, **f32)
+        self.loss = torch.empty((), **f32)
+        self.metrics = None
+        self.n_valid = torch.empty((), dtype=torch.int32, device=dev)
+        self.err = torch.zeros((), dtype=torch.int32, device=dev)
+        self.grad_out = torch.ones((), **f32)
+        self.gh = torch.empty_like(x["hidden"])
+        self.gw = torch.empty_like(x["weight"])
+        self.gb = None if x["bias"] is None else torch.empty_like(x["bias"])
+        self.ws_f = abi.flce_kl_forward_workspace_size(self.prob)
+        self.ws_b = abi.flce_kl_backward_workspace_size(self.prob)
+        self.ws = torch.empty(max(self.ws_f, self.ws_b), dtype=torch.uint8, device=dev)
+
+    rebind = Step.rebind
+
+    def __call__(self, stream):
+        a, x, p = self.abi, self.x, lambda t: None if t is None else t.data_ptr()
+        a.flce_kl_forward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]), p(x["q"]),
+                          p(x["targets"]), p(self.loss_rows), p(self.lse_rows),
+                          p(self.qsum_rows), p(self.loss), p(self.n_valid), p(self.err),
+                          p(self.ws), self.ws_f, stream)
+        if self.forward_only:
+            return
+        a.flce_kl_backward(self.prob, p(x["hidden"]), p(x["weight"]), p(x["bias"]), p(x["q"]),
+                           p(x["targets"]), p(self.lse_rows), p(self.qsum_rows),
+                           p(self.n_valid), p(self.grad_out), p(self.gh), p(self.gw),
+                           p(self.gb), p(self.err), p(self.ws), self.ws_b, stream)
+
+
 def bench_ours(args, rank, world, dev):
     from linear_cross_entropy_vocab_gb300 import abi, api, native_build
 
     native_build.build()
     w = workload_of(args)
-    xc = make_inputs(w)
+    xc = make_bench_inputs(w, args.kl)
     x = {k: (None if t is None else t.to(dev)) for k, t in xc.items()}
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    step = Step(x, w, dev, skip_ignored=not args.all_rows, forward_only=args.forward_only)
+    step = (KLStep if args.kl else Step)(x, w, dev, skip_ignored=not args.all_rows,
+                                         forward_only=args.forward_only)
     n, h, v = w.n, w.h, w.v
 
     def barrier():
@@ -319,11 +395,15 @@ def bench_ours(args, rank, world, dev):
     torch.cuda.reset_peak_memory_stats(dev)
     hh = x["hidden"].detach().requires_grad_(True)
     ww = x["weight"].detach().requires_grad_(True)
-    loss, _m = api.fused_linear_cross_entropy(hh, ww, x["targets"], return_metrics=True)
+    if args.kl:
+        loss = api.fused_linear_kl_div(hh, ww, x["q"], x["targets"],
+                                       temperature=KL_TEMPERATURE, reduction=KL_REDUCTION)
+    else:
+        loss, _m = api.fused_linear_cross_entropy(hh, ww, x["targets"], return_metrics=True)
     loss.backward()
     torch.cuda.synchronize(dev)
     peak_incr = torch.cuda.max_memory_allocated(dev) - base
-    del hh, ww, loss, _m
+    del hh, ww, loss
 
     peaks, peak_src = load_peaks()
     flops_step = gemm_flops(n, h, v) / (4.0 if args.forward_only else 1.0)
@@ -347,7 +427,7 @@ def bench_ours(args, rank, world, dev):
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "peak_kind": f"bf16 sustained, {peak_src}",
                     "flops_per_launch": flops_per_launch, "avg_launch_ms": round(avg_ms, 4),
-                    "traffic": measured_traffic(dom, w.name),
+                    "traffic": measured_traffic(dom, traffic_key(w, args)),
                     "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
                                       "dram__bytes_write.sum per launch; null if the kernels "
                                       "changed since)"}
@@ -355,7 +435,7 @@ def bench_ours(args, rank, world, dev):
                    "share": round(val[1] / sum(u[1] for u in roles.values()), 4)}
                for k, val in roles.items()}
     out = {
-        "metric": METRIC,
+        "metric": KL_METRIC if args.kl else METRIC,
         "value": round(tok_s, 1),
         "unit": UNIT,
         "n_gpus": world,
@@ -367,7 +447,7 @@ def bench_ours(args, rank, world, dev):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic, seeded (distributions as in the workload description)",
-        "config": {"workload": describe(w),
+        "config": {"workload": describe_kl(w) if args.kl else describe(w),
                    "global_batch": n * world, "seq_len": None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weight 1.05 GB), no flush",
@@ -394,6 +474,12 @@ def bench_ours(args, rank, world, dev):
     return out
 
 
+def traffic_key(w, args) -> str:
+    """Key of a workload variant in profiles/dram_traffic.json."""
+    key = w.name + ("+kl" if args.kl else "") + ("+fwd" if args.forward_only else "")
+    return key + ("+all_rows" if args.all_rows else "")
+
+
 # ----------------------------------------------------------------- oracle timing
 def _oracle_sample_step(xc, w, rows):
     import oracle
@@ -406,48 +492,63 @@ def _oracle_sample_step(xc, w, rows):
     oracle.backward(*args, 1.0, lse=f["lse"])
 
 
-def _calibrate_rows(xc, w, budget_s, max_rows):
+def _oracle_kl_sample_step(xc, w, rows):
+    from oracle import kl_oracle
+
+    args = (xc["hidden"][:rows], xc["weight"], xc["q"][:rows], xc["bias"],
+            xc["targets"][:rows], w.ignore_index, KL_TEMPERATURE, 1e-10, KL_REDUCTION)
+    kl_oracle.forward(*args)
+    kl_oracle.backward(*args, 1.0)
+
+
+def _calibrate_rows(xc, w, budget_s, max_rows, kl=False):
     """Rows per sample so that one oracle step takes at most about budget_s
     (linear in the rows of a 64-row trial, fixed costs included)."""
+    run = _oracle_kl_sample_step if kl else _oracle_sample_step
     t = time.perf_counter()
-    _oracle_sample_step(xc, w, 64)
+    run(xc, w, 64)
     per_row = (time.perf_counter() - t) / 64
     rows = int(budget_s / per_row)
     return max(8, min(max_rows, rows)), per_row
 
 
-def cpu_baseline(xc, w, budget_s=15.0):
-    rows, _ = _calibrate_rows(xc, w, budget_s, w.n)
+def cpu_baseline(xc, w, budget_s=15.0, kl=False):
+    rows, _ = _calibrate_rows(xc, w, budget_s, w.n, kl)
     t = time.perf_counter()
-    _oracle_sample_step(xc, w, rows)
+    (_oracle_kl_sample_step if kl else _oracle_sample_step)(xc, w, rows)
     dt = time.perf_counter() - t
+    what = "fused linear KL " if kl else ""
     return {"value": round(rows / dt, 2), "unit": UNIT, "cores": torch.get_num_threads(),
             "kind": "oracle",
-            "sample": f"fp64 forward+backward of the first {rows} rows of the workload "
+            "sample": f"fp64 {what}forward+backward of the first {rows} rows of the workload "
                       f"(full H={w.h}, V={w.v}) as one batch; {dt:.1f} s"}
 
 
 def bench_reference(args):
-    w = WORKLOADS[args.workload]
-    xc = make_inputs(w)
+    w = workload_of(args)
+    xc = make_bench_inputs(w, args.kl)
+    run = _oracle_kl_sample_step if args.kl else _oracle_sample_step
     total_budget = 150.0  # seconds for warmup + timed steps
     per_step = total_budget / (args.steps + max(args.warmup, 3))
-    rows, _ = _calibrate_rows(xc, w, per_step, w.n)
+    rows, _ = _calibrate_rows(xc, w, per_step, w.n, args.kl)
     for _ in range(max(args.warmup, 3)):
-        _oracle_sample_step(xc, w, rows)
+        run(xc, w, rows)
     t = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_sample_step(xc, w, rows)
+        run(xc, w, rows)
     dt = time.perf_counter() - t
     val = round(rows * args.steps / dt, 2)
-    sample = (f"each step: fp64 forward+backward of the first {rows} rows of the workload "
-              f"(full H={w.h}, V={w.v})")
+    what = "fused linear KL " if args.kl else ""
+    sample = (f"each step: fp64 {what}forward+backward of the first {rows} rows of the "
+              f"workload (full H={w.h}, V={w.v})")
     return {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+        "impl": "reference", "metric": KL_METRIC if args.kl else METRIC, "value": val,
+        "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w), "global_batch": rows},
+        "config": {"workload": describe_kl(w) if args.kl else describe(w),
+                   "global_batch": rows},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": torch.get_num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -470,6 +571,9 @@ def main():
     ap.add_argument("--z-loss", type=float, default=0.0)
     ap.add_argument("--all-rows", action="store_true",
                     help="run ignored rows through the GEMMs too (FLCE_SKIP_IGNORED_ROWS off)")
+    ap.add_argument("--kl", action="store_true",
+                    help="time the fused linear KL divergence (flce_kl_forward + "
+                         "flce_kl_backward) on the workload's shape instead")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -489,7 +593,7 @@ def main():
     out = bench_ours(args, rank, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w = workload_of(args)
-        out["cpu_baseline"] = cpu_baseline(make_inputs(w), w)
+        out["cpu_baseline"] = cpu_baseline(make_bench_inputs(w, args.kl), w, kl=args.kl)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
