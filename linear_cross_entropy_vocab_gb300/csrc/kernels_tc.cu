@@ -77,27 +77,50 @@ __device__ __forceinline__ void store32(T* dst, const float (&v)[32], int nv, fl
   }
 }
 
-// Fold 32 logits (the first nv valid) of columns [cb, cb+32) into st.
-template <bool FULL>
+// Fold 32 logits (the first nv valid) of columns [cb, cb+32) into st. The
+// chunk maximum is taken by a tree and the two sums of the chunk by four
+// interleaved partial sums, so that the dependent chains are 5 and 8 long
+// instead of 32 (the epilogue runs one warp per scheduler, so every step of
+// a chain is a stall). ARGMAX: also track the lowest index of the maximum.
+template <bool FULL, bool ARGMAX = true>
 __device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], int nv, int cb) {
-  float cm = -FLT_MAX;
+  float mx[16];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    if (FULL || k < nv) cm = fmaxf(cm, z[k]);
+  for (int k = 0; k < 16; ++k) {
+    const float lo = (FULL || 2 * k < nv) ? z[2 * k] : -FLT_MAX;
+    const float hi = (FULL || 2 * k + 1 < nv) ? z[2 * k + 1] : -FLT_MAX;
+    mx[k] = fmaxf(lo, hi);
   }
-  if (cm > st.m) {
-    int kf = 0;
 #pragma unroll
-    for (int k = 31; k >= 0; --k) {
-      if ((FULL || k < nv) && z[k] == cm) kf = k;
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
+  }
+  const float cm = mx[0];
+  if (cm > st.m) {
+    if constexpr (ARGMAX) {
+      int kf = 0;
+#pragma unroll
+      for (int k = 31; k >= 0; --k) {
+        if ((FULL || k < nv) && z[k] == cm) kf = k;
+      }
+      st.a = cb + kf;
     }
-    st.a = cb + kf;
     st.rebase(cm);
   }
+  float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float t4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int k = 0; k < 32; ++k) {
-    if (FULL || k < nv) st.add(z[k]);
+    if (FULL || k < nv) {
+      const float d = z[k] - st.m;
+      const float e = ex2_approx(d * kLog2e);
+      s4[k & 3] += e;
+      t4[k & 3] = fmaf(e, d, t4[k & 3]);
+    }
   }
+  st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+  st.t += (t4[0] + t4[1]) + (t4[2] + t4[3]);
 }
 
 // Lane l of the warp ends with the sum over the 32 lanes of v[l].
@@ -115,27 +138,48 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Loads q[c .. c+32) of one row (fewer when nv < 32; the rest are 0).
+// 32 entries q[c .. c+32) of one teacher row, fetched one chunk ahead of use.
+// issue() starts the loads of a full, 16-byte aligned chunk as streaming
+// (evict-first) 16-byte loads: each teacher entry is read once, so it should
+// not displace the weight and hidden tiles that other CTAs re-read from L2.
+// get() unpacks them; a partial or unaligned chunk is read there with scalar
+// loads instead. Entries past nv (and every entry of an inactive row) are 0.
 template <typename T>
-__device__ __forceinline__ void load_row32(const T* row_ptr, int64_t c, int nv, bool vec,
-                                           float (&q)[32]) {
-  if (vec && nv == 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(row_ptr + c);
+struct RowChunk32 {
+  uint4 w[4];
+  bool raw;
+
+  __device__ __forceinline__ void issue(const T* row_ptr, int64_t c, int nv, bool vec,
+                                        bool active) {
+    raw = active && vec && nv == 32;
+    if (raw) {
+      const uint4* src = reinterpret_cast<const uint4*>(row_ptr + c);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint4 w = __ldg(src + r);
-      const uint32_t parts[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        q[r * 8 + 2 * h] = Elem<T>::lo(parts[h]);
-        q[r * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
-      }
+      for (int r = 0; r < 4; ++r) w[r] = __ldcs(src + r);
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) q[k] = (k < nv) ? Elem<T>::to(row_ptr[c + k]) : 0.0f;
   }
-}
+
+  __device__ __forceinline__ void get(const T* row_ptr, int64_t c, int nv, bool active,
+                                      float (&q)[32]) const {
+    if (raw) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t parts[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          q[r * 8 + 2 * h] = Elem<T>::lo(parts[h]);
+          q[r * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
+        }
+      }
+    } else if (active) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) q[k] = (k < nv) ? Elem<T>::to(row_ptr[c + k]) : 0.0f;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) q[k] = 0.0f;
+    }
+  }
+};
 
 // The tail every dlogits epilogue shares: store the 32 values of D (times
 // dscale, rounded to T) for every buffer row (rows past the present ones hold
@@ -292,32 +336,42 @@ struct EpiFwdKL {
     st.init();
     float a_sum = 0.0f;  // sum q (log max(q, eps) - z)
     float q_sum = 0.0f;  // sum q
+    const bool vec = p.q_vec != 0;
+    RowChunk32<T> cur, nxt;
+    cur.issue(qrow, col0, p.v - col0 < 32 ? static_cast<int>(p.v - col0) : 32, vec, row_ok);
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int64_t cb = col0 + ch * 32;
       if (cb >= p.v) break;
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
+      const int64_t cn = cb + 32;  // next chunk of this tile
+      if (ch + 1 < kBN / 32 && cn < p.v)
+        nxt.issue(qrow, cn, p.v - cn < 32 ? static_cast<int>(p.v - cn) : 32, vec, row_ok);
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32<T>(p.bias, cb, nv, b);
 #pragma unroll
       for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
       if (nv == 32) {
-        fold_chunk<true>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<true, false>(st, z, nv, static_cast<int>(cb));
       } else {
-        fold_chunk<false>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<false, false>(st, z, nv, static_cast<int>(cb));
       }
       if (row_ok) {
         float q[32];
-        load_row32<T>(qrow, cb, nv, p.q_vec != 0, q);
+        cur.get(qrow, cb, nv, row_ok, q);  // 0 past nv
+        float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          if (k < nv) {
-            a_sum = fmaf(q[k], __logf(fmaxf(q[k], p.eps)) - z[k], a_sum);
-            q_sum += q[k];
-          }
+          // q = 0 past nv adds exactly 0 (z there is finite: the accumulator
+          // holds 0 for columns past V)
+          a4[k & 3] = fmaf(q[k], __logf(fmaxf(q[k], p.eps)) - z[k], a4[k & 3]);
+          q4[k & 3] += q[k];
         }
+        a_sum += (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        q_sum += (q4[0] + q4[1]) + (q4[2] + q4[3]);
       }
+      cur = nxt;
     }
     if (row_ok) p.partials[row * p.n_vt + n_tile] = make_float4(st.m, st.s, a_sum, q_sum);
   }
@@ -345,20 +399,21 @@ struct EpiDlogitsKL {
     const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v + p.c0;
     const int col0 = n_tile * kBN;
     const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
+    const bool vec = p.q_vec != 0;
+    RowChunk32<T> cur, nxt;
+    cur.issue(qrow, col0, p.width - col0 < 32 ? p.width - col0 : 32, vec, row_ok);
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = col0 + ch * 32;
       if (cb >= p.width) break;
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
+      const int cn = cb + 32;  // next chunk of this tile
+      if (ch + 1 < kBN / 32 && cn < p.width)
+        nxt.issue(qrow, cn, p.width - cn < 32 ? p.width - cn : 32, vec, row_ok);
       float z[32], b[32], q[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32<T>(p.bias, p.c0 + cb, nv, b);
-      if (row_ok) {
-        load_row32<T>(qrow, cb, nv, p.q_vec != 0, q);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) q[k] = 0.0f;
-      }
+      cur.get(qrow, cb, nv, row_ok, q);
       float d[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
@@ -368,6 +423,7 @@ struct EpiDlogitsKL {
       }
       emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, p.gb_partial, p.gb_ld,
                       p.c0, p.width, m_tile, n_eff, quarter, lane, ctl);
+      cur = nxt;
     }
   }
 };
