@@ -417,7 +417,10 @@ def bench_ours(args, rank, world, dev):
     roofline = None
     if dom is not None:
         launches, tot_ms = roles[dom]
-        per_step_flops = 2.0 * n * h * v if dom in GEMM_ROLES else 0.0
+        # algorithmic work of one launch: the rows it computes (ignored rows
+        # are left out of every contraction unless --all-rows)
+        n_work = n if args.all_rows else n_valid
+        per_step_flops = 2.0 * n_work * h * v if dom in GEMM_ROLES else 0.0
         launches_per_step = launches / args.steps
         flops_per_launch = per_step_flops / launches_per_step
         avg_ms = tot_ms / launches
@@ -426,7 +429,8 @@ def bench_ours(args, rank, world, dev):
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "peak_kind": f"bf16 sustained, {peak_src}",
-                    "flops_per_launch": flops_per_launch, "avg_launch_ms": round(avg_ms, 4),
+                    "flops_per_launch": flops_per_launch, "rows_per_launch": n_work,
+                    "avg_launch_ms": round(avg_ms, 4),
                     "traffic": measured_traffic(dom, traffic_key(w, args)),
                     "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
                                       "dram__bytes_write.sum per launch; null if the kernels "

@@ -12,7 +12,8 @@ one:
     and chunk boundaries, peaked rows, targets of sampled rows, the rest
     random.
 Plus a property that holds at any size: with softcap off and logit_scale 1,
-sum_j grad_weight[j, :] = 0 up to bf16 rounding.
+sum_j grad_weight[j, :] = 0 up to bf16 rounding. The fused linear KL
+divergence gets the same treatment at the Llama-3 head shape.
 
 These take minutes of host fp64 work each (the oracle's full forward is
 2·N·H·V multiply-adds).
@@ -99,3 +100,57 @@ def test_fullsize_parity(name):
         col = gw.sum(dim=0).abs()
         mag = gw.abs().sum(dim=0)
         assert bool((col <= 1e-2 * mag + 1e-12).all()), float((col / mag).max())
+
+
+def test_fullsize_kl_parity():
+    """The fused linear KL divergence at the Llama-3 head shape, in the
+    configuration `bench.py --kl` times: teacher probabilities from
+    make_teacher_probs, the workload's targets as labels (2 % ignored, left
+    out of the contractions), T = 1, batchmean. Per-row loss, lse and sum q
+    for all N rows; gradients on sampled rows; and, at any size,
+    sum_j grad_weight[j, :] = 0 (each counted row's p * sum q - q sums to 0
+    over the vocabulary)."""
+    from _parity import assert_grad_close, assert_rows_close
+    from linear_cross_entropy_vocab_gb300 import api
+    from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
+    from oracle import kl_oracle
+
+    w = WORKLOADS["llama3_head_bf16"]
+    x = make_inputs(w)
+    q = make_teacher_probs(w)
+    xd = to_dev(x)
+    qd = q.cuda()
+    tol = TOL[w.dtype]
+    err = torch.zeros((), dtype=torch.int32, device="cuda")
+    f = api.flce_kl_forward_tensors(xd["hidden"], xd["weight"], qd, xd["targets"], None,
+                                    w.ignore_index, 1.0, 1e-10, "batchmean", err_word=err,
+                                    skip_ignored=True)
+    go = torch.tensor(1.0, dtype=torch.float32, device="cuda")
+    gh, gw, _ = api.flce_kl_backward_tensors(xd["hidden"], xd["weight"], qd, f["lse_rows"],
+                                             f["qsum_rows"], f["n_counted"], go, xd["targets"],
+                                             None, w.ignore_index, 1.0, 1e-10, "batchmean",
+                                             err_word=err, skip_ignored=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    del qd
+    ref = kl_oracle.forward(x["hidden"], x["weight"], q, None, x["targets"], w.ignore_index, 1.0,
+                            1e-10, "batchmean")
+    counted = ref["counted"]
+    assert int(f["n_counted"]) == ref["n_counted"]
+    assert_rows_close("loss_rows", f["loss_rows"].cpu(), ref["loss"], tol["loss_rel"])
+    assert_rows_close("lse_rows", f["lse_rows"].cpu(), ref["lse"], tol["loss_rel"], counted)
+    assert_rows_close("qsum_rows", f["qsum_rows"].cpu(), ref["qsum"], 1e-5, counted)
+    r = ref["loss_out"]
+    assert abs(float(f["loss"]) - r) <= tol["loss_rel"] * max(1.0, abs(r))
+    rows = _sample_rows(w, x["targets"], torch.empty(0, dtype=torch.int64), k=256)
+    vocab = _sample_vocab(w, x["targets"], rows, torch.empty(0, dtype=torch.int64), k=128)
+    gref = kl_oracle.backward(x["hidden"], x["weight"], q, None, x["targets"], w.ignore_index,
+                              1.0, 1e-10, "batchmean", 1.0, rows=rows, vocab_rows=vocab)
+    gh_c, gw_c = gh.cpu(), gw.cpu()
+    assert_grad_close("grad_hidden", gh_c[rows], gref["grad_hidden"], tol)
+    assert_grad_close("grad_weight", gw_c[vocab], gref["grad_weight"], tol)
+    assert torch.all(gh_c[~counted] == 0)
+    g64 = gw_c.double()
+    col = g64.sum(dim=0).abs()
+    mag = g64.abs().sum(dim=0)
+    assert bool((col <= 1e-2 * mag + 1e-12).all()), float((col / mag).max())
