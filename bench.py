@@ -516,6 +516,23 @@ def _calibrate_rows(xc, w, budget_s, max_rows, kl=False):
     return max(8, min(max_rows, rows)), per_row
 
 
+def cpu_model() -> str:
+    """The host CPU's model name, as /proc/cpuinfo gives it (x86 and Arm)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            info = fh.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in info:
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    for line in info:  # Arm: implementer and part numbers only
+        if line.startswith("CPU part") and ":" in line:
+            return "Arm CPU part " + line.split(":", 1)[1].strip()
+    return "unknown"
+
+
 def cpu_baseline(xc, w, budget_s=15.0, kl=False):
     rows, _ = _calibrate_rows(xc, w, budget_s, w.n, kl)
     t = time.perf_counter()
@@ -523,7 +540,7 @@ def cpu_baseline(xc, w, budget_s=15.0, kl=False):
     dt = time.perf_counter() - t
     what = "fused linear KL " if kl else ""
     return {"value": round(rows / dt, 2), "unit": UNIT, "cores": torch.get_num_threads(),
-            "kind": "oracle",
+            "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"fp64 {what}forward+backward of the first {rows} rows of the workload "
                       f"(full H={w.h}, V={w.v}) as one batch; {dt:.1f} s"}
 
@@ -554,7 +571,7 @@ def bench_reference(args):
         "config": {"workload": describe_kl(w) if args.kl else describe(w),
                    "global_batch": rows},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": torch.get_num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

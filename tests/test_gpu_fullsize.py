@@ -154,3 +154,35 @@ def test_fullsize_kl_parity():
     col = g64.sum(dim=0).abs()
     mag = g64.abs().sum(dim=0)
     assert bool((col <= 1e-2 * mag + 1e-12).all()), float((col / mag).max())
+
+
+@pytest.mark.parametrize("kl", [False, True])
+def test_peak_memory_below_logits(kl):
+    """One forward+backward through the public autograd API at the Llama-3
+    head shape allocates, above what is live before it (inputs, and the
+    teacher probabilities for KL), less than the N x V logit matrix would
+    take in bf16 (N*V*2 bytes): the logits are never materialised. The
+    incremental peak includes grad_weight [V, H], grad_hidden and the
+    workspaces."""
+    from linear_cross_entropy_vocab_gb300 import fused_linear_cross_entropy, fused_linear_kl_div
+    from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
+
+    w = WORKLOADS["llama3_head_bf16"]
+    x = to_dev(make_inputs(w))
+    q = make_teacher_probs(w).cuda() if kl else None
+    h = x["hidden"].detach().requires_grad_(True)
+    wt = x["weight"].detach().requires_grad_(True)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    if kl:
+        loss = fused_linear_kl_div(h, wt, q, x["targets"])
+    else:
+        loss = fused_linear_cross_entropy(h, wt, x["targets"])
+    loss.backward()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    nxv = w.n * w.v * 2
+    assert peak < nxv, (peak, nxv)
+    assert torch.isfinite(loss).item()
