@@ -176,6 +176,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over the ranks of the default process group (the
+    slowest rank's time); `value` itself on one rank. `device` is where the
+    reduction runs: the GPU for NCCL, the CPU for gloo."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    `tokens_per_rank` tokens per step for `steps` steps, timed by the slowest
+    rank (weak scaling: the work per GPU is fixed)."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 # ----------------------------------------------------------------- our arm
 class Step:
     """Preallocated buffers and the two C-ABI calls of one fwd+bwd step."""
@@ -327,10 +346,7 @@ def bench_ours(args, rank, world, dev):
     prof, dropped = abi.flce_profile_collect()
     abi.flce_profile_enable(False)
     clk = clocks.stop()
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ------------------------------------------------------ end to end (host buffers)
     # Every step copies its inputs from pinned host memory and reads its loss
@@ -382,10 +398,7 @@ def bench_ours(args, rank, world, dev):
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     del bufs, steps2
 
     # ------------------------------------------------------ peak memory of the public API
@@ -407,10 +420,9 @@ def bench_ours(args, rank, world, dev):
 
     peaks, peak_src = load_peaks()
     flops_step = gemm_flops(n, h, v) / (4.0 if args.forward_only else 1.0)
-    sec = ms / 1e3
-    tok_s = world * n * args.steps / sec
+    tok_s = job_tokens_per_s(n, args.steps, world, ms)
     n_valid = int(step.n_valid.item())
-    achieved_step = flops_step * args.steps / sec / 1e12
+    achieved_step = flops_step * args.steps / (ms / 1e3) / 1e12
     # dominant kernel: the role with the largest share of device time
     roles = {k: val for k, val in prof.items()}
     dom = max(roles, key=lambda k: roles[k][1]) if roles else None
@@ -467,7 +479,7 @@ def bench_ours(args, rank, world, dev):
         "kernels": kernels,
         "gpu_launches": int(sum(val[0] for val in roles.values())),
         "profile_dropped": dropped,
-        "e2e": {"value": round(world * n * e2e_steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(job_tokens_per_s(n, e2e_steps, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host -> device each step on a side stream, double-buffered"},
         "clocks": clk,
