@@ -302,6 +302,21 @@ flce_status flce_kl_backward(const flce_kl_problem* p, const void* hidden,
                              void* stream);
 
 /* ------------------------------------------------------------------------
+ * Self-test of the bounded waits (not part of the method; the pages describe
+ * no such check). Every pipeline wait of the kernels gives up after a time
+ * budget, records FLCE_DEVERR_TIMEOUT in the error word and returns instead
+ * of spinning forever. This call exercises exactly those wait routines on an
+ * mbarrier that nothing arrives on, with a budget of budget_s seconds
+ * (0 < budget_s <= 1): once in a single CTA and once in a pair of CTAs (the
+ * cluster-scope wait). On completion of the stream's work, *err_word has
+ * FLCE_DEVERR_TIMEOUT set and result[0..2] (int32, device) are 0: each wait
+ * gave up. Nothing faults; the context stays usable.
+ *   err_word  int32 device scalar, ORed into (not cleared)
+ *   result    int32 device [3]                                           */
+flce_status flce_selftest_wait_timeout(int32_t* err_word, int32_t* result,
+                                       double budget_s, void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-kernel timing, for measurement tools (not part of the method; the
  * pages describe no profiler). While enabled, every kernel launch made by
  * flce_forward / flce_backward on the calling process is bracketed by two

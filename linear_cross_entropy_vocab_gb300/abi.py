@@ -55,6 +55,7 @@ EXPORTS = (
     "flce_kl_forward",
     "flce_kl_backward_workspace_size",
     "flce_kl_backward",
+    "flce_selftest_wait_timeout",
     "flce_status_string",
     "flce_last_error",
     "flce_device_supported",
@@ -164,6 +165,8 @@ def load() -> ctypes.CDLL:
         lib.flce_kl_backward.argtypes = [_KLPROB] + [_P] * 16
         lib.flce_kl_backward.argtypes[-2] = ctypes.c_size_t
         lib.flce_kl_backward.restype = ctypes.c_int
+        lib.flce_selftest_wait_timeout.argtypes = [_P, _P, ctypes.c_double, _P]
+        lib.flce_selftest_wait_timeout.restype = ctypes.c_int
         lib.flce_status_string.argtypes = [ctypes.c_int]
         lib.flce_status_string.restype = ctypes.c_char_p
         lib.flce_last_error.argtypes = []
@@ -297,6 +300,14 @@ def flce_kl_backward(p, hidden, weight, bias, target_probs, labels, lse_rows, qs
                                  stream)
     if check:
         _check(st, "flce_kl_backward")
+    return st
+
+
+def flce_selftest_wait_timeout(err_word, result, budget_s, stream, check=True) -> int:
+    """Run the bounded-wait self-test (see include/flce.h)."""
+    st = load().flce_selftest_wait_timeout(err_word, result, float(budget_s), stream)
+    if check:
+        _check(st, "flce_selftest_wait_timeout")
     return st
 
 

@@ -1225,6 +1225,22 @@ flce_status flce_kl_backward(const flce_kl_problem* k, const void* hidden, const
                        stream);
 }
 
+flce_status flce_selftest_wait_timeout(int32_t* err_word, int32_t* result, double budget_s,
+                                       void* stream) {
+  g_err[0] = 0;
+  if (err_word == nullptr || result == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "err_word and result are required");
+  if (!(budget_s > 0.0) || budget_s > 1.0)
+    return fail(FLCE_ERR_INVALID_ARG, "budget_s must be in (0, 1] seconds");
+  DeviceInfo dev;
+  flce_status st = check_device(&dev);
+  if (st != FLCE_OK) return st;
+  const cudaError_t e =
+      flce::launch_wait_selftest(err_word, static_cast<uint64_t>(budget_s * 1e9), result,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FLCE_OK : cuda_fail(e, "wait self-test kernel");
+}
+
 // Forward pass for callers that cannot provide a workspace: the same kernels
 // as flce_forward(), with their scratch taken from flce_static_scratch.
 flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden, const void* weight,

@@ -152,6 +152,9 @@ cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
                                   const CUtensorMap& tm_weight_mn, const GemmGeom& g,
                                   const AccRowsParams& p, int sms, cudaStream_t s);
 
+// Bounded-wait self-test: result[0] (one CTA) and result[1..2] (a CTA pair).
+cudaError_t launch_wait_selftest(int* err_word, uint64_t budget_ns, int* result, cudaStream_t s);
+
 // KL per-row merge and the scalar loss.
 struct MergeKLParams {
   const float4* partials;

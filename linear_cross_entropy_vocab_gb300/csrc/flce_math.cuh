@@ -37,6 +37,33 @@ __device__ __forceinline__ float tanh_exp2(float x) {
   return __fdividef(e - 1.0f, e + 1.0f);
 }
 
+// Packed pairs of fp32 values (the .f32x2 arithmetic of sm_100-family GPUs):
+// one instruction adds, multiplies or fused-multiply-adds two lanes, each
+// rounded as the scalar instruction would round it.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 struct LogitXform {
   float scale;
   float softcap;      // used only if has_cap
@@ -48,6 +75,21 @@ struct LogitXform {
     const float u = scale * (acc + b);
     if (has_cap) return softcap * tanh_exp2(u * inv_softcap);
     return u;
+  }
+  // The transform of 32 accumulator values in place, two at a time where
+  // there is no softcap (the same roundings as operator()).
+  __device__ __forceinline__ void apply32(float (&z)[32], const float (&b)[32]) const {
+    if (has_cap) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) z[k] = (*this)(z[k], b[k]);
+      return;
+    }
+    const uint64_t s2 = f2_pack(scale, scale);
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      const uint64_t u = f2_mul(s2, f2_add(f2_pack(z[k], z[k + 1]), f2_pack(b[k], b[k + 1])));
+      f2_unpack(u, z[k], z[k + 1]);
+    }
   }
   // dz/du at final logit z: 1 - (z/softcap)^2 with a softcap, else 1.
   __device__ __forceinline__ float dz_du(float z) const {

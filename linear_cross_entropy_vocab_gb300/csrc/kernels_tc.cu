@@ -110,13 +110,33 @@ __device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], i
   }
   float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float t4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if constexpr (FULL) {
+    // two columns per instruction: d = z - m, e = 2^(d log2 e), s += e,
+    // t += e d; the four running sums are two packed pairs
+    const uint64_t nm2 = f2_pack(-st.m, -st.m), l2 = f2_pack(kLog2e, kLog2e);
+    uint64_t sp[2] = {0, 0}, tp[2] = {0, 0};
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    if (FULL || k < nv) {
-      const float d = z[k] - st.m;
-      const float e = ex2_approx(d * kLog2e);
-      s4[k & 3] += e;
-      t4[k & 3] = fmaf(e, d, t4[k & 3]);
+    for (int k = 0; k < 32; k += 2) {
+      const uint64_t d = f2_add(f2_pack(z[k], z[k + 1]), nm2);
+      float x0, x1;
+      f2_unpack(f2_mul(d, l2), x0, x1);
+      const uint64_t e = f2_pack(ex2_approx(x0), ex2_approx(x1));
+      sp[(k >> 1) & 1] = f2_add(sp[(k >> 1) & 1], e);
+      tp[(k >> 1) & 1] = f2_fma(e, d, tp[(k >> 1) & 1]);
+    }
+    f2_unpack(sp[0], s4[0], s4[1]);
+    f2_unpack(sp[1], s4[2], s4[3]);
+    f2_unpack(tp[0], t4[0], t4[1]);
+    f2_unpack(tp[1], t4[2], t4[3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      if (k < nv) {
+        const float d = z[k] - st.m;
+        const float e = ex2_approx(d * kLog2e);
+        s4[k & 3] += e;
+        t4[k & 3] = fmaf(e, d, t4[k & 3]);
+      }
     }
   }
   st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
@@ -181,28 +201,35 @@ struct RowChunk32 {
   }
 };
 
-// The tail every dlogits epilogue shares: store the 32 values of D (times
-// dscale, rounded to T) for every buffer row (rows past the present ones hold
-// d = 0), and add the tile's fixed-order fp32 column sums to the grad_bias
-// partials.
+// The tail every dlogits epilogue shares, per 32-column chunk `ch`: store
+// the 32 values of D (times dscale, rounded to T) for every buffer row (rows
+// past the present ones hold d = 0) and, when grad_bias partials are wanted,
+// leave this warp's 32 column sums of D over its 32 rows in ctl->red.
 template <typename T>
 __device__ __forceinline__ void emit_dlogits(float (&d)[32], int nv, int64_t row, int64_t buf_rows,
                                              void* dbuf, int64_t ldd, int cb, float dscale,
-                                             float* gb_partial, int64_t gb_ld, int c0, int width,
-                                             int m_tile, int64_t n_eff, int quarter, int lane,
+                                             bool bias_sums, int ch, int quarter, int lane,
                                              GemmCtl* ctl) {
   if (row < buf_rows) store32<T>(static_cast<T*>(dbuf) + row * ldd + cb, d, nv, dscale);
-  if (gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff) {
-    // column sums of D over this tile's 128 rows, in a fixed order
-    const float colsum = transpose_reduce32(d, lane);
-    ctl->red[quarter][lane] = colsum;
-    named_bar_sync(1, kEpiThreads);
-    if (quarter == 0 && cb + lane < width) {
-      const float tot =
-          ((ctl->red[0][lane] + ctl->red[1][lane]) + ctl->red[2][lane]) + ctl->red[3][lane];
-      gb_partial[static_cast<int64_t>(m_tile) * gb_ld + c0 + cb + lane] = tot;
+  if (bias_sums) ctl->red[quarter][ch][lane] = transpose_reduce32(d, lane);
+}
+
+// After the chunks of a tile: grad_bias partials of the tile's columns, the
+// sum of the four warps' column sums in a fixed order. One barrier per tile;
+// the next tile's writes to ctl->red come after the epilogue warps' next
+// common barrier (epi_all), so none overtakes these reads.
+__device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld, int m_tile,
+                                                int c0, int col0, int width, int quarter,
+                                                int lane, GemmCtl* ctl) {
+  named_bar_sync(1, kEpiThreads);
+#pragma unroll
+  for (int ch = 2 * quarter; ch < 2 * quarter + 2; ++ch) {  // warp q: chunks 2q, 2q+1
+    const int col = col0 + ch * 32 + lane;
+    if (col < width) {
+      const float tot = ((ctl->red[0][ch][lane] + ctl->red[1][ch][lane]) + ctl->red[2][ch][lane]) +
+                        ctl->red[3][ch][lane];
+      gb_partial[static_cast<int64_t>(m_tile) * gb_ld + c0 + col] = tot;
     }
-    named_bar_sync(1, kEpiThreads);
   }
 }
 
@@ -234,8 +261,7 @@ struct EpiFwdStats {
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32<T>(p.bias, cb, nv, b);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
+      p.xf.apply32(z, b);
       if (nv == 32) {
         fold_chunk<true>(st, z, nv, static_cast<int>(cb));
       } else {
@@ -287,6 +313,8 @@ struct EpiDlogits {
     const int64_t tl = t - p.c0;  // target column within this chunk
     const int col0 = n_tile * kBN;
     const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
+    // grad_bias column partials, for tiles holding present rows (uniform per tile)
+    const bool bias_sums = p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       const int cb = col0 + ch * 32;
@@ -296,10 +324,21 @@ struct EpiDlogits {
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32<T>(p.bias, p.c0 + cb, nv, b);
       float d[32];
+      p.xf.apply32(z, b);
+      if (!p.xf.has_cap) {
+        // two columns per instruction; dz/dlin = logit_scale (in gs)
+        const uint64_t l2 = f2_pack(kLog2e, kLog2e), nl2 = f2_pack(-lse2, -lse2);
+        const uint64_t pz2 = f2_pack(pz, pz), ne2 = f2_pack(-eps_v, -eps_v);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        z[k] = p.xf(z[k], b[k]);
-        d[k] = fmaf(ex2_approx(fmaf(z[k], kLog2e, -lse2)), pz, -eps_v);
+        for (int k = 0; k < 32; k += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(z[k], z[k + 1]), l2, nl2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(ex2_approx(x0), ex2_approx(x1)), pz2, ne2), d[k], d[k + 1]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          d[k] = fmaf(ex2_approx(fmaf(z[k], kLog2e, -lse2)), pz, -eps_v);
       }
       const int64_t tk = tl - cb;
       if (tk >= 0 && tk < nv) {
@@ -308,13 +347,23 @@ struct EpiDlogits {
           if (k == tk) d[k] -= on_target;
         }
       }
+      if (!row_ok) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        d[k] = row_ok ? d[k] * gs * p.xf.dz_du(z[k]) : 0.0f;
+        for (int k = 0; k < 32; ++k) d[k] = 0.0f;
+      } else if (!p.xf.has_cap) {
+        const uint64_t g2 = f2_pack(gs, gs);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2)
+          f2_unpack(f2_mul(f2_pack(d[k], d[k + 1]), g2), d[k], d[k + 1]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) d[k] = d[k] * gs * p.xf.dz_du(z[k]);
       }
-      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, p.gb_partial, p.gb_ld,
-                      p.c0, p.width, m_tile, n_eff, quarter, lane, ctl);
+      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, bias_sums, ch, quarter,
+                      lane, ctl);
     }
+    if (bias_sums)
+      flush_bias_sums(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, lane, ctl);
   }
 };
 
@@ -350,8 +399,7 @@ struct EpiFwdKL {
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
       load_bias32<T>(p.bias, cb, nv, b);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) z[k] = p.xf(z[k], b[k]);
+      p.xf.apply32(z, b);
       if (nv == 32) {
         fold_chunk<true, false>(st, z, nv, static_cast<int>(cb));
       } else {
@@ -399,6 +447,7 @@ struct EpiDlogitsKL {
     const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v + p.c0;
     const int col0 = n_tile * kBN;
     const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
+    const bool bias_sums = p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff;
     const bool vec = p.q_vec != 0;
     RowChunk32<T> cur, nxt;
     cur.issue(qrow, col0, p.width - col0 < 32 ? p.width - col0 : 32, vec, row_ok);
@@ -421,10 +470,12 @@ struct EpiDlogitsKL {
         const float pr = ex2_approx(fmaf(z[k], kLog2e, -lse2));
         d[k] = counted ? fmaf(pr, qs, -q[k]) * gs * p.xf.dz_du(z[k]) : 0.0f;
       }
-      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, p.gb_partial, p.gb_ld,
-                      p.c0, p.width, m_tile, n_eff, quarter, lane, ctl);
+      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, bias_sums, ch, quarter,
+                      lane, ctl);
       cur = nxt;
     }
+    if (bias_sums)
+      flush_bias_sums(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, lane, ctl);
   }
 };
 
@@ -531,6 +582,50 @@ struct EpiAccRows {
     }
   }
 };
+
+// ------------------------------------------------------------ wait self-test
+// One thread per CTA waits, through the GEMM pipeline's own bounded wait, on
+// phase 0 of an mbarrier that nothing arrives on: the wait must give up after
+// `budget_ns`, set FLCE_DEVERR_TIMEOUT in *err_word and return false, which
+// the thread records in result[blockIdx.x] (0 = gave up, 1 = the phase
+// completed). CG = 2 runs in clusters of two CTAs and uses the cluster-scope
+// wait of the CTA-pair kernels. No tensor memory, copy or MMA is involved.
+template <int CG>
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int* err_word, uint64_t budget_ns,
+                                                            int* result) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = wait_bar<CG>(smem_addr(&bar), 0u, &abort_flag, err_word, budget_ns);
+    result[blockIdx.x] = ok ? 1 : 0;
+  }
+}
+
+cudaError_t launch_wait_selftest(int* err_word, uint64_t budget_ns, int* result, cudaStream_t s) {
+  wait_selftest_kernel<1><<<1, 32, 0, s>>>(err_word, budget_ns, result);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, wait_selftest_kernel<2>, err_word, budget_ns, result + 1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 // ------------------------------------------------------------------ launchers
 namespace {

@@ -61,7 +61,7 @@ struct GemmCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float red[4][32];  // epilogue scratch: per-warp column sums
+  float red[4][kBN / 32][32];  // epilogue scratch: per-warp column sums, [quarter][chunk][lane]
 };
 
 template <int CG>
@@ -161,9 +161,9 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 template <int CG>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         int* err_word) {
+                                         int* err_word, uint64_t budget_ns = kWaitBudgetNs) {
   if constexpr (CG == 1) {
-    return mbar_wait(bar, parity, abort_flag, err_word);
+    return mbar_wait(bar, parity, abort_flag, err_word, budget_ns);
   } else {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -171,7 +171,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       if (mbar_try_wait_cluster(bar, parity)) return true;
       if ((it & 63u) == 0u) {
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+        if (globaltimer_ns() - t0 > budget_ns) {
           *abort_flag = 1;
           if (err_word) atomicOr(err_word, 2 /* FLCE_DEVERR_TIMEOUT */);
           return false;

@@ -61,14 +61,14 @@ constexpr uint64_t kWaitBudgetNs = 4000000000ull;  // 4 s
 // complete. Returns false (after flagging) on timeout or when another role
 // of this CTA has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err_word) {
+                                          int* err_word, uint64_t budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      if (globaltimer_ns() - t0 > budget_ns) {
         *abort_flag = 1;
         if (err_word) atomicOr(err_word, 2 /* FLCE_DEVERR_TIMEOUT */);
         return false;
