@@ -464,11 +464,23 @@ struct EpiDlogitsKL {
       load_bias32<T>(p.bias, p.c0 + cb, nv, b);
       cur.get(qrow, cb, nv, row_ok, q);
       float d[32];
+      p.xf.apply32(z, b);
+      if (!counted) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        z[k] = p.xf(z[k], b[k]);
-        const float pr = ex2_approx(fmaf(z[k], kLog2e, -lse2));
-        d[k] = counted ? fmaf(pr, qs, -q[k]) * gs * p.xf.dz_du(z[k]) : 0.0f;
+        for (int k = 0; k < 32; ++k) d[k] = 0.0f;
+      } else {
+        // two columns per instruction (the KL divergence has no softcap, so
+        // dz/dlin = 1/T is in gs)
+        const uint64_t l2 = f2_pack(kLog2e, kLog2e), nl2 = f2_pack(-lse2, -lse2);
+        const uint64_t qs2 = f2_pack(qs, qs), g2 = f2_pack(gs, gs);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(z[k], z[k + 1]), l2, nl2), x0, x1);
+          const uint64_t pq = f2_fma(f2_pack(ex2_approx(x0), ex2_approx(x1)), qs2,
+                                     f2_pack(-q[k], -q[k + 1]));
+          f2_unpack(f2_mul(pq, g2), d[k], d[k + 1]);
+        }
       }
       emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, bias_sums, ch, quarter,
                       lane, ctl);
