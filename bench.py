@@ -40,8 +40,35 @@ GEMM_ROLES = ("fwd_stats", "fwd_kl", "bwd_dlogits", "bwd_dlogits_kl", "bwd_grad_
               "bwd_grad_hidden")
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source without its comments, whitespace runs collapsed to one
+    space: what the compiler sees, so that editing a comment does not count
+    as changing a kernel. String and character literals are kept verbatim."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sources_sha256() -> str:
-    """Hash of the CUDA sources and the C header, in a fixed file order."""
+    """Hash of the CUDA sources and the C header (comments stripped), in a
+    fixed file order."""
     import glob
     import hashlib
 
@@ -50,8 +77,8 @@ def kernel_sources_sha256() -> str:
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.relpath(f, ROOT).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(strip_c_comments(fh.read()).encode())
     return h.hexdigest()
 
 

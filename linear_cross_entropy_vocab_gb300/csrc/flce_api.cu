@@ -1,7 +1,10 @@
 // C ABI of libflce.so (declared in include/flce.h): argument checks,
-// workspace planning, tensor-map encoding and the launch sequence of the
-// forward and backward passes. No device memory is allocated here and no
-// call synchronises the caller's stream.
+// workspace planning, tensor-map encoding and the launch sequences of the
+// forward and backward passes of the fused linear cross-entropy and of the
+// fused linear KL divergence (which shares the backward sequence), plus the
+// fixed-scratch forward, the bounded-wait self-test and the launch profiler.
+// No device memory is allocated here and no call synchronises the caller's
+// stream.
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>

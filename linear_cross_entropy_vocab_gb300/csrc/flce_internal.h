@@ -20,8 +20,9 @@ constexpr int kPairCG = 2;
 constexpr int kTileRowsTC = kBM * kPairCG;
 constexpr int kBLoadRowsTC = kBN / kPairCG;
 
-// Width of one vocabulary tile of the forward statistics (tensor-core path);
-// the fp32 path uses kSimtTileV.
+// Tile of the fp32 (FFMA) kernels: kSimtTileN rows x kSimtTileV vocabulary
+// columns; the forward statistics of the fp32 path are per kSimtTileV
+// columns (the tensor-core path's per kBN).
 constexpr int kSimtTileV = 128;
 constexpr int kSimtTileN = 32;
 

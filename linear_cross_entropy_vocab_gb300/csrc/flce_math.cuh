@@ -1,6 +1,7 @@
-// Device math shared by the CUDA kernels of the fused linear cross-entropy:
-// the logit transform (bias, logit_scale, softcap), the running softmax
-// statistics a vocabulary sweep keeps per row, and their merge.
+// Device math shared by the CUDA kernels of the fused linear cross-entropy
+// and KL divergence: the logit transform (bias, logit_scale, softcap), the
+// running softmax statistics a vocabulary sweep keeps per row and their
+// merge, the upstream gradient of a row, and packed-pair fp32 arithmetic.
 //
 // "fused-linear-ce" model card (trl-lib), §Algorithm: each logit tile gets
 // bias / logit_scale / softcap and is folded into a running log-sum-exp with

@@ -1,10 +1,11 @@
-// bf16 tensor-core kernels of the fused linear cross-entropy (sm_103a).
+// Tensor-core kernels (sm_103a) of the fused linear cross-entropy and of the
+// fused linear KL divergence.
 //
 // Four instances of the persistent tcgen05 GEMM (tc_gemm.cuh), one per
 // contraction of the method ("fused-linear-ce" model card, §Algorithm):
-//   fwd_stats   logits = hidden @ W^T per 128 x 256 tile, folded on the fly
-//               into per-(row, vocabulary tile) softmax statistics; nothing of
-//               size N x V is written.
+//   fwd_stats   logits = hidden @ W^T per 256 x 256 pair tile, folded on the
+//               fly into per-(row, vocabulary tile) softmax statistics;
+//               nothing of size N x V is written.
 //   bwd_dlogits the same logits recomputed for one vocabulary chunk, turned
 //               into D = g (p - onehot) dz/dlin and stored in bf16.
 //   grad_weight grad_W[chunk] = D^T @ hidden (K = tokens, fp32 in TMEM,
@@ -15,6 +16,13 @@
 // both, with A and B of one type). For fp16, D is stored scaled by a power of
 // two so that its small entries stay in fp16's normal range; the two gradient
 // GEMMs undo the scale in their epilogues.
+//
+// The KL divergence (FusedLinearKLDivLoss pull request, Liger-Kernel #1423,
+// Details) runs the same four contractions; two epilogues differ:
+//   fwd_kl          per (row, tile): the softmax statistics (m, s) and, from
+//                   the teacher row, A = sum q (log max(q, eps) - z), Q = sum q;
+//   bwd_dlogits_kl  D = g (p Q - q) / T.
+// The file also holds the self-test kernel of the bounded waits.
 #include <cfloat>
 #include <cstdint>
 #include <cuda.h>
