@@ -413,6 +413,18 @@ def bench_ours(args, rank, world, dev):
             if steps2[b].metrics is not None:
                 met_h.copy_(steps2[b].metrics, non_blocking=True)
 
+    # host link bandwidth: one copy of a step's inputs alone, on the copy stream
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    c0.record(copy_stream)
+    with torch.cuda.stream(copy_stream):
+        for k, t in pin.items():
+            if t is not None:
+                bufs[0][k].copy_(t, non_blocking=True)
+    c1.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    h2d_gbs = h2d / (c0.elapsed_time(c1) / 1e3) / 1e9
+
     e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier()
@@ -508,7 +520,8 @@ def bench_ours(args, rank, world, dev):
         "profile_dropped": dropped,
         "e2e": {"value": round(job_tokens_per_s(n, e2e_steps, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": "pinned host -> device each step on a side stream, double-buffered"},
+                "copies": "pinned host -> device each step on a side stream, double-buffered",
+                "h2d_gb_per_s": round(h2d_gbs, 1)},
         "clocks": clk,
         "memory": {"peak_incremental_bytes_public_api": int(peak_incr),
                    "nxv_bf16_bytes": n * v * 2,
