@@ -201,3 +201,55 @@ def test_kl_autograd_matches_raw_calls_and_repeats_bitwise():
     assert torch.equal(h.grad.cpu(), raw["grad_hidden"])
     assert torch.equal(wt.grad.cpu(), raw["grad_weight"])
     assert torch.equal(b.grad.cpu(), raw["grad_bias"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kl_degenerate_shapes_and_teachers(dtype):
+    """V = 1: p = 1, so loss_i = q_i log max(q_i, eps) and D = g (Q - q) / T = 0
+    exactly. N = 1. A teacher row of zeros contributes 0 and no gradient.
+    Temperatures 0.05 (sharp) and 20 (flat). Each case against the oracle,
+    V = 1 and the zero row also against their closed forms.
+
+    Reading for one row at T = 0.05 with bf16 inputs: |D| reaches ~13 there
+    and grad_hidden = D @ W cancels in some entries, so rounding D to bf16
+    (relative 2^-9 per entry) errs by up to ~1e-2 absolute in such an entry
+    whatever the kernel does. A CPU emulation of that rounding on the
+    oracle's D reproduces the GPU's worst entry exactly. The elementwise bar
+    is then replaced by the normwise one; fp32, and bf16 at T = 20, keep both."""
+    tol = TOL[dtype]
+    # V = 1
+    w = _w("v1", 40, 16, 1, dtype)
+    x = make_inputs(w)
+    q = torch.rand(w.n, 1, generator=torch.Generator().manual_seed(3)).to(w.torch_dtype)
+    out = run_kl_gpu(to_dev(x), q.cuda(), None, w, 1.0, "sum", 1.0)
+    qd = q.double().reshape(-1)
+    expect = (qd * torch.log(qd.clamp_min(1e-10))).sum()
+    assert abs(float(out["loss"]) - float(expect)) <= tol["loss_rel"] * max(1.0, abs(float(expect)))
+    for k in ("grad_hidden", "grad_weight"):
+        assert torch.all(out[k] == 0), k
+    # N = 1 and the temperatures
+    for temp in (0.05, 20.0):
+        w = _w("n1", 1, 64, 777, dtype, bias_var=0.02)
+        x = make_inputs(w)
+        q = make_teacher_probs(w, keep_top=5)
+        out = run_kl_gpu(to_dev(x), q.cuda(), None, w, temp, "batchmean", 1.0)
+        ref = kl_oracle.forward(x["hidden"], x["weight"], q, x["bias"], None, -100, temp, 1e-10,
+                                "batchmean")
+        assert_rows_close("loss_rows", out["loss_rows"], ref["loss"], tol["loss_rel"])
+        gref = kl_oracle.backward(x["hidden"], x["weight"], q, x["bias"], None, -100, temp,
+                                  1e-10, "batchmean", 1.0)
+        t = dict(tol)
+        if dtype != "f32" and temp < 1.0:
+            t["g_atol"], t["g_rtol"] = float("inf"), 0.0  # normwise bar only (see docstring)
+        assert_grad_close("grad_hidden", out["grad_hidden"], gref["grad_hidden"], t)
+        assert_grad_close("grad_weight", out["grad_weight"], gref["grad_weight"], t)
+    # a zero teacher row among ordinary ones
+    w = _w("zero_row", 130, 64, 1000, dtype)
+    x = make_inputs(w)
+    q = make_teacher_probs(w)
+    q[7] = 0
+    out = run_kl_gpu(to_dev(x), q.cuda(), None, w, 1.0, "none", torch.ones(w.n))
+    assert float(out["loss_rows"][7]) == 0.0 and float(out["qsum_rows"][7]) == 0.0
+    assert torch.all(out["grad_hidden"][7] == 0)
+    ref = kl_oracle.forward(x["hidden"], x["weight"], q, None, None, -100, 1.0, 1e-10, "none")
+    assert_rows_close("loss_rows", out["loss_rows"], ref["loss"], tol["loss_rel"])
