@@ -14,7 +14,8 @@
  *   mean_token_accuracy = #{valid i : argmax_j z_ij == t_i} / n_valid
  *   entropy             = sum_{valid i} (lse_i - sum_j p_ij z_ij) / n_valid   (nats)
  *
- * and its backward (§Algorithm: "forms p - onehot"):
+ * and its backward (§Algorithm: the logits are recomputed and the logit
+ * gradient is the softmax minus the one-hot target):
  *
  *   D_ij          = g_i (p_ij - [j == t_i]) * logit_scale * (1 - tanh^2(u_ij/softcap))
  *   grad_hidden   = D @ weight,  grad_weight = D^T @ hidden,  grad_bias = sum_i D_ij
@@ -133,10 +134,10 @@ typedef struct flce_problem {
 #define FLCE_SKIP_IGNORED_ROWS 1
 
 /* Bytes of device workspace flce_forward() needs for `p` (0 if `p` is
- * invalid). Cite: §Algorithm ("tiles over the vocabulary ... merges the tile
- * into a running log-sum-exp"): the workspace holds the per-(row, vocabulary
- * tile) statistics the merge combines, about N * ceil(V/256) * 16 bytes
- * (20 with label smoothing). */
+ * invalid). Following §Algorithm (the vocabulary is swept in tiles, each
+ * folded into a running log-sum-exp), the workspace holds the per-(row,
+ * vocabulary tile) statistics that the merge combines: about
+ * N * ceil(V/256) * 16 bytes (20 with label smoothing). */
 size_t flce_forward_workspace_size(const flce_problem* p);
 
 /* Forward pass. Cite: §Algorithm (forward), §Metrics for free.

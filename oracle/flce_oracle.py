@@ -41,7 +41,8 @@ design notes):
     gets a NaN loss, is never "correct", and contributes no gradient.
 
 Two options from the feature list of the CuTe-DSL FLCE pull request
-(Liger-Kernel #1287, §Summary: "z-loss, softcap, label smoothing, ..."),
+(Liger-Kernel #1287, §Summary, which lists z-loss, softcap and label smoothing
+among its options),
 which names them without defining them; the readings taken:
   * label_smoothing eps: the target distribution is (1-eps)*onehot + eps/V,
     so loss_i = (1-eps)*(lse_i - z_{i,t_i}) + eps*(lse_i - mean_j z_ij);

@@ -23,7 +23,8 @@ p_ij * sum_k q_ik - q_ij; with respect to the linear logits it carries the
 
 Readings where the pages are silent:
   * ignored rows: a row whose label equals ignore_index contributes no loss
-    and no gradient (the pull request: "ignore_index via shift_labels");
+    and no gradient (the pull request handles ignore_index through its
+    shifted labels);
     without labels every row counts;
   * "batchmean" divides the summed loss by the number of counted rows,
     "mean" by that number times V (torch.nn.KLDivLoss divides by the batch
