@@ -176,9 +176,11 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
                                return_metrics: bool = False, *,
                                label_smoothing: float = 0.0, z_loss: float = 0.0):
     """Cross-entropy of softcap(logit_scale * (hidden @ weight.T + bias))
-    against targets, without materialising the (N, V) logits.
+    against targets, without materialising the (N, V) logits. hidden may
+    carry leading batch dimensions ([..., H] with targets [...]); its rows
+    are flattened.
 
-    Returns the loss (0-d for 'mean'/'sum', (N,) for 'none'), or with
+    Returns the loss (0-d for 'mean'/'sum', targets-shaped for 'none'), or with
     return_metrics ``(loss, {"mean_token_accuracy": 0-d, "entropy": 0-d})``;
     metrics are over non-ignored positions, entropy in nats.
 
@@ -187,6 +189,12 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
     """
     if reduction not in abi.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(abi.REDUCTIONS)}")
+    batch_shape = targets.shape
+    if hidden.dim() > 2:  # leading batch dimensions: rows are flattened
+        if hidden.shape[:-1] != targets.shape:
+            raise ValueError("hidden [..., H] and targets [...] must share the leading shape")
+        hidden = hidden.reshape(-1, hidden.shape[-1])
+        targets = targets.reshape(-1)
     hidden = hidden.contiguous()
     weight = weight.contiguous()
     targets = targets.contiguous()
@@ -195,6 +203,8 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
                                                    int(ignore_index), float(logit_scale),
                                                    softcap, reduction, bool(return_metrics),
                                                    float(label_smoothing), float(z_loss))
+    if reduction == "none":
+        loss = loss.reshape(batch_shape)
     if not return_metrics:
         return loss
     return loss, {"mean_token_accuracy": metrics[0], "entropy": metrics[1]}
@@ -319,15 +329,26 @@ def fused_linear_kl_div(hidden: torch.Tensor, weight: torch.Tensor,
                         reduction: str = "batchmean"):
     """KL(target || softmax((hidden @ weight.T + bias) / temperature)) per row,
     reduced like torch.nn.KLDivLoss ('batchmean', 'mean', 'sum', 'none'),
-    without materialising the (N, V) logits. Rows whose label equals
+    without materialising the (N, V) logits. hidden [..., H] may carry
+    leading batch dimensions, matched by target_probs [..., V] and labels. Rows whose label equals
     ignore_index are left out (labels None: every row counts). The teacher
     probabilities get no gradient."""
     if reduction not in abi.KL_REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(abi.KL_REDUCTIONS)}")
+    batch_shape = hidden.shape[:-1]
+    if hidden.dim() > 2:  # leading batch dimensions: rows are flattened
+        if target_probs.shape[:-1] != batch_shape or (
+                labels is not None and labels.shape != batch_shape):
+            raise ValueError("hidden [..., H], target_probs [..., V] and labels [...] must "
+                             "share the leading shape")
+        hidden = hidden.reshape(-1, hidden.shape[-1])
+        target_probs = target_probs.reshape(-1, target_probs.shape[-1])
+        labels = None if labels is None else labels.reshape(-1)
     hidden = hidden.contiguous()
     weight = weight.contiguous()
     target_probs = target_probs.detach().contiguous()
     labels = None if labels is None else labels.contiguous()
     bias = None if bias is None else bias.contiguous()
-    return _FusedLinearKLDiv.apply(hidden, weight, bias, target_probs, labels,
+    loss = _FusedLinearKLDiv.apply(hidden, weight, bias, target_probs, labels,
                                    int(ignore_index), float(temperature), float(eps), reduction)
+    return loss.reshape(batch_shape) if reduction == "none" else loss

@@ -120,3 +120,40 @@ def test_skip_ignored_matches_all_rows(reduction):
     for k in ("grad_weight", "grad_bias"):
         d = (a[k].double() - b[k].double()).norm() / a[k].double().norm()
         assert float(d) < 1e-2, (k, float(d))
+
+
+def test_leading_batch_dimensions_match_flattened_rows():
+    """hidden [B, T, H] with targets [B, T] (and teacher probabilities
+    [B, T, V] for KL) give bitwise the results of the flattened rows; 'none'
+    returns per-position losses in the batch shape."""
+    from linear_cross_entropy_vocab_gb300 import fused_linear_kl_div
+    from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
+
+    w = Workload("batched", 600, 128, 1000, "bf16", ignore_frac=0.1)
+    x = to_dev(make_inputs(w))
+    q = make_teacher_probs(w).cuda()
+    for reduction in ("mean", "none"):
+        outs = []
+        for shaped in (False, True):
+            h = x["hidden"].clone().requires_grad_(True)
+            wt = x["weight"].clone().requires_grad_(True)
+            hin = h.reshape(2, 300, 128) if shaped else h
+            tin = x["targets"].reshape(2, 300) if shaped else x["targets"]
+            loss = fused_linear_cross_entropy(hin, wt, tin, reduction=reduction)
+            if shaped and reduction == "none":
+                assert loss.shape == (2, 300)
+            loss.sum().backward()
+            outs.append((loss.detach().reshape(-1).cpu(), h.grad.cpu(), wt.grad.cpu()))
+        for u, v in zip(*outs):
+            assert torch.equal(u, v)
+    outs = []
+    for shaped in (False, True):
+        h = x["hidden"].clone().requires_grad_(True)
+        hin = h.reshape(2, 300, 128) if shaped else h
+        qin = q.reshape(2, 300, 1000) if shaped else q
+        lab = x["targets"].reshape(2, 300) if shaped else x["targets"]
+        loss = fused_linear_kl_div(hin, x["weight"], qin, lab, reduction="none")
+        loss.sum().backward()
+        outs.append((loss.detach().reshape(-1).cpu(), h.grad.cpu()))
+    for u, v in zip(*outs):
+        assert torch.equal(u, v)
