@@ -114,8 +114,8 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
     """Forward of the loss in fp64.
 
     Returns per-row ``loss``, ``lse``, ``argmax``, ``entropy``,
-    ``target_logit``, ``top2_gap`` (gap between the two largest logits) and
-    ``correct`` for the selected rows (all rows when ``rows`` is None), and,
+    ``target_logit``, ``max_logit``, ``top2_gap`` (gap between the two largest
+    logits) and ``correct`` for the selected rows (all rows when ``rows`` is None), and,
     when all rows are computed, the reduced ``loss_out``,
     ``mean_token_accuracy`` and ``entropy_mean``. ``n_valid`` and
     ``target_error`` (a target out of range that is not ignore_index) are
@@ -134,7 +134,7 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
     idx = torch.arange(n) if rows is None else torch.as_tensor(list(rows), dtype=torch.int64)
     k = idx.numel()
     out = {name: torch.empty(k, dtype=_F64) for name in
-           ("loss", "lse", "entropy", "target_logit", "top2_gap")}
+           ("loss", "lse", "entropy", "target_logit", "max_logit", "top2_gap")}
     out["argmax"] = torch.empty(k, dtype=torch.int64)
     blk = _row_block(v)
     for s in range(0, k, blk):
@@ -169,6 +169,7 @@ def forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
         out["entropy"][s:s + blk] = ent
         out["argmax"][s:s + blk] = am
         out["target_logit"][s:s + blk] = zt
+        out["max_logit"][s:s + blk] = m
         out["top2_gap"][s:s + blk] = gap
     t_sel = targets[idx]
     vm_sel = valid_mask(t_sel, ignore_index)

@@ -504,3 +504,20 @@ def test_planted_mistakes(monkeypatch, target, mutant):
     assert _pins_pass()  # the unmodified oracle passes
     monkeypatch.setattr(flce_oracle, target, mutant)
     assert not _pins_pass(), f"planted mistake {mutant.__name__} went unnoticed"
+
+
+def test_max_logit_and_gap_match_brute_force():
+    """max_logit and top2_gap, which the GPU tests use to tell decisive argmax
+    rows from near-ties, against the brute force's logits."""
+    g = torch.Generator().manual_seed(21)
+    hid = torch.randn(7, 5, generator=g, dtype=torch.float64)
+    w = torch.randn(11, 5, generator=g, dtype=torch.float64)
+    b = torch.randn(11, generator=g, dtype=torch.float64) * 0.2
+    t = torch.randint(0, 11, (7,), generator=g)
+    f = oracle.forward(hid, w, t, b, -100, 0.8, 3.0, "mean")
+    z = brute.logits(hid.tolist(), w.tolist(), b.tolist(), 0.8, 3.0)
+    for i, row in enumerate(z):
+        srt = sorted(row, reverse=True)
+        assert f["max_logit"][i].item() == pytest.approx(srt[0], rel=1e-12)
+        assert f["top2_gap"][i].item() == pytest.approx(srt[0] - srt[1], rel=1e-9, abs=1e-12)
+        assert f["target_logit"][i].item() == pytest.approx(row[int(t[i])], rel=1e-12)
