@@ -253,3 +253,30 @@ def test_kl_degenerate_shapes_and_teachers(dtype):
     assert torch.all(out["grad_hidden"][7] == 0)
     ref = kl_oracle.forward(x["hidden"], x["weight"], q, None, None, -100, 1.0, 1e-10, "none")
     assert_rows_close("loss_rows", out["loss_rows"], ref["loss"], tol["loss_rel"])
+
+
+def test_kl_grad_weight_fp32_output():
+    """grad_weight kept in fp32 (grad_weight_dtype=float32) for the KL
+    divergence: same bars as bf16 (D is still bf16), and it equals the bf16
+    output up to that output's rounding."""
+    w = _w("gw32", 300, 136, 1000, bias_var=0.02, ignore_frac=0.1)
+    x = make_inputs(w)
+    q = make_teacher_probs(w)
+    xd = to_dev(x)
+    qd, lab = q.cuda(), xd["targets"]
+    f = api.flce_kl_forward_tensors(xd["hidden"], xd["weight"], qd, lab, xd["bias"],
+                                    temperature=1.3)
+    go = torch.tensor(1.0, dtype=torch.float32, device="cuda")
+    outs = {}
+    for dt in (None, torch.float32):
+        outs[dt] = api.flce_kl_backward_tensors(xd["hidden"], xd["weight"], qd, f["lse_rows"],
+                                                f["qsum_rows"], f["n_counted"], go, lab,
+                                                xd["bias"], temperature=1.3,
+                                                grad_weight_dtype=dt)
+    torch.cuda.synchronize()
+    gw32 = outs[torch.float32][1]
+    assert gw32.dtype == torch.float32
+    assert torch.equal(gw32.to(torch.bfloat16), outs[None][1])
+    gref = kl_oracle.backward(x["hidden"], x["weight"], q, x["bias"], x["targets"], -100, 1.3,
+                              1e-10, "batchmean", 1.0)
+    assert_grad_close("grad_weight fp32", gw32.cpu(), gref["grad_weight"], TOL["bf16"])
