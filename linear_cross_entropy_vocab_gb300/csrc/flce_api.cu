@@ -968,6 +968,9 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       fp.n_rows_dyn = n_kept;
       fp.v = p->v;
       fp.n_vt = plan.n_vt;
+      // the argmax and entropy terms only when an output uses them
+      fp.metrics = (metrics_out != nullptr || correct_rows != nullptr || entropy_rows != nullptr)
+                       ? 1 : 0;
       fp.xf = xf;
       ProfScope ps("fwd_stats", s);
       e = flce::launch_tc_fwd_stats(tc_type(p), tm_h, tm_w, g, fp, dev.sms, s);

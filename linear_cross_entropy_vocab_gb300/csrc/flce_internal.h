@@ -39,6 +39,7 @@ struct FwdStatsParams {
   const int32_t* n_rows_dyn;  // rows actually present (device count) or null
   int64_t v;
   int64_t n_vt;
+  int metrics;                // 1: also the argmax and entropy terms (t); 0: (m, s) only
   LogitXform xf;
 };
 

@@ -89,8 +89,9 @@ __device__ __forceinline__ void store32(T* dst, const float (&v)[32], int nv, fl
 // chunk maximum is taken by a tree and the two sums of the chunk by four
 // interleaved partial sums, so that the dependent chains are 5 and 8 long
 // instead of 32 (the epilogue runs one warp per scheduler, so every step of
-// a chain is a stall). ARGMAX: also track the lowest index of the maximum.
-template <bool FULL, bool ARGMAX = true>
+// a chain is a stall). ARGMAX: also track the lowest index of the maximum;
+// ENTROPY: also keep t = sum e^{z-m} (z-m) (otherwise t is left as it was).
+template <bool FULL, bool ARGMAX = true, bool ENTROPY = true>
 __device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], int nv, int cb) {
   float mx[16];
 #pragma unroll
@@ -130,12 +131,14 @@ __device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], i
       f2_unpack(f2_mul(d, l2), x0, x1);
       const uint64_t e = f2_pack(ex2_approx(x0), ex2_approx(x1));
       sp[(k >> 1) & 1] = f2_add(sp[(k >> 1) & 1], e);
-      tp[(k >> 1) & 1] = f2_fma(e, d, tp[(k >> 1) & 1]);
+      if constexpr (ENTROPY) tp[(k >> 1) & 1] = f2_fma(e, d, tp[(k >> 1) & 1]);
     }
     f2_unpack(sp[0], s4[0], s4[1]);
     f2_unpack(sp[1], s4[2], s4[3]);
-    f2_unpack(tp[0], t4[0], t4[1]);
-    f2_unpack(tp[1], t4[2], t4[3]);
+    if constexpr (ENTROPY) {
+      f2_unpack(tp[0], t4[0], t4[1]);
+      f2_unpack(tp[1], t4[2], t4[3]);
+    }
   } else {
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
@@ -143,12 +146,12 @@ __device__ __forceinline__ void fold_chunk(RowStats& st, const float (&z)[32], i
         const float d = z[k] - st.m;
         const float e = ex2_approx(d * kLog2e);
         s4[k & 3] += e;
-        t4[k & 3] = fmaf(e, d, t4[k & 3]);
+        if constexpr (ENTROPY) t4[k & 3] = fmaf(e, d, t4[k & 3]);
       }
     }
   }
   st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-  st.t += (t4[0] + t4[1]) + (t4[2] + t4[3]);
+  if constexpr (ENTROPY) st.t += (t4[0] + t4[1]) + (t4[2] + t4[3]);
 }
 
 // Lane l of the warp ends with the sum over the 32 lanes of v[l].
@@ -244,7 +247,10 @@ __device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld
 }  // namespace
 
 // ------------------------------------------------------------------ forward
-template <typename T>
+// METRICS: also fold what the metrics need (the argmax and the entropy sum);
+// without them the statistics are (m, s) only, and a and t stay at their
+// initial values (the per-row correctness and entropy are then not computed).
+template <typename T, bool METRICS = true>
 struct EpiFwdStats {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = FwdStatsParams;
@@ -271,9 +277,9 @@ struct EpiFwdStats {
       load_bias32<T>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
-        fold_chunk<true>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<true, METRICS, METRICS>(st, z, nv, static_cast<int>(cb));
       } else {
-        fold_chunk<false>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<false, METRICS, METRICS>(st, z, nv, static_cast<int>(cb));
       }
       if (p.zsum != nullptr) {
 #pragma unroll
@@ -409,9 +415,9 @@ struct EpiFwdKL {
       load_bias32<T>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
-        fold_chunk<true, false>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<true, false, false>(st, z, nv, static_cast<int>(cb));
       } else {
-        fold_chunk<false, false>(st, z, nv, static_cast<int>(cb));
+        fold_chunk<false, false, false>(st, z, nv, static_cast<int>(cb));
       }
       if (row_ok) {
         float q[32];
@@ -700,11 +706,18 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
                                 const FwdStatsParams& p, int sms, cudaStream_t s) {
+  if (p.metrics) {
+    if (type == kTcF16)
+      return launch_gemm<kPairCG, false, false, EpiFwdStats<__half, true>>(tm_hidden_k,
+                                                                          tm_weight_k, g, p, sms, s);
+    return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, true>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  }
   if (type == kTcF16)
-    return launch_gemm<kPairCG, false, false, EpiFwdStats<__half>>(tm_hidden_k, tm_weight_k, g,
-                                                                    p, sms, s);
-  return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
-                                                                         g, p, sms, s);
+    return launch_gemm<kPairCG, false, false, EpiFwdStats<__half, false>>(tm_hidden_k,
+                                                                         tm_weight_k, g, p, sms, s);
+  return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, false>>(
+      tm_hidden_k, tm_weight_k, g, p, sms, s);
 }
 
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
