@@ -23,7 +23,7 @@ import torch
 
 import oracle
 from _parity import TOL, check_backward, check_forward, grad_scale, oracle_args, run_gpu, to_dev
-from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, make_inputs, peaked_rows
+from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs, peaked_rows
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -186,3 +186,25 @@ def test_peak_memory_below_logits(kl):
     nxv = w.n * w.v * 2
     assert peak < nxv, (peak, nxv)
     assert torch.isfinite(loss).item()
+
+
+def test_largest_vocabulary_sampled():
+    """A 262144-entry vocabulary (1024 vocabulary tiles per row; 8 backward
+    chunks), N=4096, H=2048, bf16, bias and softcap, 10 % ignored rows left
+    out: every row's loss and lse against the oracle, gradients on sampled
+    rows and vocabulary entries."""
+    w = Workload("v262144", 4096, 2048, 262144, "bf16", bias_var=0.02, softcap=30.0,
+                 logit_scale=0.9, ignore_frac=0.1, reduction="mean")
+    x = make_inputs(w)
+    xd = to_dev(x)
+    tol = TOL[w.dtype]
+    out = run_gpu(xd, w, grad_out=1.0, skip_ignored=True, row_metrics=True)
+    assert out["err_word"] == 0
+    ref = oracle.forward(*oracle_args(x, w))
+    check_forward(out, ref, w, tol, skipped=True)
+    rows = _sample_rows(w, x["targets"], torch.empty(0, dtype=torch.int64), k=128)
+    vocab = _sample_vocab(w, x["targets"], rows, torch.empty(0, dtype=torch.int64), k=128)
+    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab)
+    sampled = {"grad_hidden": out["grad_hidden"][rows], "grad_weight": out["grad_weight"][vocab],
+               "grad_bias": out["grad_bias"][vocab]}
+    check_backward(sampled, gref, tol, True, grad_scale(w.reduction, ref["n_valid"]))
