@@ -157,3 +157,60 @@ def test_leading_batch_dimensions_match_flattened_rows():
         outs.append((loss.detach().reshape(-1).cpu(), h.grad.cpu()))
     for u, v in zip(*outs):
         assert torch.equal(u, v)
+
+
+def test_two_threads_two_streams_match_sequential():
+    """Two host threads, each on its own CUDA stream, run forward+backward of
+    different problems (bf16 cross-entropy with bias and softcap; fp16 KL
+    divergence) at the same time. Per-thread library state (the error text,
+    the tensor-map element type) and the kernels' independence from other
+    grids must give bitwise the results of running them one after the
+    other."""
+    import threading
+
+    from linear_cross_entropy_vocab_gb300 import fused_linear_kl_div
+    from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
+
+    w1 = _w("bf16")
+    x1 = to_dev(make_inputs(w1))
+    w2 = Workload("thr_kl", 500, 256, 3000, "f16", ignore_frac=0.2)
+    x2 = to_dev(make_inputs(w2))
+    q2 = make_teacher_probs(w2).cuda()
+
+    def job1():
+        h = x1["hidden"].clone().requires_grad_(True)
+        wt = x1["weight"].clone().requires_grad_(True)
+        loss = fused_linear_cross_entropy(h, wt, x1["targets"], x1["bias"], softcap=w1.softcap,
+                                          logit_scale=w1.logit_scale)
+        loss.backward()
+        return loss.detach(), h.grad, wt.grad
+
+    def job2():
+        h = x2["hidden"].clone().requires_grad_(True)
+        wt = x2["weight"].clone().requires_grad_(True)
+        loss = fused_linear_kl_div(h, wt, q2, x2["targets"], temperature=1.7)
+        loss.backward()
+        return loss.detach(), h.grad, wt.grad
+
+    seq = [job1(), job2()]
+    torch.cuda.synchronize()
+    res, errs = [None, None], []
+
+    def run(i, fn):
+        try:
+            with torch.cuda.stream(torch.cuda.Stream()):
+                out = fn()
+                torch.cuda.current_stream().synchronize()
+            res[i] = out
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    ts = [threading.Thread(target=run, args=(0, job1)), threading.Thread(target=run, args=(1, job2))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    for a, b in zip(seq, res):
+        for u, v in zip(a, b):
+            assert torch.equal(u.cpu(), v.cpu())
