@@ -38,6 +38,10 @@ DEFAULT_WORKLOAD = "llama3_head_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_ROLES = ("fwd_stats", "fwd_kl", "bwd_dlogits", "bwd_dlogits_kl", "bwd_grad_weight",
               "bwd_grad_hidden")
+# the fp32 path's contractions run on the FP32 FMA units (ALU-bound)
+ALU_ROLES = ("fwd_stats_f32", "fwd_kl_f32", "bwd_dlogits_f32", "bwd_grad_weight_f32",
+             "bwd_grad_hidden_f32")
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 schedulers x 32)
 
 
 def strip_c_comments(src: str) -> str:
@@ -482,7 +486,10 @@ def bench_ours(args, rank, world, dev):
         # algorithmic work of one launch: the rows it computes (ignored rows
         # are left out of every contraction unless --all-rows)
         n_work = n if args.all_rows else n_valid
-        per_step_flops = 2.0 * n_work * h * v if dom in GEMM_ROLES else 0.0
+        alu = dom in ALU_ROLES
+        if alu:
+            n_work = n  # the fp32 path computes every row
+        per_step_flops = 2.0 * n_work * h * v if (dom in GEMM_ROLES or alu) else 0.0
         launches_per_step = launches / args.steps
         flops_per_launch = per_step_flops / launches_per_step
         avg_ms = tot_ms / launches
@@ -490,11 +497,21 @@ def bench_ours(args, rank, world, dev):
         # a kernel timed inside a run of a second or more runs at the power-capped
         # clock: the sustained peak; in a shorter run, the burst peak
         long_run = ms >= 1000.0
-        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+        if alu:
+            # FP32 FMA peak from unit counts and the maximum SM clock
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            mhz = peaks.get("sm_max_mhz", 2070.0)
+            peak = round(sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, 1)
+            peak_kind = (f"fp32 FMA: {sms} SMs x {FP32_LANES_PER_SM} lanes x 2 FLOP x "
+                         f"{mhz:g} MHz (unit counts and maximum clock)")
+        else:
+            peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+            peak_kind = (f"bf16 {'sustained' if long_run else 'burst'}, {peak_src} "
+                         f"(timed region {ms / 1e3:.2f} s)")
+        roofline = {"bound": "alu" if alu else "tensor", "kernel": dom,
+                    "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "peak_kind": (f"bf16 {'sustained' if long_run else 'burst'}, {peak_src} "
-                                  f"(timed region {ms / 1e3:.2f} s)"),
+                    "peak_kind": peak_kind,
                     "flops_per_launch": flops_per_launch, "rows_per_launch": n_work,
                     "avg_launch_ms": round(avg_ms, 4),
                     "traffic": measured_traffic(dom, traffic_key(w, args)),
@@ -656,7 +673,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--dtype", choices=["bf16", "f16"], default=None,
+    ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default=None,
                     help="run the workload with this input type (default: the workload's)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time flce_forward alone (the long workload uses reduction none)")
