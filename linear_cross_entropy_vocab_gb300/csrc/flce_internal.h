@@ -22,9 +22,10 @@ constexpr int kBLoadRowsTC = kBN / kPairCG;
 
 // Tile of the fp32 (FFMA) kernels: kSimtTileN rows x kSimtTileV vocabulary
 // columns; the forward statistics of the fp32 path are per kSimtTileV
-// columns (the tensor-core path's per kBN).
+// columns (the tensor-core path's per kBN), and its grad_bias partials per
+// kSimtTileN rows.
 constexpr int kSimtTileV = 128;
-constexpr int kSimtTileN = 32;
+constexpr int kSimtTileN = 128;
 
 // Input element types of the tensor-core path (FLCE_BF16, FLCE_F16).
 enum TcType { kTcBF16 = 1, kTcF16 = 2 };

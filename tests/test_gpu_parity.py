@@ -82,6 +82,44 @@ def test_parity_multi_chunk_backward(chunk):
     _check_case(w, vocab_chunk=chunk)
 
 
+@pytest.mark.parametrize("h", [37, 64])
+def test_parity_f32_multi_chunk(h):
+    """fp32 backward in six vocabulary chunks of 256, the last 219 wide (not a
+    multiple of 4), with a bias: H = 37 runs the element-wise loads, H = 64 the
+    16-byte ones with a ragged k tail in the grad_hidden contraction; N = 300
+    leaves a 44-row tail in the third 128-row tile."""
+    w = _case(f"f32_chunked_h{h}", 300, h, 1499, dtype="f32", bias_var=0.02, softcap=20.0,
+              ignore_frac=0.1)
+    _check_case(w, vocab_chunk=256)
+
+
+def _misaligned(t):
+    """A copy of `t` whose data starts 4 bytes past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
+    view = buf[1:1 + t.numel()].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 16 == 4
+    return view
+
+
+def test_parity_f32_misaligned_inputs():
+    """fp32 accepts any 4-byte-aligned hidden and weight: with both 4 bytes
+    off a 16-byte boundary (H = 64 would otherwise take the vector loads) the
+    kernels fall back to element-wise loads and give the same results."""
+    w = _case("f32_misaligned", 200, 64, 900, dtype="f32", bias_var=0.02, ignore_frac=0.1)
+    x = make_inputs(w)
+    xd = to_dev(x)
+    xd["hidden"] = _misaligned(xd["hidden"])
+    xd["weight"] = _misaligned(xd["weight"])
+    out = run_gpu(xd, w, grad_out=0.75)
+    assert out["err_word"] == 0
+    ref = oracle.forward(*oracle_args(x, w), **oracle_opts(w))
+    tol = TOL[w.dtype]
+    check_forward(out, ref, w, tol)
+    gref = oracle.backward(*oracle_args(x, w), 0.75, lse=ref["lse"], **oracle_opts(w))
+    check_backward(out, gref, tol, True, grad_scale(w.reduction, ref["n_valid"]))
+
+
 def test_parity_grad_weight_fp32():
     """grad_weight kept in fp32 (accumulated in fp32 tensor memory, stored once)."""
     w = _case("gw_f32", 384, 256, 3000, ignore_frac=0.05)
