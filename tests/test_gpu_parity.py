@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import oracle
-from _parity import (TOL, check_backward, check_forward, grad_scale, oracle_args, oracle_opts,
-                     run_gpu, to_dev)
+from _parity import (TOL, assert_grad_close, check_backward, check_forward, grad_scale,
+                     oracle_args, oracle_opts, run_gpu, to_dev)
 from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -150,6 +150,51 @@ def test_single_row_and_vocab_of_one(dtype):
     assert torch.all(out["lse_rows"] == out["lse_rows"])  # finite, no NaN
     for k in ("grad_hidden", "grad_weight", "grad_bias"):
         assert float(out[k].abs().max()) < 1e-6
+
+
+@pytest.mark.parametrize("dtype,skip", [("bf16", False), ("bf16", True), ("f16", False),
+                                        ("f32", False)])
+def test_zero_weight_uniform_softmax(dtype, skip):
+    """weight = 0 and bias = 0 make every logit 0, so the softmax is uniform:
+    lse = loss = entropy = ln V on every valid row; all V logits tie, so the
+    argmax is index 0 on every row (the lowest index wins across tiles and
+    vocabulary splits); D = g (1/V - onehot), hence grad_hidden = D W = 0
+    exactly and grad_bias_j = g (n_valid / V - #{valid rows with target j}).
+    V = 5000 spans 20 vocabulary tiles with a ragged last one."""
+    w = _case("zero_weight", 300, 64, 5000, dtype=dtype, bias_var=0.02, ignore_frac=0.1)
+    x = make_inputs(w)
+    x["weight"] = torch.zeros_like(x["weight"])
+    x["bias"] = torch.zeros_like(x["bias"])
+    t = x["targets"]
+    valid = t != w.ignore_index
+    t[((torch.arange(w.n) % 7) == 0) & valid] = 0  # some rows whose target is the argmax
+    go = 0.75
+    out = run_gpu(to_dev(x), w, grad_out=go, skip_ignored=skip)
+    assert out["err_word"] == 0
+    nv = int(valid.sum())
+    lnv = math.log(w.v)
+    assert int(out["n_valid"]) == nv
+    lse = out["lse_rows"].double()[valid]
+    assert torch.allclose(lse, torch.full_like(lse, lnv), rtol=1e-5, atol=0)
+    expect_loss = torch.where(valid, torch.tensor(lnv, dtype=torch.float64), 0.0)
+    assert torch.allclose(out["loss_rows"].double(), expect_loss, rtol=1e-5, atol=0)
+    assert abs(float(out["loss"]) - lnv) <= 1e-5 * lnv
+    hits = t[valid] == 0
+    assert torch.equal(out["correct_rows"][valid] != 0, hits)
+    assert abs(float(out["metrics"][0]) - float(hits.sum()) / nv) <= 1e-6
+    ent = out["entropy_rows"].double()[valid]
+    assert torch.allclose(ent, torch.full_like(ent, lnv), rtol=1e-4, atol=0)
+    assert abs(float(out["metrics"][1]) - lnv) <= 1e-4 * lnv
+    assert torch.count_nonzero(out["grad_hidden"]) == 0
+    g = go / nv
+    counts = torch.bincount(t[valid], minlength=w.v).double()
+    expect_gb = g * (nv / w.v - counts)
+    tol = TOL[w.dtype]
+    assert_grad_close("grad_bias (closed form)", out["grad_bias"], expect_gb, tol,
+                      grad_scale(w.reduction, nv))
+    ref = oracle.forward(*oracle_args(x, w), **oracle_opts(w))
+    gref = oracle.backward(*oracle_args(x, w), go, lse=ref["lse"], **oracle_opts(w))
+    check_backward(out, gref, tol, True, grad_scale(w.reduction, ref["n_valid"]))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
