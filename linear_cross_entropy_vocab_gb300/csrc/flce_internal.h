@@ -226,7 +226,7 @@ struct SimtDlogitsParams {
   const int32_t* n_valid;
   float* d;  // [N][ldd]
   int64_t ldd;
-  float* gb_partial;  // [ceil(N/32)][gb_ld] or null
+  float* gb_partial;  // [ceil(N / kSimtTileN)][gb_ld] or null
   int64_t gb_ld;
   int64_t n, h, v, ignore_index;
   int64_t c0, width;
