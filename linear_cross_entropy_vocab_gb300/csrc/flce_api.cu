@@ -611,7 +611,8 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
         dp.reduction = kl->reduction;
         dp.xf = xf;
         ProfScope ps("bwd_dlogits_kl", s);
-        e = flce::launch_tc_dlogits_kl(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
+        e = flce::launch_tc_dlogits_kl(type, tm_h_k, tm_w_k, g1, dp,
+                                       flce::dlogits_epi_warps(p->h), dev.sms, s);
       } else {
         flce::DlogitsParams dp{};
         dp.bias = bias;
@@ -636,7 +637,8 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
         dp.xf = xf;
         {
           ProfScope ps("bwd_dlogits", s);
-          e = flce::launch_tc_dlogits(type, tm_h_k, tm_w_k, g1, dp, dev.sms, s);
+          e = flce::launch_tc_dlogits(type, tm_h_k, tm_w_k, g1, dp,
+                                      flce::dlogits_epi_warps(p->h), dev.sms, s);
         }
       }
       if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");

@@ -139,15 +139,24 @@ cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
                              const FwdKLParams& p, int sms, cudaStream_t s);
 cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
                                  const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                                 const DlogitsKLParams& p, int sms, cudaStream_t s);
+                                 const DlogitsKLParams& p, int epi_warps, int sms,
+                                 cudaStream_t s);
 
 // `type` is a TcType; every launcher runs the CTA-pair GEMM of that type.
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
                                 const FwdStatsParams& p, int sms, cudaStream_t s);
+// epi_warps (4 or 8): epilogue warps of the dlogits GEMMs, see dlogits_epi_warps.
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
                               const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                              const DlogitsParams& p, int sms, cudaStream_t s);
+                              const DlogitsParams& p, int epi_warps, int sms, cudaStream_t s);
+
+// Epilogue warps for the dlogits GEMMs of a contraction of length h. A
+// 256 x 256 pair tile's MMAs take time in proportion to h while its epilogue
+// (softmax, D, its store and the grad_bias sums) does not; at short h two
+// warps per TMEM lane quarter keep the epilogue under the MMAs.
+constexpr int64_t kDlogitsEpi8MaxH = 2048;
+inline int dlogits_epi_warps(int64_t h) { return h <= kDlogitsEpi8MaxH ? 8 : 4; }
 cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,
                                   const CUtensorMap& tm_hidden_mn, const GemmGeom& g,
                                   const StoreRowsParams& p, int sms, cudaStream_t s);

@@ -226,15 +226,20 @@ __device__ __forceinline__ void emit_dlogits(float (&d)[32], int nv, int64_t row
 }
 
 // After the chunks of a tile: grad_bias partials of the tile's columns, the
-// sum of the four warps' column sums in a fixed order. One barrier per tile;
-// the next tile's writes to ctl->red come after the epilogue warps' next
-// common barrier (epi_all), so none overtakes these reads.
+// sum of the four lane quarters' column sums in a fixed order. With W
+// epilogue warps, warp (quarter, part) flushes chunks e * 8/W .. +8/W - 1,
+// e = 4 part + quarter. One barrier per tile; the next tile's writes to
+// ctl->red come after the epilogue warps' next common barrier (epi_all), so
+// none overtakes these reads.
+template <int W>
 __device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld, int m_tile,
                                                 int c0, int col0, int width, int quarter,
-                                                int lane, GemmCtl* ctl) {
-  named_bar_sync(1, kEpiThreads);
+                                                int part, int lane, GemmCtl* ctl) {
+  constexpr int kPer = (kBN / 32) / W;
+  named_bar_sync(1, 32 * W);
+  const int first = (4 * part + quarter) * kPer;
 #pragma unroll
-  for (int ch = 2 * quarter; ch < 2 * quarter + 2; ++ch) {  // warp q: chunks 2q, 2q+1
+  for (int ch = first; ch < first + kPer; ++ch) {
     const int col = col0 + ch * 32 + lane;
     if (col < width) {
       const float tot = ((ctl->red[0][ch][lane] + ctl->red[1][ch][lane]) + ctl->red[2][ch][lane]) +
@@ -255,7 +260,8 @@ struct EpiFwdStats {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = FwdStatsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*lane*/,
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*part*/,
+                              int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
@@ -304,13 +310,17 @@ struct EpiFwdStats {
 };
 
 // ------------------------------------------------------------------ dlogits
-template <typename T>
+// W = 8: two warps per TMEM lane quarter, one per column half of the tile
+// (for short contractions, where the epilogue would outlast the MMAs).
+template <typename T, int W = 4>
 struct EpiDlogits {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  static constexpr int kEpiWarps = W;
+  static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int quarter, int lane,
-                              GemmCtl* ctl) {
+                              bool acc_zero, int row_in_tile, int quarter, int part,
+                              int lane, GemmCtl* ctl) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
@@ -330,7 +340,7 @@ struct EpiDlogits {
     // grad_bias column partials, for tiles holding present rows (uniform per tile)
     const bool bias_sums = p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = part * kChunks; ch < (part + 1) * kChunks; ++ch) {
       const int cb = col0 + ch * 32;
       if (cb >= p.width) break;
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
@@ -377,7 +387,8 @@ struct EpiDlogits {
                       lane, ctl);
     }
     if (bias_sums)
-      flush_bias_sums(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, lane, ctl);
+      flush_bias_sums<W>(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, part,
+                         lane, ctl);
   }
 };
 
@@ -387,7 +398,8 @@ struct EpiFwdKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = FwdKLParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*lane*/,
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*part*/,
+                              int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
@@ -441,13 +453,15 @@ struct EpiFwdKL {
 
 // ------------------------------------------------------------ KL dlogits
 // D = g (p * sum_k q_k - q) * dz/dlin, with dz/dlin = 1 / temperature.
-template <typename T>
+template <typename T, int W = 4>
 struct EpiDlogitsKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  static constexpr int kEpiWarps = W;
+  static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsKLParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int quarter, int lane,
-                              GemmCtl* ctl) {
+                              bool acc_zero, int row_in_tile, int quarter, int part,
+                              int lane, GemmCtl* ctl) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
@@ -464,14 +478,17 @@ struct EpiDlogitsKL {
     const bool bias_sums = p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff;
     const bool vec = p.q_vec != 0;
     RowChunk32<T> cur, nxt;
-    cur.issue(qrow, col0, p.width - col0 < 32 ? p.width - col0 : 32, vec, row_ok);
+    const int ch_end = (part + 1) * kChunks;
+    const int c_first = col0 + part * kChunks * 32;
+    if (c_first < p.width)
+      cur.issue(qrow, c_first, p.width - c_first < 32 ? p.width - c_first : 32, vec, row_ok);
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = part * kChunks; ch < ch_end; ++ch) {
       const int cb = col0 + ch * 32;
       if (cb >= p.width) break;
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
-      const int cn = cb + 32;  // next chunk of this tile
-      if (ch + 1 < kBN / 32 && cn < p.width)
+      const int cn = cb + 32;  // next chunk of this warp
+      if (ch + 1 < ch_end && cn < p.width)
         nxt.issue(qrow, cn, p.width - cn < 32 ? p.width - cn : 32, vec, row_ok);
       float z[32], b[32], q[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
@@ -501,7 +518,8 @@ struct EpiDlogitsKL {
       cur = nxt;
     }
     if (bias_sums)
-      flush_bias_sums(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, lane, ctl);
+      flush_bias_sums<W>(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, part,
+                         lane, ctl);
   }
 };
 
@@ -511,7 +529,7 @@ struct EpiStoreRows {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = StoreRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
+                              bool acc_zero, int row_in_tile, int, int, int, GemmCtl*) {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < p.rows;
     const float scale = p.out_scale != nullptr ? *p.out_scale : 1.0f;
@@ -550,7 +568,7 @@ struct EpiAccRows {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = AccRowsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int, int, GemmCtl*) {
+                              bool acc_zero, int row_in_tile, int, int, int, GemmCtl*) {
     const int64_t n_eff = p.rows_dyn != nullptr ? *p.rows_dyn : p.rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
@@ -667,7 +685,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.blockDim = dim3(gemm_threads<Epi>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int units = sms;
@@ -722,7 +740,14 @@ cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
 
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
                               const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                              const DlogitsParams& p, int sms, cudaStream_t s) {
+                              const DlogitsParams& p, int epi_warps, int sms, cudaStream_t s) {
+  if (epi_warps == 8) {
+    if (type == kTcF16)
+      return launch_gemm<kPairCG, false, false, EpiDlogits<__half, 8>>(tm_hidden_k, tm_weight_k,
+                                                                        g, p, sms, s);
+    return launch_gemm<kPairCG, false, false, EpiDlogits<__nv_bfloat16, 8>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  }
   if (type == kTcF16)
     return launch_gemm<kPairCG, false, false, EpiDlogits<__half>>(tm_hidden_k, tm_weight_k, g, p,
                                                                    sms, s);
@@ -742,7 +767,15 @@ cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
 
 cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
                                  const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                                 const DlogitsKLParams& p, int sms, cudaStream_t s) {
+                                 const DlogitsKLParams& p, int epi_warps, int sms,
+                                 cudaStream_t s) {
+  if (epi_warps == 8) {
+    if (type == kTcF16)
+      return launch_gemm<kPairCG, false, false, EpiDlogitsKL<__half, 8>>(tm_hidden_k, tm_weight_k,
+                                                                          g, p, sms, s);
+    return launch_gemm<kPairCG, false, false, EpiDlogitsKL<__nv_bfloat16, 8>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  }
   if (type == kTcF16)
     return launch_gemm<kPairCG, false, false, EpiDlogitsKL<__half>>(tm_hidden_k, tm_weight_k, g,
                                                                      p, sms, s);

@@ -27,6 +27,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 
 #include "tc_ptx.cuh"
@@ -37,9 +38,7 @@ constexpr int kBM = 128;  // accumulator rows per CTA = TMEM lanes
 constexpr int kBN = 256;  // accumulator columns per buffer
 constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUK = 16;   // K per tcgen05.mma (kind::f16)
-constexpr int kGemmThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;  // epilogue warps unless the epilogue declares kEpiWarps = 8
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kMaxStages = 6;
 
@@ -149,6 +148,23 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
   }
 }
 
+// Epilogue warps of Epi: Epi::kEpiWarps where it declares one, else 4. With
+// 8, warps w and w + 4 share TMEM lane quarter w % 4 and split the tile's
+// columns into halves (`part` 0 and 1).
+template <class Epi, class = void>
+struct EpiWarps {
+  static constexpr int value = kEpiWarps;
+};
+template <class Epi>
+struct EpiWarps<Epi, std::void_t<decltype(Epi::kEpiWarps)>> {
+  static constexpr int value = Epi::kEpiWarps;
+};
+// Threads per CTA: the TMA warp, the MMA warp and the epilogue warps.
+template <class Epi>
+constexpr int gemm_threads() {
+  return 64 + 32 * EpiWarps<Epi>::value;
+}
+
 // Descriptor of the kk-th K=16 slice of a staged operand.
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
@@ -190,15 +206,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// AND of `ok` over the kThreads epilogue threads (named barrier 1).
+template <int kThreads>
 __device__ __forceinline__ bool epi_all(bool ok) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok))
+      : "r"(static_cast<uint32_t>(ok)), "n"(kThreads)
       : "memory");
   return r != 0;
 }
@@ -208,13 +226,15 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 //   struct Params;
 //   static __device__ void tile(const Params&, int m_block, int n_tile,
 //                               uint32_t taddr, bool acc_zero, int row_in_tile,
-//                               int quarter, int lane, GemmCtl* ctl);
+//                               int quarter, int part, int lane, GemmCtl* ctl);
+// and may declare static constexpr int kEpiWarps = 8 (see EpiWarps).
 // m_block indexes 128-row blocks of M (this CTA's rows are
 // m_block*128 + [0, 128)). `taddr` addresses this warp's 32 TMEM lanes at
 // column 0 of the tile's accumulator (read it with load_acc(..., acc_zero));
-// the 128 epilogue threads may use named barrier 1.
+// `part` is this warp's column half with 8 epilogue warps, else 0; the
+// epilogue threads may use named barrier 1.
 template <int CG, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const GemmGeom g, const typename Epi::Params ep) {
   using Cfg = TileCfg<CG>;
@@ -253,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiWarps * CG);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), EpiWarps<Epi>::value * CG);
     }
     mbar_init(smem_addr(&ctl->mma_done), 1);
     ctl->abort = 0;
@@ -384,6 +404,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // -------------------------------------------------- epilogue warps
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
+    const int part = (warp - 2) >> 2;  // column half with 8 epilogue warps, else 0
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc_empty_leader = smem_addr(&ctl->acc_empty[0]);
     if constexpr (CG == 2) acc_empty_leader = map_to_rank(acc_empty_leader, 0);
@@ -392,14 +413,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
       const bool got = wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, g.err_word);
-      if (!epi_all(got)) break;
+      if (!epi_all<32 * EpiWarps<Epi>::value>(got)) break;
       tc_fence_after_sync();
       int m, n;
       tile_coords(g, m_tiles, u, m, n);
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
       Epi::tile(ep, m * CG + static_cast<int>(rank), n, taddr, k_iters == 0, row_in_tile,
-                quarter, lane, ctl);
+                quarter, part, lane, ctl);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
