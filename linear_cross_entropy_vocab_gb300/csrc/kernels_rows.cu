@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_rows_kernel(const Merg
 }
 
 constexpr int kFinThreads = 1024;
+constexpr int kFinUnroll = 4;
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams p) {
   __shared__ double s_loss[kFinThreads];
@@ -83,12 +84,29 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   const int tid = threadIdx.x;
   double ls = 0.0, es = 0.0;
   long long nv = 0, nc = 0;
-  for (int64_t i = tid; i < p.n; i += kFinThreads) {
-    if (p.targets[i] == p.ignore_index) continue;
-    ++nv;
-    ls += static_cast<double>(p.loss_rows[i]);
-    es += static_cast<double>(p.entropy_ws[i]);
-    nc += p.correct_ws[i];
+  // Rows tid, tid + kFinThreads, ... in that order. A row's four loads do
+  // not wait for its target, and kFinUnroll rows are in flight per thread.
+  for (int64_t i0 = tid; i0 < p.n; i0 += kFinUnroll * kFinThreads) {
+    int64_t t[kFinUnroll];
+    float l[kFinUnroll], e[kFinUnroll];
+    int c[kFinUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinUnroll; ++u) {
+      const int64_t i = i0 + u * kFinThreads;
+      const bool in = i < p.n;
+      t[u] = in ? p.targets[i] : p.ignore_index;
+      l[u] = in ? p.loss_rows[i] : 0.0f;
+      e[u] = in ? p.entropy_ws[i] : 0.0f;
+      c[u] = in ? p.correct_ws[i] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kFinUnroll; ++u) {
+      if (t[u] == p.ignore_index) continue;
+      ++nv;
+      ls += static_cast<double>(l[u]);
+      es += static_cast<double>(e[u]);
+      nc += c[u];
+    }
   }
   s_loss[tid] = ls;
   s_ent[tid] = es;
@@ -163,10 +181,22 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kl_kernel(const Finalize
   const int tid = threadIdx.x;
   double ls = 0.0;
   long long nc = 0;
-  for (int64_t i = tid; i < p.n; i += kFinThreads) {
-    if (p.labels != nullptr && p.labels[i] == p.ignore_index) continue;
-    ++nc;
-    ls += static_cast<double>(p.loss_rows[i]);
+  for (int64_t i0 = tid; i0 < p.n; i0 += kFinUnroll * kFinThreads) {
+    bool counted[kFinUnroll];
+    float l[kFinUnroll];
+#pragma unroll
+    for (int u = 0; u < kFinUnroll; ++u) {
+      const int64_t i = i0 + u * kFinThreads;
+      const bool in = i < p.n;
+      counted[u] = in && (p.labels == nullptr || p.labels[i] != p.ignore_index);
+      l[u] = in ? p.loss_rows[i] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kFinUnroll; ++u) {
+      if (!counted[u]) continue;
+      ++nc;
+      ls += static_cast<double>(l[u]);
+    }
   }
   s_loss[tid] = ls;
   s_nc[tid] = nc;
@@ -282,10 +312,15 @@ __global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const Com
   __shared__ int chunk_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int carry = 0;
+  // the target of this thread's row in the next pass is loaded one pass ahead
+  int64_t t_next = tid < p.n ? p.targets[tid] : p.ignore_index;
   for (int64_t base = 0; base < p.n; base += kCompactThreads) {
     const int64_t i = base + tid;
     const bool in = i < p.n;
-    const bool keep = in && p.targets[i] != p.ignore_index;
+    const int64_t t = t_next;
+    const int64_t i_next = i + kCompactThreads;
+    t_next = i_next < p.n ? p.targets[i_next] : p.ignore_index;
+    const bool keep = in && t != p.ignore_index;
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     const int before = __popc(bal & ((1u << lane) - 1u));
     if (lane == 0) warp_off[warp] = __popc(bal);
@@ -320,12 +355,33 @@ __global__ void __launch_bounds__(kCompactThreads) compact_rows_kernel(const Com
   if (tid == 0) *p.n_kept = carry;
 }
 
-constexpr int kGatherThreads = 128;
+constexpr int kGatherThreads = 256;  // 8 warps: one row per warp
+constexpr int kRowsPerBlock = kGatherThreads / 32;
+constexpr int kCopyUnroll = 4;  // 16-byte loads in flight per lane
+
+// dst[q] = src[q] (or 0 when src is null) for q < vecs, by one warp.
+__device__ __forceinline__ void copy_row(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                         int64_t vecs, int lane) {
+  for (int64_t q0 = lane; q0 < vecs; q0 += 32 * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t q = q0 + 32 * u;
+      v[u] = (src != nullptr && q < vecs) ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t q = q0 + 32 * u;
+      if (q < vecs) dst[q] = v[u];
+    }
+  }
+}
 
 // Compacted row j <- original row row_map[j]; rows [n_kept, pad) are zero so
 // that a contraction over rows reads zeros past the last kept row.
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherParams p) {
-  const int64_t j = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
   const int64_t kept = *p.n_kept;
   const int64_t pad = (kept + p.pad_rows - 1) / p.pad_rows * p.pad_rows;
   if (j >= pad || j >= p.n) return;
@@ -333,17 +389,16 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
   uint4* dst = reinterpret_cast<uint4*>(p.hidden_c) + j * vecs;
   if (j < kept) {
     const int64_t src_row = p.row_map[j];
-    const uint4* src = reinterpret_cast<const uint4*>(p.hidden) + src_row * vecs;
-    for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = __ldg(src + q);
-    if (threadIdx.x == 0) {
+    copy_row(dst, reinterpret_cast<const uint4*>(p.hidden) + src_row * vecs, vecs, lane);
+    if (lane == 0) {
       p.targets_c[j] = p.targets[src_row];
       if (p.lse_c) p.lse_c[j] = p.lse[src_row];
       if (p.grad_rows_c) p.grad_rows_c[j] = p.grad_rows[src_row];
       if (p.qsum_c) p.qsum_c[j] = p.qsum[src_row];
     }
   } else {
-    for (int64_t q = threadIdx.x; q < vecs; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x == 0) {
+    copy_row(dst, nullptr, vecs, lane);
+    if (lane == 0) {
       p.targets_c[j] = p.ignore_index;
       if (p.lse_c) p.lse_c[j] = 0.0f;
       if (p.grad_rows_c) p.grad_rows_c[j] = 0.0f;
@@ -353,12 +408,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
 }
 
 __global__ void __launch_bounds__(kGatherThreads)
-    zero_ignored_rows_kernel(const int64_t* __restrict__ targets, int64_t ignore_index,
+    zero_ignored_rows_kernel(const int64_t* __restrict__ targets, int64_t n, int64_t ignore_index,
                              void* out, int64_t h) {
-  const int64_t i = blockIdx.x;
-  if (targets[i] != ignore_index) return;
-  uint4* dst = reinterpret_cast<uint4*>(out) + i * (h / 8);
-  for (int64_t q = threadIdx.x; q < h / 8; q += kGatherThreads) dst[q] = make_uint4(0, 0, 0, 0);
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+  if (i >= n || targets[i] != ignore_index) return;
+  copy_row(reinterpret_cast<uint4*>(out) + i * (h / 8), nullptr, h / 8, threadIdx.x & 31);
 }
 
 }  // namespace
@@ -370,7 +424,8 @@ cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t s) {
 
 cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s) {
   if (p.n == 0) return cudaSuccess;
-  gather_rows_kernel<<<static_cast<unsigned>(p.n), kGatherThreads, 0, s>>>(p);
+  const unsigned grid = static_cast<unsigned>((p.n + kRowsPerBlock - 1) / kRowsPerBlock);
+  gather_rows_kernel<<<grid, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -399,8 +454,8 @@ cudaError_t launch_finalize_kl(const FinalizeKLParams& p, cudaStream_t s) {
 cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,
                                      void* out, int64_t h, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  zero_ignored_rows_kernel<<<static_cast<unsigned>(n), kGatherThreads, 0, s>>>(targets,
-                                                                                ignore_index, out, h);
+  const unsigned grid = static_cast<unsigned>((n + kRowsPerBlock - 1) / kRowsPerBlock);
+  zero_ignored_rows_kernel<<<grid, kGatherThreads, 0, s>>>(targets, n, ignore_index, out, h);
   return cudaGetLastError();
 }
 
