@@ -17,6 +17,8 @@
 //   warps 2-5  the epilogue: each thread owns one accumulator row (TMEM
 //            lane), pulls its 256 fp32 columns with tcgen05.ld and hands them
 //            to the epilogue policy.
+// An epilogue may ask for 8 warps (320 threads): warps 2-9, two per TMEM lane
+// quarter, each pulling one 128-column half of its rows.
 // The 512 TMEM columns hold two 128 x 256 fp32 accumulators per CTA, so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 //
