@@ -48,6 +48,12 @@ CASES = [
     (_w("f32_bias_bm", 100, 50, 777, "f32", bias_var=0.02, ignore_frac=0.1), 2.0, "batchmean",
      True, None, 0, False),
     (_w("f32_none", 257, 96, 2100, "f32"), 1.0, "none", False, 30, 512, False),
+    # last vocabulary chunk 100 columns wide: with H <= 2048 the dlogits GEMM runs two
+    # epilogue warps per lane quarter, and those of the second column half get no columns
+    (_w("narrow_last_chunk_bias", 700, 192, 868, bias_var=0.02, ignore_frac=0.1), 1.3,
+     "batchmean", True, None, 256, True),
+    (_w("f16_narrow_last_chunk", 300, 128, 868, "f16", bias_var=0.02), 0.8, "sum", False,
+     None, 256, False),
 ]
 
 

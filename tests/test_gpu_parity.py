@@ -82,6 +82,17 @@ def test_parity_multi_chunk_backward(chunk):
     _check_case(w, vocab_chunk=chunk)
 
 
+@pytest.mark.parametrize("dtype,skip", [("bf16", False), ("bf16", True), ("f16", False)])
+def test_parity_narrow_last_chunk(dtype, skip):
+    """V = 868 in vocabulary chunks of 256: the last chunk is 100 columns wide. At
+    H <= 2048 the dlogits GEMM runs two epilogue warps per TMEM lane quarter, one
+    per 128-column half of a tile; in the last chunk the second-half warps get no
+    column but still take part in the grad_bias flush and the tile barriers."""
+    w = _case("narrow_last_chunk", 700, 192, 868, dtype=dtype, bias_var=0.02, softcap=15.0,
+              ignore_frac=0.1)
+    _check_case(w, vocab_chunk=256, skip_ignored=skip)
+
+
 @pytest.mark.parametrize("h", [37, 64])
 def test_parity_f32_multi_chunk(h):
     """fp32 backward in six vocabulary chunks of 256, the last 219 wide (not a
