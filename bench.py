@@ -484,40 +484,16 @@ def bench_ours(args, rank, world, dev):
     if dom is not None:
         launches, tot_ms = roles[dom]
         # algorithmic work of one launch: the rows it computes (ignored rows
-        # are left out of every contraction unless --all-rows)
-        n_work = n if args.all_rows else n_valid
-        alu = dom in ALU_ROLES
-        if alu:
-            n_work = n  # the fp32 path computes every row
-        per_step_flops = 2.0 * n_work * h * v if (dom in GEMM_ROLES or alu) else 0.0
-        launches_per_step = launches / args.steps
-        flops_per_launch = per_step_flops / launches_per_step
-        avg_ms = tot_ms / launches
-        achieved = flops_per_launch / (avg_ms / 1e3) / 1e12
-        # a kernel timed inside a run of a second or more runs at the power-capped
-        # clock: the sustained peak; in a shorter run, the burst peak
-        long_run = ms >= 1000.0
-        if alu:
-            # FP32 FMA peak from unit counts and the maximum SM clock
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            mhz = peaks.get("sm_max_mhz", 2070.0)
-            peak = round(sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, 1)
-            peak_kind = (f"fp32 FMA: {sms} SMs x {FP32_LANES_PER_SM} lanes x 2 FLOP x "
-                         f"{mhz:g} MHz (unit counts and maximum clock)")
-        else:
-            peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
-            peak_kind = (f"bf16 {'sustained' if long_run else 'burst'}, {peak_src} "
-                         f"(timed region {ms / 1e3:.2f} s)")
-        roofline = {"bound": "alu" if alu else "tensor", "kernel": dom,
-                    "achieved": round(achieved, 1),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "peak_kind": peak_kind,
-                    "flops_per_launch": flops_per_launch, "rows_per_launch": n_work,
-                    "avg_launch_ms": round(avg_ms, 4),
-                    "traffic": measured_traffic(dom, traffic_key(w, args)),
-                    "traffic_source": "profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
+        # are left out of every contraction unless --all-rows; the fp32 path
+        # computes every row)
+        n_work = n if (args.all_rows or dom in ALU_ROLES) else n_valid
+        roofline = roofline_entry(dom, launches, tot_ms, args.steps, n_work, h, v, ms, peaks,
+                                  peak_src,
+                                  torch.cuda.get_device_properties(dev).multi_processor_count)
+        roofline["traffic"] = measured_traffic(dom, traffic_key(w, args))
+        roofline["traffic_source"] = ("profiles/dram_traffic.json (ncu dram__bytes_read.sum + "
                                       "dram__bytes_write.sum per launch; null if the kernels "
-                                      "changed since)"}
+                                      "changed since)")
     kernels = {k: {"launches": val[0], "ms_per_step": round(val[1] / args.steps, 4),
                    "share": round(val[1] / sum(u[1] for u in roles.values()), 4)}
                for k, val in roles.items()}
@@ -664,6 +640,39 @@ def bench_reference(args):
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
+
+
+def roofline_entry(dom, launches, tot_ms, steps, n_work, h, v, run_ms, peaks, peak_src, sms):
+    """The `roofline` object of the dominant kernel `dom`, which ran `launches`
+    times in `tot_ms` over `steps` timed steps of a `run_ms` timed region.
+
+    achieved = the launch's algorithmic flops (2 n_work h v per step, split
+    over its launches per step) / its average duration. A kernel timed inside
+    a region of a second or more runs at the power-capped clock, so it is set
+    against the sustained bf16 peak, a shorter one against the burst peak; the
+    fp32 (FFMA) roles against sms x 128 FP32 lanes x 2 flops x the maximum SM
+    clock."""
+    alu = dom in ALU_ROLES
+    per_step_flops = 2.0 * n_work * h * v if (dom in GEMM_ROLES or alu) else 0.0
+    flops_per_launch = per_step_flops / (launches / steps)
+    avg_ms = tot_ms / launches
+    achieved = flops_per_launch / (avg_ms / 1e3) / 1e12
+    if alu:
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak = round(sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, 1)
+        peak_kind = (f"fp32 FMA: {sms} SMs x {FP32_LANES_PER_SM} lanes x 2 FLOP x "
+                     f"{mhz:g} MHz (unit counts and maximum clock)")
+    else:
+        long_run = run_ms >= 1000.0
+        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+        peak_kind = (f"bf16 {'sustained' if long_run else 'burst'}, {peak_src} "
+                     f"(timed region {run_ms / 1e3:.2f} s)")
+    return {"bound": "alu" if alu else "tensor", "kernel": dom,
+            "achieved": round(achieved, 1),
+            "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "peak_kind": peak_kind,
+            "flops_per_launch": flops_per_launch, "rows_per_launch": n_work,
+            "avg_launch_ms": round(avg_ms, 4)}
 
 def main():
     ap = argparse.ArgumentParser()

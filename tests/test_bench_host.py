@@ -1,6 +1,7 @@
 """Host-side helpers of bench.py, without a GPU: the comment stripping behind
 the kernel-source hash that ties profiles/dram_traffic.json to the kernels
-it was measured on, and the traffic lookup."""
+it was measured on, the traffic lookup, and the roofline entry of the
+dominant kernel (its achieved flops and the peak it is set against)."""
 import importlib.util
 import json
 import os
@@ -45,3 +46,49 @@ def test_traffic_lookup_follows_the_hash(tmp_path, monkeypatch):
     (csrc / "k.cu").write_text("__global__ void k() { return; }\n")
     assert b.measured_traffic("fwd_stats", "w") is None
     assert b.measured_traffic("fwd_stats", "other") is None
+
+
+PEAKS = {"bf16_tflops": 1856.7, "bf16_tflops_sustained": 1661.6, "sm_max_mhz": 2070.0}
+
+
+def test_roofline_tensor_peak_follows_the_timed_region():
+    """A GEMM role is set against the sustained bf16 peak when the timed region
+    lasts a second or more, else against the burst peak; achieved is the
+    launch's 2 n h v flops (split over its launches per step) over its average
+    duration."""
+    b = _bench()
+    n, h, v, steps = 8028, 4096, 128256, 60
+    # 4 dlogits launches per step, 1.267 ms each
+    long = b.roofline_entry("bwd_dlogits", 4 * steps, 4 * steps * 1.267, steps, n, h, v,
+                            1200.0, PEAKS, "measured", 152)
+    per_launch = 2.0 * n * h * v / 4
+    assert long["flops_per_launch"] == per_launch
+    assert abs(long["achieved"] - per_launch / 1.267e-3 / 1e12) < 0.1
+    assert long["bound"] == "tensor" and long["peak"] == 1661.6
+    assert "sustained" in long["peak_kind"]
+    assert abs(long["frac"] - long["achieved"] / 1661.6) < 1e-3
+    short = b.roofline_entry("bwd_dlogits", 4 * steps, 4 * steps * 1.267, steps, n, h, v,
+                             999.0, PEAKS, "measured", 152)
+    assert short["peak"] == 1856.7 and "burst" in short["peak_kind"]
+    assert short["achieved"] == long["achieved"]
+
+
+def test_roofline_fp32_roles_use_the_fma_peak():
+    """The fp32 (FFMA) roles are ALU-bound: the peak is SMs x 128 lanes x 2 flops
+    x the maximum SM clock, whatever the length of the timed region."""
+    b = _bench()
+    r = b.roofline_entry("bwd_grad_hidden_f32", 3, 3 * 10.8, 3, 4096, 2048, 32000, 120.0,
+                         PEAKS, "measured", 152)
+    assert r["bound"] == "alu"
+    assert r["peak"] == round(152 * 128 * 2 * 2070e6 / 1e12, 1) == 80.5
+    assert abs(r["achieved"] - 2.0 * 4096 * 2048 * 32000 / 10.8e-3 / 1e12) < 0.1
+    r2 = b.roofline_entry("bwd_grad_hidden_f32", 3, 3 * 10.8, 3, 4096, 2048, 32000, 5000.0,
+                          PEAKS, "measured", 152)
+    assert r2["peak"] == r["peak"]
+
+
+def test_roofline_non_gemm_role_has_no_flops():
+    b = _bench()
+    r = b.roofline_entry("merge_rows", 60, 1.2, 60, 8192, 4096, 128256, 1200.0, PEAKS,
+                         "measured", 152)
+    assert r["flops_per_launch"] == 0.0 and r["achieved"] == 0.0
