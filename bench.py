@@ -230,7 +230,8 @@ def job_tokens_per_s(tokens_per_rank: int, steps: int, world: int, max_ms: float
 class Step:
     """Preallocated buffers and the two C-ABI calls of one fwd+bwd step."""
 
-    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False):
+    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False,
+                 vocab_chunk: int = 0):
         from linear_cross_entropy_vocab_gb300 import abi
 
         self.abi = abi
@@ -243,7 +244,7 @@ class Step:
                 torch.float32: abi.FLCE_F32}[x["hidden"].dtype]
         self.prob = abi.make_problem(n, h, v, code, x["bias"] is not None, w.ignore_index,
                                      w.logit_scale, w.softcap, w.reduction,
-                                     skip_ignored=skip_ignored,
+                                     vocab_chunk=vocab_chunk, skip_ignored=skip_ignored,
                                      label_smoothing=w.label_smoothing, z_loss=w.z_loss)
         f32 = dict(dtype=torch.float32, device=dev)
         self.loss_rows = torch.empty(n, **f32)
@@ -286,7 +287,8 @@ class KLStep:
     """Preallocated buffers and the two C-ABI calls of one fused linear KL
     fwd+bwd step."""
 
-    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False):
+    def __init__(self, x: dict, w, dev, skip_ignored: bool = True, forward_only: bool = False,
+                 vocab_chunk: int = 0):
         from linear_cross_entropy_vocab_gb300 import abi
 
         self.abi = abi
@@ -299,7 +301,7 @@ class KLStep:
                 torch.float32: abi.FLCE_F32}[x["hidden"].dtype]
         self.prob = abi.make_kl_problem(n, h, v, code, x["bias"] is not None, w.ignore_index,
                                         KL_TEMPERATURE, 1e-10, KL_REDUCTION,
-                                        skip_ignored=skip_ignored)
+                                        vocab_chunk=vocab_chunk, skip_ignored=skip_ignored)
         f32 = dict(dtype=torch.float32, device=dev)
         self.loss_rows = torch.empty(n, **f32)
         self.lse_rows = torch.empty(n, **f32)
@@ -342,7 +344,8 @@ def bench_ours(args, rank, world, dev):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     step = (KLStep if args.kl else Step)(x, w, dev, skip_ignored=not args.all_rows,
-                                         forward_only=args.forward_only)
+                                         forward_only=args.forward_only,
+                                         vocab_chunk=args.vocab_chunk)
     n, h, v = w.n, w.h, w.v
 
     def barrier():
@@ -464,9 +467,11 @@ def bench_ours(args, rank, world, dev):
     ww = x["weight"].detach().requires_grad_(True)
     if args.kl:
         loss = api.fused_linear_kl_div(hh, ww, x["q"], x["targets"],
-                                       temperature=KL_TEMPERATURE, reduction=KL_REDUCTION)
+                                       temperature=KL_TEMPERATURE, reduction=KL_REDUCTION,
+                                       vocab_chunk=args.vocab_chunk)
     else:
-        loss, _m = api.fused_linear_cross_entropy(hh, ww, x["targets"], return_metrics=True)
+        loss, _m = api.fused_linear_cross_entropy(hh, ww, x["targets"], return_metrics=True,
+                                                  vocab_chunk=args.vocab_chunk)
     loss.backward()
     torch.cuda.synchronize(dev)
     peak_incr = torch.cuda.max_memory_allocated(dev) - base
@@ -515,6 +520,7 @@ def bench_ours(args, rank, world, dev):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weight 1.05 GB), no flush",
                    "skip_ignored_rows": not args.all_rows,
+                   "vocab_chunk": args.vocab_chunk or "library default",
                    "step": "forward only" if args.forward_only else "forward+backward"},
         "tensor_peak_frac": {
             "achieved_tflops": round(achieved_step, 1),
@@ -686,6 +692,9 @@ def main():
                     help="run the workload with this input type (default: the workload's)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time flce_forward alone (the long workload uses reduction none)")
+    ap.add_argument("--vocab-chunk", type=int, default=0,
+                    help="vocabulary columns of the backward's dlogits buffer (0: the library's "
+                         "default)")
     ap.add_argument("--label-smoothing", type=float, default=0.0)
     ap.add_argument("--z-loss", type=float, default=0.0)
     ap.add_argument("--all-rows", action="store_true",

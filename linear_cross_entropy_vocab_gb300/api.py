@@ -142,13 +142,14 @@ def flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid, grad_out, 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, ignore_index, logit_scale, softcap,
-                reduction, return_metrics, label_smoothing, z_loss):
+                reduction, return_metrics, label_smoothing, z_loss, vocab_chunk):
         # ignored rows contribute nothing, so they are left out of the GEMMs
         out = flce_forward_tensors(hidden, weight, targets, bias, ignore_index, logit_scale,
                                    softcap, reduction, return_metrics, skip_ignored=True,
                                    label_smoothing=label_smoothing, z_loss=z_loss)
         ctx.save_for_backward(hidden, weight, bias, targets, out["lse_rows"], out["n_valid"])
-        ctx.opts = (ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss)
+        ctx.opts = (ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss,
+                    vocab_chunk)
         metrics = out["metrics"]
         if metrics is None:
             metrics = torch.empty(0, dtype=torch.float32, device=hidden.device)
@@ -158,15 +159,17 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_loss, _grad_metrics):
         hidden, weight, bias, targets, lse_rows, n_valid = ctx.saved_tensors
-        ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss = ctx.opts
+        (ignore_index, logit_scale, softcap, reduction, label_smoothing, z_loss,
+         vocab_chunk) = ctx.opts
         gh, gw, gb = flce_backward_tensors(hidden, weight, targets, lse_rows, n_valid,
                                            grad_loss, bias, ignore_index, logit_scale,
                                            softcap, reduction, skip_ignored=True,
-                                           label_smoothing=label_smoothing, z_loss=z_loss)
+                                           label_smoothing=label_smoothing, z_loss=z_loss,
+                                           vocab_chunk=vocab_chunk)
         need = ctx.needs_input_grad
         return (gh if need[0] else None, gw if need[1] else None,
                 gb if (bias is not None and need[2]) else None,
-                None, None, None, None, None, None, None, None)
+                None, None, None, None, None, None, None, None, None)
 
 
 def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
@@ -174,7 +177,8 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
                                ignore_index: int = -100, logit_scale: float = 1.0,
                                softcap: Optional[float] = None, reduction: str = "mean",
                                return_metrics: bool = False, *,
-                               label_smoothing: float = 0.0, z_loss: float = 0.0):
+                               label_smoothing: float = 0.0, z_loss: float = 0.0,
+                               vocab_chunk: int = 0):
     """Cross-entropy of softcap(logit_scale * (hidden @ weight.T + bias))
     against targets, without materialising the (N, V) logits. hidden may
     carry leading batch dimensions ([..., H] with targets [...]); its rows
@@ -186,6 +190,10 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
 
     Keyword-only extras: ``label_smoothing`` eps (cross-entropy against
     (1-eps)*onehot + eps/V) and ``z_loss`` lam (adds lam * lse^2 per row).
+    ``vocab_chunk`` bounds the vocabulary columns of the backward's dlogits
+    buffer (rounded up to a multiple of 256); 0 takes the library's default
+    (a 512 MiB buffer, or the whole vocabulary when that is smaller). A
+    smaller chunk lowers peak memory at some cost in speed.
     """
     if reduction not in abi.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(abi.REDUCTIONS)}")
@@ -202,7 +210,8 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
     loss, metrics = _FusedLinearCrossEntropy.apply(hidden, weight, bias, targets,
                                                    int(ignore_index), float(logit_scale),
                                                    softcap, reduction, bool(return_metrics),
-                                                   float(label_smoothing), float(z_loss))
+                                                   float(label_smoothing), float(z_loss),
+                                                   int(vocab_chunk))
     if reduction == "none":
         loss = loss.reshape(batch_shape)
     if not return_metrics:
@@ -300,39 +309,41 @@ def flce_kl_backward_tensors(hidden, weight, target_probs, lse_rows, qsum_rows, 
 class _FusedLinearKLDiv(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, bias, target_probs, labels, ignore_index, temperature, eps,
-                reduction):
+                reduction, vocab_chunk):
         out = flce_kl_forward_tensors(hidden, weight, target_probs, labels, bias, ignore_index,
                                       temperature, eps, reduction, skip_ignored=True)
         ctx.save_for_backward(hidden, weight, bias, target_probs, labels, out["lse_rows"],
                               out["qsum_rows"], out["n_counted"])
-        ctx.opts = (ignore_index, temperature, eps, reduction)
+        ctx.opts = (ignore_index, temperature, eps, reduction, vocab_chunk)
         return out["loss"]
 
     @staticmethod
     def backward(ctx, grad_loss):
         hidden, weight, bias, target_probs, labels, lse_rows, qsum_rows, n_counted = \
             ctx.saved_tensors
-        ignore_index, temperature, eps, reduction = ctx.opts
+        ignore_index, temperature, eps, reduction, vocab_chunk = ctx.opts
         gh, gw, gb = flce_kl_backward_tensors(hidden, weight, target_probs, lse_rows, qsum_rows,
                                               n_counted, grad_loss, labels, bias, ignore_index,
-                                              temperature, eps, reduction, skip_ignored=True)
+                                              temperature, eps, reduction, skip_ignored=True,
+                                              vocab_chunk=vocab_chunk)
         need = ctx.needs_input_grad
         return (gh if need[0] else None, gw if need[1] else None,
                 gb if (bias is not None and need[2]) else None,
-                None, None, None, None, None, None)
+                None, None, None, None, None, None, None)
 
 
 def fused_linear_kl_div(hidden: torch.Tensor, weight: torch.Tensor,
                         target_probs: torch.Tensor, labels: Optional[torch.Tensor] = None,
                         bias: Optional[torch.Tensor] = None, ignore_index: int = -100,
                         temperature: float = 1.0, eps: float = 1e-10,
-                        reduction: str = "batchmean"):
+                        reduction: str = "batchmean", *, vocab_chunk: int = 0):
     """KL(target || softmax((hidden @ weight.T + bias) / temperature)) per row,
     reduced like torch.nn.KLDivLoss ('batchmean', 'mean', 'sum', 'none'),
     without materialising the (N, V) logits. hidden [..., H] may carry
     leading batch dimensions, matched by target_probs [..., V] and labels. Rows whose label equals
     ignore_index are left out (labels None: every row counts). The teacher
-    probabilities get no gradient."""
+    probabilities get no gradient. ``vocab_chunk`` bounds the backward's
+    dlogits buffer as in fused_linear_cross_entropy."""
     if reduction not in abi.KL_REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(abi.KL_REDUCTIONS)}")
     batch_shape = hidden.shape[:-1]
@@ -350,5 +361,6 @@ def fused_linear_kl_div(hidden: torch.Tensor, weight: torch.Tensor,
     labels = None if labels is None else labels.contiguous()
     bias = None if bias is None else bias.contiguous()
     loss = _FusedLinearKLDiv.apply(hidden, weight, bias, target_probs, labels,
-                                   int(ignore_index), float(temperature), float(eps), reduction)
+                                   int(ignore_index), float(temperature), float(eps), reduction,
+                                   int(vocab_chunk))
     return loss.reshape(batch_shape) if reduction == "none" else loss

@@ -58,17 +58,20 @@ def test_metrics_leave_loss_and_grads_bit_identical(dtype):
         assert torch.equal(u, v)
 
 
-def test_autograd_matches_raw_calls():
+@pytest.mark.parametrize("vocab_chunk", [0, 512])
+def test_autograd_matches_raw_calls(vocab_chunk):
     """The autograd entry point leaves ignored rows out of the GEMMs; it equals
-    the raw calls made with the same flag."""
+    the raw calls made with the same flag, and passes its vocab_chunk to the
+    backward (512: seven chunks, bitwise the raw calls with that chunk)."""
     w = _w("bf16", reduction="sum")
     x = to_dev(make_inputs(w))
-    raw = run_gpu(x, w, grad_out=1.0, skip_ignored=True)
+    raw = run_gpu(x, w, grad_out=1.0, skip_ignored=True, vocab_chunk=vocab_chunk)
     h = x["hidden"].clone().requires_grad_(True)
     wt = x["weight"].clone().requires_grad_(True)
     b = x["bias"].clone().requires_grad_(True)
     loss = fused_linear_cross_entropy(h, wt, x["targets"], b, softcap=w.softcap,
-                                      logit_scale=w.logit_scale, reduction="sum")
+                                      logit_scale=w.logit_scale, reduction="sum",
+                                      vocab_chunk=vocab_chunk)
     loss.backward()
     assert torch.equal(loss.detach().cpu(), raw["loss"])
     assert torch.equal(h.grad.cpu(), raw["grad_hidden"])

@@ -207,6 +207,15 @@ def test_kl_autograd_matches_raw_calls_and_repeats_bitwise():
     assert torch.equal(h.grad.cpu(), raw["grad_hidden"])
     assert torch.equal(wt.grad.cpu(), raw["grad_weight"])
     assert torch.equal(b.grad.cpu(), raw["grad_bias"])
+    # vocab_chunk reaches the backward: 1024 gives five chunks, bitwise the raw calls
+    raw_c = run_kl_gpu(xd, q, xd["targets"], w, 1.3, "batchmean", 1.0, vocab_chunk=1024,
+                       skip_ignored=True)
+    for t in (h, wt, b):
+        t.grad = None
+    loss = fused_linear_kl_div(h, wt, q, xd["targets"], b, temperature=1.3, vocab_chunk=1024)
+    loss.backward()
+    assert torch.equal(h.grad.cpu(), raw_c["grad_hidden"])
+    assert torch.equal(wt.grad.cpu(), raw_c["grad_weight"])
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
