@@ -93,9 +93,12 @@ typedef enum flce_reduction {
  *   softcap            > 0 enables z = softcap*tanh(u/softcap); <= 0 disables
  *   reduction          flce_reduction
  *   grad_weight_dtype  dtype of grad_weight: FLCE_F32, or equal to dtype
- *   vocab_chunk        backward vocabulary chunk width; 0 picks the default
- *                      (the chunk's N x chunk dlogits buffer is the largest
- *                      workspace item); rounded up to a multiple of 256
+ *   vocab_chunk        backward vocabulary chunk width; 0 picks the default:
+ *                      the widest chunk whose N x chunk dlogits buffer fits
+ *                      in 512 MiB, at most the whole vocabulary. The buffer
+ *                      is the largest workspace item, so a smaller chunk
+ *                      lowers peak memory at some cost in speed. Rounded up
+ *                      to a multiple of 256
  *   flags              OR of FLCE_SKIP_IGNORED_ROWS; 0 for none
  *   label_smoothing    eps in [0, 1]: cross-entropy against the target
  *                      distribution (1-eps)*onehot + eps/V, i.e.
