@@ -245,6 +245,12 @@ def _dlogits(z: torch.Tensor, u: torch.Tensor, lse: torch.Tensor,
     return d
 
 
+def _abs_terms(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """|a| @ |b|: entry (i, k) is the sum of the absolute values of the terms
+    a_ij b_jk that make up (a @ b)_ik."""
+    return a.abs() @ b.abs()
+
+
 def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
              bias: Optional[torch.Tensor] = None, ignore_index: int = -100,
              logit_scale: float = 1.0, softcap: Optional[float] = None,
@@ -253,7 +259,8 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
              rows: Optional[Sequence[int]] = None,
              vocab_rows: Optional[Sequence[int]] = None,
              want_hidden: bool = True, want_weight: bool = True,
-             label_smoothing: float = 0.0, z_loss: float = 0.0) -> dict:
+             label_smoothing: float = 0.0, z_loss: float = 0.0,
+             magnitudes: bool = False) -> dict:
     """Gradients of the loss in fp64 (§Algorithm: grad_hidden = (p - onehot)
     @ weight, grad_weight = (p - onehot).T @ hidden; bias gets the column
     sums), with the chain factor of logit_scale and softcap.
@@ -262,6 +269,15 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
     grad_weight and grad_bias to those vocabulary rows. ``lse`` (fp64 [N]) may
     be passed from :func:`forward` to avoid recomputing it; grad_weight needs
     the lse of every row.
+
+    ``magnitudes`` also returns, for every gradient entry, the sum of the
+    absolute values of the terms it adds up (``*_mag``):
+    ``sum_j |D_ij| |W_jk|`` for grad_hidden, ``sum_i |D_ij| |h_ik|`` for
+    grad_weight and ``sum_i |D_ij|`` for grad_bias, with D = d loss / d lin as
+    above. Perturbing every D_ij by at most a fraction u of itself moves the
+    entry by at most u times this sum, so it is the scale against which an
+    implementation that rounds D (or accumulates the terms in finite
+    precision) is judged. Test infrastructure; it does not enter the gradients.
     """
     n, _ = hidden.shape
     v = weight.shape[0]
@@ -274,6 +290,7 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
         idx = torch.arange(n) if rows is None else torch.as_tensor(list(rows), dtype=torch.int64)
         w64 = weight
         gh = torch.empty(idx.numel(), hidden.shape[1], dtype=_F64)
+        gh_mag = torch.empty_like(gh) if magnitudes else None
         blk = _row_block(v)
         for s in range(0, idx.numel(), blk):
             ri = idx[s:s + blk]
@@ -288,8 +305,12 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
             d = _dlogits(z, u, lse_b, pos, g_all[ri], logit_scale, softcap,
                          label_smoothing, z_loss, v)
             gh[s:s + blk] = d @ w64
+            if magnitudes:
+                gh_mag[s:s + blk] = _abs_terms(d, w64)
         out["grad_hidden"] = gh
         out["rows"] = idx
+        if magnitudes:
+            out["grad_hidden_mag"] = gh_mag
     if want_weight:
         if lse is None:
             lse = forward(hidden, weight, targets, bias, ignore_index,
@@ -305,6 +326,8 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
             b_sel = None if bias is None else bias[jdx]
         gw = torch.zeros(jdx.numel(), hidden.shape[1], dtype=_F64)
         gb = torch.zeros(jdx.numel(), dtype=_F64)
+        gw_mag = torch.zeros_like(gw) if magnitudes else None
+        gb_mag = torch.zeros_like(gb) if magnitudes else None
         blk = _row_block(jdx.numel())
         for s in range(0, n, blk):
             ri = torch.arange(s, min(n, s + blk))
@@ -317,7 +340,13 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                          softcap, label_smoothing, z_loss, v)
             gw += d.T @ hidden[ri].to(_F64)
             gb += d.sum(dim=0)
+            if magnitudes:
+                gw_mag += _abs_terms(d.T, hidden[ri].to(_F64))
+                gb_mag += d.abs().sum(dim=0)
         out["grad_weight"] = gw
         out["grad_bias"] = gb if bias is not None else None
         out["vocab_rows"] = jdx
+        if magnitudes:
+            out["grad_weight_mag"] = gw_mag
+            out["grad_bias_mag"] = gb_mag if bias is not None else None
     return out

@@ -127,15 +127,26 @@ def row_weights(labels, n: int, v: int, ignore_index: int, reduction: str, grad_
     return torch.where(counted, g, torch.zeros_like(g))
 
 
+def _abs_terms(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """|a| @ |b|: the sums of the absolute values of the terms of a @ b."""
+    return a.abs() @ b.abs()
+
+
 def backward(hidden: torch.Tensor, weight: torch.Tensor, target_probs: torch.Tensor,
              bias: Optional[torch.Tensor] = None, labels: Optional[torch.Tensor] = None,
              ignore_index: int = -100, temperature: float = 1.0, eps: float = 1e-10,
              reduction: str = "batchmean", grad_out=1.0,
              rows: Optional[Sequence[int]] = None,
-             vocab_rows: Optional[Sequence[int]] = None) -> dict:
+             vocab_rows: Optional[Sequence[int]] = None,
+             magnitudes: bool = False) -> dict:
     """grad_hidden (selected rows), grad_weight and grad_bias (selected
     vocabulary rows) in fp64: with D_ij = g_i (p_ij sum_k q_ik - q_ij) / T,
-    grad_hidden = D @ W, grad_weight = D^T @ H, grad_bias = sum_i D_ij."""
+    grad_hidden = D @ W, grad_weight = D^T @ H, grad_bias = sum_i D_ij.
+
+    ``magnitudes`` also returns the sums of the absolute values of each
+    entry's terms (``*_mag``: sum_j |D_ij||W_jk|, sum_i |D_ij||h_ik|,
+    sum_i |D_ij|), the scale against which rounding D is judged (as in the
+    cross-entropy oracle). Test infrastructure; the gradients are unchanged."""
     n = hidden.shape[0]
     v = weight.shape[0]
     g_all = row_weights(labels, n, v, ignore_index, reduction, grad_out)
@@ -146,6 +157,9 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, target_probs: torch.Ten
     gh = torch.empty(idx.numel(), hidden.shape[1], dtype=_F64)
     gw = torch.zeros(jdx.numel(), hidden.shape[1], dtype=_F64)
     gb = torch.zeros(jdx.numel(), dtype=_F64)
+    gh_mag = torch.empty_like(gh) if magnitudes else None
+    gw_mag = torch.zeros_like(gw) if magnitudes else None
+    gb_mag = torch.zeros_like(gb) if magnitudes else None
     blk = _row_block(v)
     pos_of = torch.full((n,), -1, dtype=torch.int64)  # position of each row among `rows`
     pos_of[idx] = torch.arange(idx.numel())
@@ -162,5 +176,14 @@ def backward(hidden: torch.Tensor, weight: torch.Tensor, target_probs: torch.Ten
         pos = pos_of[ri]
         take = pos >= 0
         gh[pos[take]] = d[take] @ w64
-    return {"grad_hidden": gh, "grad_weight": gw,
-            "grad_bias": gb if bias is not None else None, "rows": idx, "vocab_rows": jdx}
+        if magnitudes:
+            gw_mag += _abs_terms(d[:, jdx].T, hidden[ri].to(_F64))
+            gb_mag += d[:, jdx].abs().sum(dim=0)
+            gh_mag[pos[take]] = _abs_terms(d[take], w64)
+    out = {"grad_hidden": gh, "grad_weight": gw,
+           "grad_bias": gb if bias is not None else None, "rows": idx, "vocab_rows": jdx}
+    if magnitudes:
+        out["grad_hidden_mag"] = gh_mag
+        out["grad_weight_mag"] = gw_mag
+        out["grad_bias_mag"] = gb_mag if bias is not None else None
+    return out

@@ -22,7 +22,7 @@ import pytest
 import torch
 
 import oracle
-from _parity import TOL, check_backward, check_forward, grad_scale, oracle_args, run_gpu, to_dev
+from _parity import TOL, check_backward, check_forward, grad_kappas, oracle_args, run_gpu, to_dev
 from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make_inputs, peaked_rows
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -87,14 +87,14 @@ def test_fullsize_parity(name):
     peaked = peaked_rows(w)
     rows = _sample_rows(w, x["targets"], peaked)
     vocab = _sample_vocab(w, x["targets"], rows, peaked)
-    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab)
+    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab,
+                           magnitudes=True)
     sampled = {
         "grad_hidden": out["grad_hidden"][rows],
         "grad_weight": out["grad_weight"][vocab],
         "grad_bias": None if out["grad_bias"] is None else out["grad_bias"][vocab],
     }
-    check_backward(sampled, gref, tol, x["bias"] is not None,
-                   grad_scale(w.reduction, ref["n_valid"]))
+    check_backward(sampled, gref, tol, x["bias"] is not None, grad_kappas(w))
     if w.softcap is None and w.logit_scale == 1.0:
         gw = out["grad_weight"].double()
         col = gw.sum(dim=0).abs()
@@ -110,7 +110,8 @@ def test_fullsize_kl_parity():
     for all N rows; gradients on sampled rows; and, at any size,
     sum_j grad_weight[j, :] = 0 (each counted row's p * sum q - q sums to 0
     over the vocabulary)."""
-    from _parity import assert_grad_close, assert_rows_close
+    from _parity import (assert_grad_close, assert_rows_close, assert_scalar_close, kl_row_ops,
+                         row_floor)
     from linear_cross_entropy_vocab_gb300 import api
     from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
     from oracle import kl_oracle
@@ -137,18 +138,27 @@ def test_fullsize_kl_parity():
                             1e-10, "batchmean")
     counted = ref["counted"]
     assert int(f["n_counted"]) == ref["n_counted"]
-    assert_rows_close("loss_rows", f["loss_rows"].cpu(), ref["loss"], tol["loss_rel"])
-    assert_rows_close("lse_rows", f["lse_rows"].cpu(), ref["lse"], tol["loss_rel"], counted)
+    floor = row_floor(w.h, kl_row_ops(ref))
+    assert_rows_close("loss_rows", f["loss_rows"].cpu(), ref["loss"], tol["loss_rel"],
+                      floor=floor)
+    assert_rows_close("lse_rows", f["lse_rows"].cpu(), ref["lse"], tol["loss_rel"], counted,
+                      floor)
     assert_rows_close("qsum_rows", f["qsum_rows"].cpu(), ref["qsum"], 1e-5, counted)
-    r = ref["loss_out"]
-    assert abs(float(f["loss"]) - r) <= tol["loss_rel"] * max(1.0, abs(r))
+    nc = ref["n_counted"]
+    assert_scalar_close("loss", float(f["loss"]), ref["loss_out"], tol["loss_rel"],
+                        float(floor[counted].sum()) / nc,
+                        float(ref["loss"][counted].abs().sum()) / nc, nc)
     rows = _sample_rows(w, x["targets"], torch.empty(0, dtype=torch.int64), k=256)
     vocab = _sample_vocab(w, x["targets"], rows, torch.empty(0, dtype=torch.int64), k=128)
     gref = kl_oracle.backward(x["hidden"], x["weight"], q, None, x["targets"], w.ignore_index,
-                              1.0, 1e-10, "batchmean", 1.0, rows=rows, vocab_rows=vocab)
+                              1.0, 1e-10, "batchmean", 1.0, rows=rows, vocab_rows=vocab,
+                              magnitudes=True)
     gh_c, gw_c = gh.cpu(), gw.cpu()
-    assert_grad_close("grad_hidden", gh_c[rows], gref["grad_hidden"], tol)
-    assert_grad_close("grad_weight", gw_c[vocab], gref["grad_weight"], tol)
+    kap = grad_kappas(w)
+    assert_grad_close("grad_hidden", gh_c[rows], gref["grad_hidden"], tol,
+                      gref["grad_hidden_mag"], kap["grad_hidden"])
+    assert_grad_close("grad_weight", gw_c[vocab], gref["grad_weight"], tol,
+                      gref["grad_weight_mag"], kap["grad_weight"])
     assert torch.all(gh_c[~counted] == 0)
     g64 = gw_c.double()
     col = g64.sum(dim=0).abs()
@@ -204,7 +214,8 @@ def test_largest_vocabulary_sampled():
     check_forward(out, ref, w, tol, skipped=True)
     rows = _sample_rows(w, x["targets"], torch.empty(0, dtype=torch.int64), k=128)
     vocab = _sample_vocab(w, x["targets"], rows, torch.empty(0, dtype=torch.int64), k=128)
-    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab)
+    gref = oracle.backward(*oracle_args(x, w), 1.0, lse=ref["lse"], rows=rows, vocab_rows=vocab,
+                           magnitudes=True)
     sampled = {"grad_hidden": out["grad_hidden"][rows], "grad_weight": out["grad_weight"][vocab],
                "grad_bias": out["grad_bias"][vocab]}
-    check_backward(sampled, gref, tol, True, grad_scale(w.reduction, ref["n_valid"]))
+    check_backward(sampled, gref, tol, True, grad_kappas(w))
