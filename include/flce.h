@@ -175,13 +175,17 @@ flce_status flce_forward(const flce_problem* p, const void* hidden,
  *   Arguments and outputs are those of flce_forward() without `workspace`
  *   and `workspace_bytes`; results are the same as flce_forward's.
  *   Scratch: a fixed 16 MiB array inside the library, held by every GPU that
- *   loads the library until the process exits. Problems whose forward
- *   workspace (flce_forward_workspace_size) exceeds 16 MiB -- roughly
- *   N * ceil(V/256) * 16 bytes for bf16, e.g. N <= 2000 at V = 128256 -- are
- *   rejected with FLCE_ERR_UNSUPPORTED before any launch.
+ *   loads the library until the process exits. A problem is accepted when
+ *   flce_forward_workspace_size(p) <= 16 MiB, and otherwise rejected with
+ *   FLCE_ERR_UNSUPPORTED before any launch. For bf16 at H = 4096,
+ *   V = 128256 that is N <= 2089 tokens; with FLCE_SKIP_IGNORED_ROWS, whose
+ *   gathered copy of the kept hidden rows adds N * H * 2 bytes, N <= 1033
+ *   (N <= 919 with label smoothing as well).
  *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress) with that device current, and so does the first
+ *   call after the device's context was destroyed and re-created (for
+ *   example by cudaDeviceReset); make that first call before any stream
+ *   capture.
  *   All calls share the one array, which keeps the last call's contents:
  *   calls whose work overlaps on the GPU (for example on two streams without
  *   ordering between them) race and corrupt each other's results. Order them

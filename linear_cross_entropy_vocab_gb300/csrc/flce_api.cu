@@ -357,6 +357,34 @@ flce_status check_workspace(void* ws, size_t have, size_t need) {
   return FLCE_OK;
 }
 
+// Problem and pointer checks of the cross-entropy forward (flce_forward and
+// flce_forward_noalloc): argument errors are reported before anything else.
+flce_status check_forward_args(const flce_problem* p, const void* hidden, const void* weight,
+                               const void* bias, const int64_t* targets, const float* loss_rows,
+                               const float* lse_rows, const float* loss_out,
+                               const int32_t* n_valid) {
+  flce_status st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  const size_t in_align = is_tc(p) ? 16 : 4;
+  if (weight == nullptr) return fail(FLCE_ERR_INVALID_ARG, "weight is NULL");
+  if (n_valid == nullptr) return fail(FLCE_ERR_INVALID_ARG, "n_valid is NULL");
+  if (p->reduction != FLCE_RED_NONE && loss_out == nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "loss_out is NULL (required for sum and mean)");
+  if (p->has_bias && bias == nullptr) return fail(FLCE_ERR_INVALID_ARG, "has_bias but bias is NULL");
+  if (!p->has_bias && bias != nullptr)
+    return fail(FLCE_ERR_INVALID_ARG, "bias given but has_bias is 0");
+  if (p->n > 0) {
+    if (hidden == nullptr || targets == nullptr || loss_rows == nullptr || lse_rows == nullptr)
+      return fail(FLCE_ERR_INVALID_ARG, "hidden, targets, loss_rows and lse_rows are required");
+    if (!aligned(hidden, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "hidden is misaligned");
+    if (!aligned(targets, 8)) return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
+  }
+  if (!aligned(weight, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "weight is misaligned");
+  if (bias != nullptr && !aligned(bias, in_align))
+    return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
+  return FLCE_OK;
+}
+
 // Valid-row compaction (FLCE_SKIP_IGNORED_ROWS): row_map / n_kept from the
 // targets, then the kept rows of hidden (and, through `gp`, of the per-row
 // inputs the caller names) gathered into the workspace. `cp` and `gp` carry
@@ -775,27 +803,66 @@ static __device__ __align__(256) unsigned char flce_static_scratch[kStaticScratc
 
 namespace {
 
+// The array's device address, per device, with the id of the context it was
+// looked up in: a context that is torn down and re-created (cudaDeviceReset)
+// loads the module again, possibly at another address.
+struct ScratchAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {nullptr};
+ScratchAddr g_scratch_addr[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_fn_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Unique id of the context current on the calling thread.
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // Device address of flce_static_scratch on the current device. The host-side
 // name of the array is only a stand-in, so the address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress with the device current: once per device, and again
+// whenever the device's context is not the one the cached address came from.
+// The caller has made the device's primary context current (check_device).
 flce_status static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(FLCE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  unsigned long long ctx_id = 0;
+  if (!current_context_id(&ctx_id))
+    return fail(FLCE_ERR_CUDA, "cannot identify the current CUDA context");
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    e = cudaSetDevice(dev);  // bind this device's primary context to the thread
-    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (a.ptr == nullptr || a.ctx_id != ctx_id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, flce_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(flce_static_scratch)");
-    g_scratch_addr[dev] = ptr;
+    a.ptr = ptr;
+    a.ctx_id = ctx_id;
   }
-  *out = g_scratch_addr[dev];
+  *out = a.ptr;
   return FLCE_OK;
 }
 
@@ -887,28 +954,12 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
                          float* loss_out, float* metrics_out, int32_t* n_valid, int32_t* err_word,
                          void* workspace, size_t workspace_bytes, void* stream) {
   g_err[0] = 0;
-  flce_status st = check_problem(p);
+  flce_status st = check_forward_args(p, hidden, weight, bias, targets, loss_rows, lse_rows,
+                                      loss_out, n_valid);
   if (st != FLCE_OK) return st;
   const bool bf16 = is_tc(p);  // tensor-core path (bf16 or fp16)
-  const size_t in_align = bf16 ? 16 : 4;
   g_map_type = p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (weight == nullptr) return fail(FLCE_ERR_INVALID_ARG, "weight is NULL");
-  if (n_valid == nullptr) return fail(FLCE_ERR_INVALID_ARG, "n_valid is NULL");
-  if (p->reduction != FLCE_RED_NONE && loss_out == nullptr)
-    return fail(FLCE_ERR_INVALID_ARG, "loss_out is NULL (required for sum and mean)");
-  if (p->has_bias && bias == nullptr) return fail(FLCE_ERR_INVALID_ARG, "has_bias but bias is NULL");
-  if (!p->has_bias && bias != nullptr)
-    return fail(FLCE_ERR_INVALID_ARG, "bias given but has_bias is 0");
-  if (p->n > 0) {
-    if (hidden == nullptr || targets == nullptr || loss_rows == nullptr || lse_rows == nullptr)
-      return fail(FLCE_ERR_INVALID_ARG, "hidden, targets, loss_rows and lse_rows are required");
-    if (!aligned(hidden, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "hidden is misaligned");
-    if (!aligned(targets, 8)) return fail(FLCE_ERR_UNSUPPORTED, "targets is misaligned");
-  }
-  if (!aligned(weight, in_align)) return fail(FLCE_ERR_UNSUPPORTED, "weight is misaligned");
-  if (bias != nullptr && !aligned(bias, in_align))
-    return fail(FLCE_ERR_UNSUPPORTED, "bias is misaligned");
   const FwdPlan plan = plan_forward(p);
   st = check_workspace(workspace, workspace_bytes, plan.total);
   if (st != FLCE_OK) return st;
@@ -1257,15 +1308,21 @@ flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden, cons
                                  float* loss_out, float* metrics_out, int32_t* n_valid,
                                  int32_t* err_word, void* stream) {
   g_err[0] = 0;
-  flce_status st = check_problem(p);
+  flce_status st = check_forward_args(p, hidden, weight, bias, targets, loss_rows, lse_rows,
+                                      loss_out, n_valid);
   if (st != FLCE_OK) return st;
   const size_t need = plan_forward(p).total;
   if (need > kStaticScratchBytes)
     return fail(FLCE_ERR_UNSUPPORTED,
                 "flce_forward_noalloc: this problem needs %zu bytes of scratch, the fixed "
-                "scratch holds %zu (about N * ceil(V/256) * 16 bytes for bf16 must fit); "
+                "scratch holds %zu (flce_forward_workspace_size must not exceed it); "
                 "call flce_forward with a workspace instead",
                 need, kStaticScratchBytes);
+  // the same device check, in the same order, as flce_forward: an unsupported
+  // or absent device gives the same status before the symbol is looked up
+  DeviceInfo dev;
+  st = check_device(&dev);
+  if (st != FLCE_OK) return st;
   void* scratch = nullptr;
   st = static_scratch(&scratch);
   if (st != FLCE_OK) return st;
