@@ -36,8 +36,10 @@ KL_METRIC = "fused linear KL fwd+bwd tokens/s at H4096 V128256 bf16; % of dense-
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "llama3_head_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_ROLES = ("fwd_stats", "fwd_kl", "bwd_dlogits", "bwd_dlogits_kl", "bwd_grad_weight",
-              "bwd_grad_hidden")
+# contractions of N x H x V per step of each tensor-core role: bwd_grads runs
+# both gradient GEMMs (grad_hidden and grad_weight) in one launch per chunk
+GEMM_ROLES = {"fwd_stats": 1, "fwd_kl": 1, "bwd_dlogits": 1, "bwd_dlogits_kl": 1,
+              "bwd_grads": 2}
 # the fp32 path's contractions run on the FP32 FMA units (ALU-bound)
 ALU_ROLES = ("fwd_stats_f32", "fwd_kl_f32", "bwd_dlogits_f32", "bwd_grad_weight_f32",
              "bwd_grad_hidden_f32")
@@ -359,13 +361,8 @@ def bench_ours(args, rank, world, dev):
         raise RuntimeError(f"device error word {int(step.err.item())}")
 
     # ------------------------------------------------------ device-timed region
-    try:
-        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        smi_id = str(torch.cuda.current_device())
-    clocks = ClockSampler(smi_id)
+    clocks = ClockSampler(_smi_id(dev))
     clocks.start()
-    abi.flce_profile_enable(True)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -377,10 +374,18 @@ def bench_ours(args, rank, world, dev):
     torch.cuda.synchronize(dev)
     barrier()
     ms = t0.elapsed_time(t1)
-    prof, dropped = abi.flce_profile_collect()
-    abi.flce_profile_enable(False)
     clk = clocks.stop()
     ms = max_over_ranks(ms, world, dev)
+    # per-kernel times: a second pass of the same steps with CUDA events
+    # around every launch (events between launches keep the backward's
+    # launches from overlapping, so they are not recorded in the timed region)
+    abi.flce_profile_enable(True)
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        step(sh)
+    torch.cuda.synchronize(dev)
+    prof, dropped = abi.flce_profile_collect()
+    abi.flce_profile_enable(False)
 
     # ------------------------------------------------------ end to end (host buffers)
     # Every step copies its inputs from pinned host memory and reads its loss
@@ -502,6 +507,10 @@ def bench_ours(args, rank, world, dev):
     kernels = {k: {"launches": val[0], "ms_per_step": round(val[1] / args.steps, 4),
                    "share": round(val[1] / sum(u[1] for u in roles.values()), 4)}
                for k, val in roles.items()}
+    kernels_how = ("a second pass of the timed steps with CUDA events around every "
+                       "launch, on the launching stream; those events serialise launches that "
+                       "overlap in the timed region, so the per-kernel sum can exceed "
+                       "ms_per_step")
     out = {
         "metric": KL_METRIC if args.kl else METRIC,
         "value": round(tok_s, 1),
@@ -530,7 +539,10 @@ def bench_ours(args, rank, world, dev):
             "flops_per_step": flops_step, "peaks": peak_src},
         "roofline": roofline,
         "kernels": kernels,
+        "kernels_how": kernels_how,
         "gpu_launches": int(sum(val[0] for val in roles.values())),
+        "gpu_launches_how": "launches of this library's kernels in the profiled pass of the "
+                            "same steps (same launch sequence as the timed region)",
         "profile_dropped": dropped,
         "e2e": {"value": round(job_tokens_per_s(n, e2e_steps, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -547,6 +559,153 @@ def bench_ours(args, rank, world, dev):
                    "workspace_fwd_bytes": step.ws_f, "workspace_bwd_bytes": step.ws_b},
     }
     return out
+
+
+# ----------------------------------------------------------------- other workloads
+# Every workload besides the headline one, measured in the same process after
+# it: (key, workload name, options). The long batch is measured in both of its
+# phases: forward only with reduction none, then forward+backward with mean.
+PER_CONFIG = (
+    ("tiny_fp32", "tiny_fp32", {}),
+    ("mid_bf16", "mid_bf16", {}),
+    ("softcap_bf16", "softcap_bf16", {}),
+    ("long_bf16_forward_none", "long_bf16", {"forward_only": True}),
+    ("long_bf16", "long_bf16", {}),
+    ("llama3_head_bf16_kl", "llama3_head_bf16", {"kl": True}),
+)
+L2_BYTES = 129 << 20
+PER_CONFIG_TIMED_S = 0.4  # device time per workload's timed region (at least `steps` steps)
+
+
+def _flush_l2(buf):
+    buf.add_(1)  # writes 2 x L2 of memory: nothing of the last step stays in L2
+
+
+def measure_config(w, dev, steps, warmup, peaks, peak_src, forward_only=False, kl=False,
+                   cpu_budget_s=6.0, with_cpu=True):
+    """One workload: device-timed fwd(+bwd) steps through the C ABI (ignored
+    rows left out of the contractions), the dominant kernel's share, the
+    clock, peak incremental memory of one public-API step, and the oracle
+    timed on a bounded sample of the workload's rows."""
+    from linear_cross_entropy_vocab_gb300 import abi, api
+
+    xc = make_bench_inputs(w, kl)
+    x = {k: (None if t is None else t.to(dev)) for k, t in xc.items()}
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    step = (KLStep if kl else Step)(x, w, dev, skip_ignored=True, forward_only=forward_only)
+    in_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(max(warmup, 3)):
+        step(sh)
+    torch.cuda.synchronize(dev)
+    # steps: enough for about PER_CONFIG_TIMED_S of device time
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    step(sh)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    est = max(t0.elapsed_time(t1), 1e-3)
+    k = int(min(2000, max(steps, PER_CONFIG_TIMED_S * 1e3 / est)))
+    clocks = ClockSampler(_smi_id(dev))
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(k if flush is not None else 1)]
+    if flush is not None:
+        # per-step events, L2 written over between steps (inputs smaller than L2)
+        for a, b in ev:
+            _flush_l2(flush)
+            a.record(stream)
+            step(sh)
+            b.record(stream)
+    else:
+        ev[0][0].record(stream)
+        for _ in range(k):
+            step(sh)
+        ev[0][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    clk = clocks.stop()
+    abi.flce_profile_enable(True)  # per-kernel shares from a second, event-bracketed pass
+    for _ in range(min(k, 50)):
+        step(sh)
+    torch.cuda.synchronize(dev)
+    prof, _dropped = abi.flce_profile_collect()
+    abi.flce_profile_enable(False)
+    if int(step.err.item()) != 0:
+        raise RuntimeError(f"{w.name}: device error word {int(step.err.item())}")
+    n_valid = int(step.n_valid.item())
+    del step
+    # peak memory of one public-API step
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    hh = x["hidden"].detach().requires_grad_(not forward_only)
+    ww = x["weight"].detach().requires_grad_(not forward_only)
+    bb = None if x["bias"] is None else x["bias"].detach().requires_grad_(not forward_only)
+    if kl:
+        loss = api.fused_linear_kl_div(hh, ww, x["q"], x["targets"], bb,
+                                       temperature=KL_TEMPERATURE, reduction=KL_REDUCTION)
+    else:
+        loss = api.fused_linear_cross_entropy(hh, ww, x["targets"], bb, w.ignore_index,
+                                              w.logit_scale, w.softcap, w.reduction,
+                                              return_metrics=w.return_metrics)
+        if w.return_metrics:
+            loss = loss[0]
+    if not forward_only:
+        (loss.sum() if loss.dim() else loss).backward()
+    torch.cuda.synchronize(dev)
+    peak_incr = torch.cuda.max_memory_allocated(dev) - base
+    del hh, ww, bb, loss, flush
+    n, h, v = w.n, w.h, w.v
+    flops = gemm_flops(n, h, v) / (4.0 if forward_only else 1.0)
+    t_step = ms / k / 1e3
+    alu = w.dtype == "f32"
+    out = {
+        "workload": describe_kl(w) if kl else describe(w),
+        "step": "forward only" if forward_only else "forward+backward",
+        "steps": k, "ms_per_step": round(ms / k, 4), "tokens_per_s": round(n / t_step, 1),
+        "achieved_tflops": round(flops / t_step / 1e12, 2),
+        "l2": ("L2 written over between steps (inputs smaller than L2)" if len(ev) > 1
+               else f"inputs {in_bytes / 1e6:.0f} MB > L2, no flush"),
+        "clocks": {"sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons"),
+                   "samples": clk.get("samples")},
+        "memory": {"peak_incremental_bytes_public_api": int(peak_incr),
+                   "nxv_bf16_bytes": n * v * 2,
+                   "of_nxv_bf16": round(peak_incr / (n * v * 2), 4)},
+    }
+    if alu:
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        fma_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        out["fp32_fma_peak_frac"] = round(flops / t_step / 1e12 / fma_peak, 4)
+    else:
+        a = flops / t_step / 1e12
+        out["tensor_peak_frac"] = {
+            "of_burst": round(a / peaks["bf16_tflops"], 4),
+            "of_sustained": round(a / peaks["bf16_tflops_sustained"], 4),
+            "of_burst_kept_rows": round(a * n_valid / n / peaks["bf16_tflops"], 4),
+            "kept_rows": n_valid, "peaks": peak_src}
+    if prof:
+        dom = max(prof, key=lambda r: prof[r][1])
+        out["dominant_kernel"] = {"kernel": dom, "share": round(
+            prof[dom][1] / sum(u[1] for u in prof.values()), 4)}
+    del x
+    torch.cuda.empty_cache()
+    if with_cpu:
+        out["cpu_baseline"] = cpu_baseline(xc, w, budget_s=cpu_budget_s, kl=kl)
+    return out
+
+
+def _smi_id(dev) -> str:
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(torch.cuda.current_device())
 
 
 def traffic_key(w, args) -> str:
@@ -605,15 +764,23 @@ def cpu_model() -> str:
 
 
 def cpu_baseline(xc, w, budget_s=15.0, kl=False):
+    """The oracle's fp64 forward+backward on the first rows of the workload
+    (all of them when they fit the budget), as tokens/s. A sample of fewer
+    rows than the workload is extrapolated linearly in the rows: every row
+    costs the same full-vocabulary work."""
     rows, _ = _calibrate_rows(xc, w, budget_s, w.n, kl)
     t = time.perf_counter()
     (_oracle_kl_sample_step if kl else _oracle_sample_step)(xc, w, rows)
     dt = time.perf_counter() - t
     what = "fused linear KL " if kl else ""
+    full = rows >= w.n
     return {"value": round(rows / dt, 2), "unit": UNIT, "cores": torch.get_num_threads(),
-            "cpu_model": cpu_model(), "kind": "oracle",
-            "sample": f"fp64 {what}forward+backward of the first {rows} rows of the workload "
-                      f"(full H={w.h}, V={w.v}) as one batch; {dt:.1f} s"}
+            "cpu_model": cpu_model(), "kind": "oracle", "extrapolated": not full,
+            "sample": (f"fp64 {what}forward+backward of all {rows} rows of the workload; "
+                       f"{dt:.1f} s" if full else
+                       f"fp64 {what}forward+backward of the first {rows} of {w.n} rows of the "
+                       f"workload (full H={w.h}, V={w.v}) as one batch, {dt:.1f} s; "
+                       f"tokens/s extrapolated linearly in the rows")}
 
 
 def bench_reference(args):
@@ -659,7 +826,7 @@ def roofline_entry(dom, launches, tot_ms, steps, n_work, h, v, run_ms, peaks, pe
     fp32 (FFMA) roles against sms x 128 FP32 lanes x 2 flops x the maximum SM
     clock."""
     alu = dom in ALU_ROLES
-    per_step_flops = 2.0 * n_work * h * v if (dom in GEMM_ROLES or alu) else 0.0
+    per_step_flops = 2.0 * n_work * h * v * (GEMM_ROLES.get(dom, 0) or (1 if alu else 0))
     flops_per_launch = per_step_flops / (launches / steps)
     avg_ms = tot_ms / launches
     achieved = flops_per_launch / (avg_ms / 1e3) / 1e12
@@ -688,6 +855,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only (skip the per_config block)")
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default=None,
                     help="run the workload with this input type (default: the workload's)")
     ap.add_argument("--forward-only", action="store_true",
@@ -722,6 +891,16 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w = workload_of(args)
         out["cpu_baseline"] = cpu_baseline(make_bench_inputs(w, args.kl), w, kl=args.kl)
+    if not args.no_per_config and world == 1:
+        peaks, peak_src = load_peaks()
+        per = {}
+        for key, name, opts in PER_CONFIG:
+            wk = WORKLOADS[name]
+            if opts.get("forward_only") and name == "long_bf16":
+                wk = wk.with_shape(reduction="none")
+            per[key] = measure_config(wk, dev, args.steps, args.warmup, peaks, peak_src,
+                                      with_cpu=not args.no_cpu_baseline, **opts)
+        out["per_config"] = per
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -192,7 +192,7 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor,
     (1-eps)*onehot + eps/V) and ``z_loss`` lam (adds lam * lse^2 per row).
     ``vocab_chunk`` bounds the vocabulary columns of the backward's dlogits
     buffer (rounded up to a multiple of 256); 0 takes the library's default
-    (a 512 MiB buffer, or the whole vocabulary when that is smaller). A
+    (about a fifth of the vocabulary and at most a 512 MiB buffer). A
     smaller chunk lowers peak memory at some cost in speed.
     """
     if reduction not in abi.REDUCTIONS:

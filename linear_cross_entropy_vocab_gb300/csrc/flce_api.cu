@@ -170,7 +170,17 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Default backward vocabulary chunking: the dlogits buffer D of one chunk is
+// at most 512 MiB and spans at most about a fifth of the vocabulary (V/5
+// rounded up to whole 256-column tiles), so that together with grad_weight
+// (V x H), grad_hidden and its fp32 accumulator the backward stays below
+// the N x V logits of a plain implementation even where H is half of N (the
+// 4096-token, 2048-wide, 32000-word head: peak 0.96 x N V 2 bytes). Chunks
+// narrower than 2048 columns are not made for the sake of the fifth: small
+// vocabularies keep fewer, wider chunks.
 constexpr int64_t kDefaultDlogitsBudget = int64_t(512) << 20;  // bytes of one dlogits chunk
+constexpr int64_t kMinDefaultChunks = 5;
+constexpr int64_t kMinDefaultChunkWidth = 2048;
 
 // Tile bands (GemmGeom::group) of the row-tile-fastest GEMMs. With bands of
 // 16 pair row tiles (4096 rows) the forward and dlogits kernels re-read
@@ -198,7 +208,7 @@ struct FwdPlan {
 
 struct BwdPlan {
   int64_t chunk = 0, n_chunks = 0, gb_parts = 0;
-  size_t d = 0, acc = 0, gb = 0, scales = 0, total = 0;
+  size_t d = 0, acc = 0, gb = 0, scales = 0, sched = 0, sched_bytes = 0, total = 0;
   bool use_acc = false;
   CompactPlan cp;
 };
@@ -307,9 +317,19 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   if (c > 0) {
     c = cdiv(c, 256) * 256;
   } else {
+    // balanced chunks: at least kMinDefaultChunks (while each stays at least
+    // kMinDefaultChunkWidth wide), more when one would exceed the budget
     const int64_t rows = p->n > 0 ? p->n : 1;
-    c = (kDefaultDlogitsBudget / (rows * elem)) / 256 * 256;
-    if (c < 256) c = 256;
+    int64_t nch = cdiv(rows * elem * v_round, kDefaultDlogitsBudget);
+    const int64_t wide_enough = v_round / kMinDefaultChunkWidth;
+    const int64_t floor_chunks = wide_enough < kMinDefaultChunks ? wide_enough : kMinDefaultChunks;
+    if (nch < floor_chunks) nch = floor_chunks;
+    if (nch < 1) nch = 1;
+    c = cdiv(cdiv(p->v, nch), 256) * 256;
+    while (c > 256 && c * rows * elem > kDefaultDlogitsBudget) {
+      ++nch;
+      c = cdiv(cdiv(p->v, nch), 256) * 256;
+    }
   }
   if (c > v_round) c = v_round;
   b.chunk = c;
@@ -325,6 +345,13 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
   b.scales = off;
   if (p->dtype == FLCE_F16) off = align_up(off + 2 * sizeof(float));
+  // tile counters of the dynamically scheduled gradient launches, one per
+  // chunk, zeroed at the start of every backward call
+  b.sched = off;
+  if (is_tc(p)) {
+    b.sched_bytes = align_up(static_cast<size_t>(b.n_chunks) * sizeof(int));
+    off += b.sched_bytes;
+  }
   off = plan_compaction(p, true, kl, off, &b.cp);
   b.total = off;
   return b;
@@ -540,6 +567,9 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
     void* dbuf = ws + plan.d;
     float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
     const int type = tc_type(p);
+    int* sched = reinterpret_cast<int*>(ws + plan.sched);
+    e = cudaMemsetAsync(sched, 0, plan.sched_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (tile counters)");
     // fp16: D is stored times a power of two, undone by the gradient GEMMs
     float* scales = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + plan.scales) : nullptr;
     if (scales != nullptr) {
@@ -614,6 +644,13 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       g1.dyn_rows = n_kept;
       g1.dyn_axis = 0;
       g1.err_word = err_word;
+      // Successive launches overlap: the next kernel's CTAs start on the SMs
+      // the previous one has left. dlogits stores D only after the previous
+      // chunk's gradient launch, which reads D, has completed; the gradient
+      // launch reads D only after this dlogits has completed. Each kernel
+      // thus completes after its predecessor, so the fp32 grad_hidden
+      // accumulator is updated one chunk after another.
+      g1.pdl = flce::kPdlWaitEpilogue;
       if (kl != nullptr) {
         flce::DlogitsKLParams dp{};
         dp.bias = bias;
@@ -671,8 +708,14 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       }
       if (e != cudaSuccess) return cuda_fail(e, "dlogits kernel");
 
-      // 2. grad_weight[c0 : c0+width] = D^T @ hidden
-      GemmGeom g2{};
+      // 2. and 3., one launch: grad_weight[c0 : c0+width] = D^T @ hidden and
+      // grad_hidden (+)= D @ weight[c0 : c0+width]
+      flce::GradsLaunch gl{};
+      gl.tm_d_k = tm_d_k;
+      gl.tm_weight_mn = tm_w_mn;
+      gl.tm_d_mn = tm_d_mn;
+      gl.tm_hidden_mn = tm_h_mn;
+      GemmGeom& g2 = gl.g_gw;
       g2.m_tiles = static_cast<int>(cdiv(width, flce::kTileRowsTC));
       g2.n_tiles = h_tiles;
       g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
@@ -680,7 +723,7 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       g2.dyn_rows = n_kept;  // the contraction runs over the kept rows
       g2.dyn_axis = 1;
       g2.err_word = err_word;
-      flce::StoreRowsParams sp{};
+      flce::StoreRowsParams& sp = gl.sp;
       sp.out = grad_weight;
       sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
       sp.out_scale = scales != nullptr ? scales + 1 : nullptr;
@@ -688,14 +731,7 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       sp.rows = width;
       sp.row0 = c0;
       sp.cols = static_cast<int>(p->h);
-      {
-        ProfScope ps("bwd_grad_weight", s);
-        e = flce::launch_tc_grad_weight(type, tm_d_mn, tm_h_mn, g2, sp, dev.sms, s);
-      }
-      if (e != cudaSuccess) return cuda_fail(e, "grad_weight kernel");
-
-      // 3. grad_hidden (+)= D @ weight[c0 : c0+width]
-      GemmGeom g3{};
+      GemmGeom& g3 = gl.g_gh;
       g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
       g3.n_tiles = h_tiles;
       g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
@@ -705,7 +741,7 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       g3.dyn_rows = n_kept;
       g3.dyn_axis = 0;
       g3.err_word = err_word;
-      flce::AccRowsParams ap{};
+      flce::AccRowsParams& ap = gl.ap;
       ap.acc = acc;
       ap.out = grad_hidden;
       ap.out_scale = scales != nullptr ? scales + 1 : nullptr;
@@ -722,11 +758,16 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       ap.rows_dyn = n_kept;
       ap.row_map = row_map;
       ap.cols = static_cast<int>(p->h);
+      gl.sched = sched + c;
+      g2.pdl = flce::kPdlWaitLoads | flce::kPdlWaitEpilogue;
+      g3.pdl = flce::kPdlWaitLoads | flce::kPdlWaitEpilogue;
+      // the longer contraction's tiles are handed out first
+      gl.gh_first = g3.k_iters >= g2.k_iters;
       {
-        ProfScope ps("bwd_grad_hidden", s);
-        e = flce::launch_tc_grad_hidden(type, tm_d_k, tm_w_mn, g3, ap, dev.sms, s);
+        ProfScope ps("bwd_grads", s);
+        e = flce::launch_tc_grads(type, gl, dev.sms, s);
       }
-      if (e != cudaSuccess) return cuda_fail(e, "grad_hidden kernel");
+      if (e != cudaSuccess) return cuda_fail(e, "gradient kernel");
     }
   } else {
     float* dbuf = reinterpret_cast<float*>(ws + plan.d);

@@ -157,12 +157,21 @@ cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
 // warps per TMEM lane quarter keep the epilogue under the MMAs.
 constexpr int64_t kDlogitsEpi8MaxH = 2048;
 inline int dlogits_epi_warps(int64_t h) { return h <= kDlogitsEpi8MaxH ? 8 : 4; }
-cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,
-                                  const CUtensorMap& tm_hidden_mn, const GemmGeom& g,
-                                  const StoreRowsParams& p, int sms, cudaStream_t s);
-cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
-                                  const CUtensorMap& tm_weight_mn, const GemmGeom& g,
-                                  const AccRowsParams& p, int sms, cudaStream_t s);
+
+// Both gradient GEMMs of one vocabulary chunk in one launch, tiles drawn
+// from the device counter `sched` (zero before the launch):
+//   grad_hidden: A = D (K-major, tm_d_k), B = weight rows (MN-major), AccRows;
+//   grad_weight: A = D^T (MN-major, tm_d_mn), B = hidden (MN-major), StoreRows.
+// gh_first puts grad_hidden's tiles first (the longer contraction should).
+struct GradsLaunch {
+  CUtensorMap tm_d_k, tm_weight_mn, tm_d_mn, tm_hidden_mn;
+  GemmGeom g_gh, g_gw;
+  AccRowsParams ap;
+  StoreRowsParams sp;
+  int* sched;
+  bool gh_first;
+};
+cudaError_t launch_tc_grads(int type, const GradsLaunch& l, int sms, cudaStream_t s);
 
 // Bounded-wait self-test: result[0] (one CTA) and result[1..2] (a CTA pair).
 cudaError_t launch_wait_selftest(int* err_word, uint64_t budget_ns, int* result, cudaStream_t s);

@@ -675,26 +675,25 @@ cudaError_t launch_wait_selftest(int* err_word, uint64_t budget_ns, int* result,
 namespace {
 
 // Persistent grid: one CTA (CG = 1) or one CTA pair (CG = 2) per resident
-// slot, never more than there are tiles.
-template <int CG, bool A_MN, bool B_MN, class Epi>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmGeom& g,
-                        const typename Epi::Params& ep, int sms, cudaStream_t stream) {
-  auto kern = tc_gemm_kernel<CG, A_MN, B_MN, Epi>;
+// slot, never more than there are tiles (of both segments).
+template <int CG, class S0, class S1>
+cudaError_t launch_gemm_args(const GemmArgs<S0, S1>& a, int sms, cudaStream_t stream) {
+  auto kern = tc_gemm_kernel<CG, S0, S1>;
   constexpr int smem = gemm_smem_bytes<CG>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(gemm_threads<Epi>(), 1, 1);
+  cudaLaunchAttribute attr[2];
+  cfg.blockDim = dim3(gemm_threads<typename S0::Epi>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  cfg.attrs = attr;
   int units = sms;
   if constexpr (CG == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
     int dev = 0;
     e = cudaGetDevice(&dev);
@@ -711,12 +710,66 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
     }
     units = max_clusters[dev];
   }
-  const int64_t total = static_cast<int64_t>(g.m_tiles) * g.n_tiles;
+  int64_t total = static_cast<int64_t>(a.g0.m_tiles) * a.g0.n_tiles;
+  if constexpr (S1::kPresent) total += static_cast<int64_t>(a.g1.m_tiles) * a.g1.n_tiles;
   const int64_t grid_units = total < units ? total : units;
+  if (grid_units < 1) return cudaSuccess;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CG), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, g, ep);
+  if (a.g0.pdl != 0) {
+    // may start while the previous kernel of the stream drains (see GemmGeom::pdl)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// One GEMM (one segment), statically scheduled unless g.sched is set.
+template <int CG, bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmGeom& g,
+                        const typename Epi::Params& ep, int sms, cudaStream_t stream) {
+  GemmArgs<Seg<A_MN, B_MN, Epi>, NoSeg> a{};
+  a.a0 = ta;
+  a.b0 = tb;
+  a.g0 = g;
+  a.ep0 = ep;
+  return launch_gemm_args<CG>(a, sms, stream);
+}
+
+// grad_hidden (D K-major times W MN-major, accumulated rows) and grad_weight
+// (D^T times hidden, both MN-major, stored rows) of one vocabulary chunk in
+// one dynamically scheduled launch; the segment with the longer contraction
+// goes first so that its tiles are handed out before the shorter ones.
+template <typename T>
+cudaError_t launch_grads_typed(const GradsLaunch& l, int sms, cudaStream_t s) {
+  using GH = Seg<false, true, EpiAccRows<T>>;
+  using GW = Seg<true, true, EpiStoreRows<T>>;
+  if (l.gh_first) {
+    GemmArgs<GH, GW> a{};
+    a.a0 = l.tm_d_k;
+    a.b0 = l.tm_weight_mn;
+    a.g0 = l.g_gh;
+    a.ep0 = l.ap;
+    a.a1 = l.tm_d_mn;
+    a.b1 = l.tm_hidden_mn;
+    a.g1 = l.g_gw;
+    a.ep1 = l.sp;
+    a.g0.sched = l.sched;
+    return launch_gemm_args<kPairCG>(a, sms, s);
+  }
+  GemmArgs<GW, GH> a{};
+  a.a0 = l.tm_d_mn;
+  a.b0 = l.tm_hidden_mn;
+  a.g0 = l.g_gw;
+  a.ep0 = l.sp;
+  a.a1 = l.tm_d_k;
+  a.b1 = l.tm_weight_mn;
+  a.g1 = l.g_gh;
+  a.ep1 = l.ap;
+  a.g0.sched = l.sched;
+  return launch_gemm_args<kPairCG>(a, sms, s);
 }
 
 }  // namespace
@@ -784,24 +837,9 @@ cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
                                                                           sms, s);
 }
 
-cudaError_t launch_tc_grad_weight(int type, const CUtensorMap& tm_d_mn,
-                                  const CUtensorMap& tm_hidden_mn, const GemmGeom& g,
-                                  const StoreRowsParams& p, int sms, cudaStream_t s) {
-  if (type == kTcF16)
-    return launch_gemm<kPairCG, true, true, EpiStoreRows<__half>>(tm_d_mn, tm_hidden_mn, g, p,
-                                                                   sms, s);
-  return launch_gemm<kPairCG, true, true, EpiStoreRows<__nv_bfloat16>>(tm_d_mn, tm_hidden_mn, g,
-                                                                        p, sms, s);
-}
-
-cudaError_t launch_tc_grad_hidden(int type, const CUtensorMap& tm_d_k,
-                                  const CUtensorMap& tm_weight_mn, const GemmGeom& g,
-                                  const AccRowsParams& p, int sms, cudaStream_t s) {
-  if (type == kTcF16)
-    return launch_gemm<kPairCG, false, true, EpiAccRows<__half>>(tm_d_k, tm_weight_mn, g, p, sms,
-                                                                  s);
-  return launch_gemm<kPairCG, false, true, EpiAccRows<__nv_bfloat16>>(tm_d_k, tm_weight_mn, g, p,
-                                                                        sms, s);
+cudaError_t launch_tc_grads(int type, const GradsLaunch& l, int sms, cudaStream_t s) {
+  if (type == kTcF16) return launch_grads_typed<__half>(l, sms, s);
+  return launch_grads_typed<__nv_bfloat16>(l, sms, s);
 }
 
 }  // namespace flce

@@ -22,6 +22,15 @@
 // The 512 TMEM columns hold two 128 x 256 fp32 accumulators per CTA, so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 //
+// A launch runs the tiles of one GEMM or of two GEMMs that share nothing but
+// the SMs ("segments": each with its own operands, majorness, extents and
+// epilogue). Tiles are taken either statically (unit u of U takes tiles u,
+// u + U, ...) or dynamically: the even CTA's producer thread draws the next
+// tile index from a global counter and hands it to every role of both CTAs
+// through a small ring in shared memory, so that a pair that finishes early
+// takes more tiles. Dynamic scheduling balances tiles of unequal length (the
+// two segments' contractions differ) and fills the last round.
+//
 // Each operand is K-major (rows of K contiguous elements) or MN-major (K rows
 // of contiguous M or N elements); both are staged with 128-byte swizzle:
 //   K-major:  one TMA box {64 (K), rows}; 8-row groups 1024 B apart.
@@ -54,12 +63,17 @@ struct TileCfg {
   static constexpr int kTileRows = kBM * CG;  // M rows of one (pair) tile
 };
 
+constexpr int kSchedSlots = 8;  // tile indices in flight between the roles (dynamic scheduling)
+
 struct GemmCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
+  uint64_t sched_full[kSchedSlots];   // slot holds a tile index (count 1: the fetching thread)
+  uint64_t sched_empty[kSchedSlots];  // every reading role has taken it (even CTA's barriers)
+  int sched_tile[kSchedSlots];        // tile index, or -1: no tiles left
   uint32_t tmem_base;
   int abort;
   float red[4][kBN / 32][32];  // epilogue scratch: per-warp column sums, [quarter][chunk][lane]
@@ -90,7 +104,19 @@ struct GemmGeom {
   // the other axis reuses, which keeps it in L2.
   int group;
   int* err_word;
+  // Dynamic scheduling (read from the first segment's geometry): a device
+  // counter, zero before the launch, from which tile indices are drawn; null
+  // for static scheduling.
+  int* sched;
+  // Programmatic dependent launch (first segment's geometry; the launch
+  // carries the attribute when non-zero). Every CTA lets the next kernel
+  // start at once; kPdlWaitLoads: the producer waits for the previous
+  // kernels before its first load; kPdlWaitEpilogue: the epilogue threads
+  // wait before their first tile.
+  int pdl;
 };
+constexpr int kPdlWaitLoads = 1;
+constexpr int kPdlWaitEpilogue = 2;
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int m_tiles, int u, int& m,
                                             int& n) {
@@ -223,6 +249,31 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
+// Tile and contraction extents of one segment, with the device-side row
+// count applied.
+template <int CG>
+__device__ __forceinline__ void seg_extent(const GemmGeom& g, int& m_tiles, int& k_iters) {
+  using Cfg = TileCfg<CG>;
+  m_tiles = g.m_tiles;
+  k_iters = g.k_iters;
+  if (g.dyn_rows != nullptr) {
+    const int r = *g.dyn_rows;
+    if (g.dyn_axis == 0) {
+      const int t = (r + Cfg::kTileRows - 1) / Cfg::kTileRows;
+      m_tiles = t < m_tiles ? t : m_tiles;
+    } else {
+      const int t = (r + kBK - 1) / kBK;
+      k_iters = t < k_iters ? t : k_iters;
+    }
+  }
+}
+
+// Stores `v` into the shared variable at shared::cluster address `addr`
+// (possibly in the peer CTA).
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Epi must provide:
 //   static constexpr uint32_t kABFormat;  // operand type: 1 bf16, 0 fp16
 //   struct Params;
@@ -235,30 +286,64 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 // column 0 of the tile's accumulator (read it with load_acc(..., acc_zero));
 // `part` is this warp's column half with 8 epilogue warps, else 0; the
 // epilogue threads may use named barrier 1.
-template <int CG, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const GemmGeom g, const typename Epi::Params ep) {
+
+// One GEMM of a launch: operand majorness and epilogue.
+template <bool A_MN_, bool B_MN_, class Epi_>
+struct Seg {
+  static constexpr bool kPresent = true;
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+  using Epi = Epi_;
+};
+
+// The absent second segment of a one-GEMM launch.
+struct NoEpi {
+  static constexpr uint32_t kABFormat = 1;
+  struct Params {};
+  __device__ static void tile(const Params&, int, int, uint32_t, bool, int, int, int, int,
+                              GemmCtl*) {}
+};
+struct NoSeg {
+  static constexpr bool kPresent = false;
+  static constexpr bool A_MN = false;
+  static constexpr bool B_MN = false;
+  using Epi = NoEpi;
+};
+
+// Kernel arguments: tensor maps, geometry and epilogue parameters of both
+// segments (the second ones unused for a one-GEMM launch). Tile indices
+// [0, tiles of segment 0) are segment 0's, the rest segment 1's.
+template <class S0, class S1>
+struct GemmArgs {
+  CUtensorMap a0, b0, a1, b1;
+  GemmGeom g0, g1;
+  typename S0::Epi::Params ep0;
+  typename S1::Epi::Params ep1;
+};
+
+template <int CG, class S0, class S1>
+__global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
+    tc_gemm_kernel(const __grid_constant__ GemmArgs<S0, S1> args) {
   using Cfg = TileCfg<CG>;
+  using E0 = typename S0::Epi;
+  using E1 = typename S1::Epi;
+  constexpr int W = EpiWarps<E0>::value;
+  static_assert(!S1::kPresent || EpiWarps<E1>::value == W, "segments differ in epilogue warps");
+  static_assert(!S1::kPresent || E1::kABFormat == E0::kABFormat, "segments differ in type");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int m_tiles = g.m_tiles;
-  int k_iters = g.k_iters;
-  if (g.dyn_rows != nullptr) {
-    const int r = *g.dyn_rows;
-    if (g.dyn_axis == 0) {
-      const int t = (r + Cfg::kTileRows - 1) / Cfg::kTileRows;
-      m_tiles = t < m_tiles ? t : m_tiles;
-    } else {
-      const int t = (r + kBK - 1) / kBK;
-      k_iters = t < k_iters ? t : k_iters;
-    }
-  }
-  const int total = m_tiles * g.n_tiles;
+  int m_tiles0, k_iters0, m_tiles1 = 0, k_iters1 = 0;
+  seg_extent<CG>(args.g0, m_tiles0, k_iters0);
+  if constexpr (S1::kPresent) seg_extent<CG>(args.g1, m_tiles1, k_iters1);
+  const int total0 = m_tiles0 * args.g0.n_tiles;
+  const int total = total0 + (S1::kPresent ? m_tiles1 * args.g1.n_tiles : 0);
+  int* const err_word = args.g0.err_word;
+  int* const sched = args.g0.sched;
+  const bool dynamic = sched != nullptr;
   volatile int* abort_flag = &ctl->abort;
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
@@ -275,15 +360,25 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-      mbar_init(smem_addr(&ctl->acc_empty[b]), EpiWarps<Epi>::value * CG);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), W * CG);
+    }
+    // readers of a schedule slot: the MMA thread and the epilogue warps of
+    // the even CTA, the producer and the epilogue warps of the odd one
+    for (int s = 0; s < kSchedSlots; ++s) {
+      mbar_init(smem_addr(&ctl->sched_full[s]), 1);
+      mbar_init(smem_addr(&ctl->sched_empty[s]), CG * (1 + W));
     }
     mbar_init(smem_addr(&ctl->mma_done), 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&args.a0);
+    tma_prefetch_desc(&args.b0);
+    if constexpr (S1::kPresent) {
+      tma_prefetch_desc(&args.a1);
+      tma_prefetch_desc(&args.b1);
+    }
   }
   if (warp == 1) {
     if constexpr (CG == 1) {
@@ -302,6 +397,48 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   }
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
+  const int pdl = args.g0.pdl;
+  if (pdl != 0 && threadIdx.x == 0) grid_launch_dependents();
+
+  // ---- the tile sequence
+  // Static: iteration it takes tile unit0 + it * units. Dynamic: the even
+  // CTA's producer draws tickets from `sched` and publishes each (or -1 once
+  // they run out) in slot it % kSchedSlots of both CTAs; every other role
+  // reads the slot and releases it on the even CTA's sched_empty barrier.
+  auto slot_of = [](int it) { return it % kSchedSlots; };
+  auto phase_of = [](int it) { return static_cast<uint32_t>(it / kSchedSlots) & 1u; };
+  auto sched_ack = [&](int slot) {
+    const uint32_t bar = smem_addr(&ctl->sched_empty[slot]);
+    if constexpr (CG == 2)
+      mbar_arrive_cluster(map_to_rank(bar, 0));
+    else
+      mbar_arrive(bar);
+  };
+  // Reader side of iteration it: the tile index (-1: none left); false when
+  // the wait gave up.
+  auto sched_read = [&](int it, int& u) -> bool {
+    const int slot = slot_of(it);
+    if (!wait_bar<CG>(smem_addr(&ctl->sched_full[slot]), phase_of(it), abort_flag, err_word))
+      return false;
+    u = *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]);
+    sched_ack(slot);
+    return true;
+  };
+  // Fetcher side: publish u in slot it % kSchedSlots of both CTAs.
+  auto sched_publish = [&](int it, int u) {
+    const int slot = slot_of(it);
+    const uint32_t tile_addr = smem_addr(&ctl->sched_tile[slot]);
+    const uint32_t bar = smem_addr(&ctl->sched_full[slot]);
+    if constexpr (CG == 2) {
+      st_shared_cluster(map_to_rank(tile_addr, 0), u);
+      st_shared_cluster(map_to_rank(tile_addr, 1), u);
+      mbar_arrive_cluster(map_to_rank(bar, 0));  // release: the stores come first
+      mbar_arrive_cluster(map_to_rank(bar, 1));
+    } else {
+      *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]) = u;
+      mbar_arrive(bar);
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -311,23 +448,24 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       uint32_t armed = 0;       // bit s: stage s has been loaded at least once
       uint32_t last_phase = 0;  // bit s: phase of the last load into stage s
       bool ok = true;
-      for (int u = unit0; u < total && ok; u += units) {
+      // loads of one tile of segment S (tile index ul within the segment)
+      auto produce = [&](auto seg, const CUtensorMap* ta, const CUtensorMap* tb,
+                         const GemmGeom& g, int m_tiles, int k_iters, int ul) -> bool {
+        using S = decltype(seg);
         int m, n;
-        tile_coords(g, m_tiles, u, m, n);
+        tile_coords(g, m_tiles, ul, m, n);
         for (int k = 0; k < k_iters; ++k) {
-          if (!wait_bar<CG>(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, g.err_word)) {
-            ok = false;
-            break;
-          }
+          if (!wait_bar<CG>(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, err_word))
+            return false;
           const uint32_t full_local = smem_addr(&ctl->full[stage]);
           uint32_t full = full_local;
           if constexpr (CG == 2) full = map_to_rank(full_local, 0);
           if (leader) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
-          load_operand<CG, A_MN, kBM>(stage_a(stage), &tm_a, full,
-                                      g.a_mn0 + m * Cfg::kTileRows + static_cast<int>(rank) * kBM,
-                                      g.a_k0 + k * kBK);
-          load_operand<CG, B_MN, Cfg::kBNLoad>(
-              stage_b(stage), &tm_b, full,
+          load_operand<CG, S::A_MN, kBM>(stage_a(stage), ta, full,
+                                         g.a_mn0 + m * Cfg::kTileRows + static_cast<int>(rank) * kBM,
+                                         g.a_k0 + k * kBK);
+          load_operand<CG, S::B_MN, Cfg::kBNLoad>(
+              stage_b(stage), tb, full,
               g.b_mn0 + n * kBN + static_cast<int>(rank) * Cfg::kBNLoad, g.b_k0 + k * kBK);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -336,6 +474,38 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
             phase ^= 1u;
           }
         }
+        return true;
+      };
+      if (pdl & kPdlWaitLoads) grid_dependency_wait();
+      // the fetcher keeps one ticket in flight: it is drawn while the
+      // current tile's loads are issued
+      int ticket = (dynamic && leader) ? atomicAdd(sched, 1) : 0;
+      for (int it = 0; ok; ++it) {
+        int u;
+        if (!dynamic) {
+          u = unit0 + it * units;
+          if (u >= total) break;
+        } else if (leader) {
+          if (!wait_bar<CG>(smem_addr(&ctl->sched_empty[slot_of(it)]), phase_of(it) ^ 1u,
+                            abort_flag, err_word)) {
+            ok = false;
+            break;
+          }
+          u = ticket < total ? ticket : -1;
+          if (u >= 0) ticket = atomicAdd(sched, 1);
+          sched_publish(it, u);
+          if (u < 0) break;
+        } else {
+          if (!sched_read(it, u)) {
+            ok = false;
+            break;
+          }
+          if (u < 0) break;
+        }
+        if (!S1::kPresent || u < total0)
+          ok = produce(S0{}, &args.a0, &args.b0, args.g0, m_tiles0, k_iters0, u);
+        else
+          ok = produce(S1{}, &args.a1, &args.b1, args.g1, m_tiles1, k_iters1, u - total0);
       }
       if (!ok && leader) {
         // let every copy already issued land before the CTAs exit
@@ -347,36 +517,28 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc =
-          idesc_f16kind_f32(kBM * CG, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0, Epi::kABFormat);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int it = 0;
-      for (int u = unit0; u < total && ok; u += units, ++it) {
-        const int buf = it & 1;
-        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-        if (!wait_bar<CG>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, g.err_word)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
+      // the MMAs of one tile of segment S into accumulator d_tmem
+      auto mma = [&](auto seg, int k_iters, uint32_t d_tmem) -> bool {
+        using S = decltype(seg);
+        constexpr uint32_t idesc =
+            idesc_f16kind_f32(kBM * CG, kBN, S::A_MN ? 1 : 0, S::B_MN ? 1 : 0, E0::kABFormat);
         for (int k = 0; k < k_iters; ++k) {
-          if (!wait_bar<CG>(smem_addr(&ctl->full[stage]), phase, abort_flag, g.err_word)) {
-            ok = false;
-            break;
-          }
+          if (!wait_bar<CG>(smem_addr(&ctl->full[stage]), phase, abort_flag, err_word))
+            return false;
           tc_fence_after_sync();
           const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
 #pragma unroll
           for (int kk = 0; kk < kBK / kUK; ++kk) {
             const uint32_t acc = (k | kk) != 0 ? 1u : 0u;
             if constexpr (CG == 1)
-              umma_bf16(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc, acc);
+              umma_bf16(d_tmem, operand_desc<S::A_MN>(a0, kk), operand_desc<S::B_MN>(b0, kk),
+                        idesc, acc);
             else
-              umma_bf16_pair(d_tmem, operand_desc<A_MN>(a0, kk), operand_desc<B_MN>(b0, kk), idesc,
-                             acc);
+              umma_bf16_pair(d_tmem, operand_desc<S::A_MN>(a0, kk),
+                             operand_desc<S::B_MN>(b0, kk), idesc, acc);
           }
           if constexpr (CG == 1)
             umma_commit(smem_addr(&ctl->empty[stage]));
@@ -387,6 +549,32 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
             phase ^= 1u;
           }
         }
+        return true;
+      };
+      for (int it = 0; ok; ++it) {
+        int u;
+        if (!dynamic) {
+          u = unit0 + it * units;
+          if (u >= total) break;
+        } else {
+          if (!sched_read(it, u)) {
+            ok = false;
+            break;
+          }
+          if (u < 0) break;
+        }
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!wait_bar<CG>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, err_word)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
+        if (!S1::kPresent || u < total0)
+          ok = mma(S0{}, k_iters0, d_tmem);
+        else
+          ok = mma(S1{}, k_iters1, d_tmem);
         if (!ok) break;
         if constexpr (CG == 1)
           umma_commit(smem_addr(&ctl->acc_full[buf]));
@@ -410,19 +598,40 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc_empty_leader = smem_addr(&ctl->acc_empty[0]);
     if constexpr (CG == 2) acc_empty_leader = map_to_rank(acc_empty_leader, 0);
-    int it = 0;
-    for (int u = unit0; u < total; u += units, ++it) {
+    if (pdl & kPdlWaitEpilogue) grid_dependency_wait();
+    for (int it = 0;; ++it) {
+      int u;
+      if (!dynamic) {
+        u = unit0 + it * units;
+        if (u >= total) break;
+      } else {
+        // one lane per warp reads the slot; the warps decide together
+        int uu = -1;
+        bool got_s = true;
+        if (lane == 0) got_s = sched_read(it, uu);
+        got_s = __shfl_sync(0xffffffffu, got_s ? 1 : 0, 0) != 0;
+        uu = __shfl_sync(0xffffffffu, uu, 0);
+        if (!epi_all<32 * W>(got_s)) break;
+        u = uu;
+        if (u < 0) break;
+      }
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-      const bool got = wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, g.err_word);
-      if (!epi_all<32 * EpiWarps<Epi>::value>(got)) break;
+      const bool got = wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, err_word);
+      if (!epi_all<32 * W>(got)) break;
       tc_fence_after_sync();
-      int m, n;
-      tile_coords(g, m_tiles, u, m, n);
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
-      Epi::tile(ep, m * CG + static_cast<int>(rank), n, taddr, k_iters == 0, row_in_tile,
-                quarter, part, lane, ctl);
+      int m, n;
+      if (!S1::kPresent || u < total0) {
+        tile_coords(args.g0, m_tiles0, u, m, n);
+        E0::tile(args.ep0, m * CG + static_cast<int>(rank), n, taddr, k_iters0 == 0, row_in_tile,
+                 quarter, part, lane, ctl);
+      } else {
+        tile_coords(args.g1, m_tiles1, u - total0, m, n);
+        E1::tile(args.ep1, m * CG + static_cast<int>(rank), n, taddr, k_iters1 == 0, row_in_tile,
+                 quarter, part, lane, ctl);
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {

@@ -119,6 +119,19 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch. launch_dependents lets the next kernel of
+// the stream, if it was launched with programmatic stream serialization,
+// start once every CTA of this grid has issued it or exited; wait blocks
+// until the grids this one depends on have completed and their memory is
+// visible (it returns at once in a grid launched without the attribute).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -73,6 +73,17 @@ def test_roofline_tensor_peak_follows_the_timed_region():
     assert short["achieved"] == long["achieved"]
 
 
+def test_roofline_fused_gradient_role_counts_both_contractions():
+    """bwd_grads runs grad_hidden and grad_weight of a chunk in one launch:
+    4 n h v flops per step, split over its launches."""
+    b = _bench()
+    n, h, v, steps = 8028, 4096, 128256, 10
+    r = b.roofline_entry("bwd_grads", 5 * steps, 5 * steps * 2.0, steps, n, h, v, 500.0,
+                         PEAKS, "measured", 152)
+    assert r["flops_per_launch"] == 4.0 * n * h * v / 5
+    assert abs(r["achieved"] - 4.0 * n * h * v / 5 / 2.0e-3 / 1e12) < 0.1
+
+
 def test_roofline_fp32_roles_use_the_fma_peak():
     """The fp32 (FFMA) roles are ALU-bound: the peak is SMs x 128 lanes x 2 flops
     x the maximum SM clock, whatever the length of the timed region."""

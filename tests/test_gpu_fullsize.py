@@ -27,7 +27,20 @@ from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS, Workload, make
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-BWD_CHUNK_BF16_BUDGET = 512 << 20  # default dlogits chunk budget of the library
+
+
+def default_chunk(n, v, elem=2, budget=512 << 20):
+    """The library's default backward chunk width (include/flce.h, vocab_chunk):
+    at least five equal chunks of whole 256-column tiles, each at least 2048
+    wide, more while a chunk's n x width buffer exceeds 512 MiB. Used only to
+    place sampled vocabulary rows at chunk boundaries."""
+    v_round = -(-v // 256) * 256
+    nch = max(-(-(max(n, 1) * elem * v_round) // budget), min(5, v_round // 2048), 1)
+    width = -(-(-(-v // nch)) // 256) * 256
+    while width > 256 and width * max(n, 1) * elem > budget:
+        nch += 1
+        width = -(-(-(-v // nch)) // 256) * 256
+    return min(width, v_round)
 
 
 def _sample_rows(w, targets, peaked, k=512, seed=11):
@@ -49,7 +62,7 @@ def _sample_rows(w, targets, peaked, k=512, seed=11):
 def _sample_vocab(w, targets, rows, peaked, k=256, seed=12):
     v = w.v
     g = torch.Generator().manual_seed(seed)
-    chunk = max(256, (BWD_CHUNK_BF16_BUDGET // (w.n * 2)) // 256 * 256)
+    chunk = default_chunk(w.n, v)
     picks = [0, 1, v - 1, v - 2, 255, 256, 257]
     c = chunk
     while c < v:
@@ -166,22 +179,27 @@ def test_fullsize_kl_parity():
     assert bool((col <= 1e-2 * mag + 1e-12).all()), float((col / mag).max())
 
 
-@pytest.mark.parametrize("kl", [False, True])
-def test_peak_memory_below_logits(kl):
-    """One forward+backward through the public autograd API at the Llama-3
-    head shape allocates, above what is live before it (inputs, and the
-    teacher probabilities for KL), less than the N x V logit matrix would
-    take in bf16 (N*V*2 bytes): the logits are never materialised. The
-    incremental peak includes grad_weight [V, H], grad_hidden and the
-    workspaces."""
+@pytest.mark.parametrize("name,kl", [("llama3_head_bf16", False), ("llama3_head_bf16", True),
+                                     ("mid_bf16", False), ("softcap_bf16", False),
+                                     ("long_bf16", False)])
+def test_peak_memory_below_logits(name, kl):
+    """One forward+backward through the public autograd API, with the
+    workload's options and the library's default chunking, allocates above
+    what is live before it (inputs, and the teacher probabilities for KL)
+    less than the N x V logit matrix would take in bf16 (N*V*2 bytes): the
+    logits are never materialised. The incremental peak includes grad_weight
+    [V, H], grad_hidden, grad_bias and the workspaces. At the mid shape
+    grad_weight alone is half of N*V*2, so this also pins the default
+    chunking's fifth-of-the-vocabulary bound."""
     from linear_cross_entropy_vocab_gb300 import fused_linear_cross_entropy, fused_linear_kl_div
     from linear_cross_entropy_vocab_gb300.workloads import make_teacher_probs
 
-    w = WORKLOADS["llama3_head_bf16"]
+    w = WORKLOADS[name]
     x = to_dev(make_inputs(w))
     q = make_teacher_probs(w).cuda() if kl else None
     h = x["hidden"].detach().requires_grad_(True)
     wt = x["weight"].detach().requires_grad_(True)
+    b = None if x["bias"] is None else x["bias"].detach().requires_grad_(True)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     base = torch.cuda.memory_allocated()
@@ -189,7 +207,8 @@ def test_peak_memory_below_logits(kl):
     if kl:
         loss = fused_linear_kl_div(h, wt, q, x["targets"])
     else:
-        loss = fused_linear_cross_entropy(h, wt, x["targets"])
+        loss = fused_linear_cross_entropy(h, wt, x["targets"], b, w.ignore_index, w.logit_scale,
+                                          w.softcap, w.reduction)
     loss.backward()
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated() - base
