@@ -675,8 +675,9 @@ def measure_config(w, dev, steps, warmup, peaks, peak_src, forward_only=False, k
         "clocks": {"sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons"),
                    "samples": clk.get("samples")},
         "memory": {"peak_incremental_bytes_public_api": int(peak_incr),
-                   "nxv_bf16_bytes": n * v * 2,
-                   "of_nxv_bf16": round(peak_incr / (n * v * 2), 4)},
+                   "nxv_bytes": n * v * x["hidden"].element_size(),
+                   "of_nxv": round(peak_incr / (n * v * x["hidden"].element_size()), 4),
+                   "nxv": "one N x V logit matrix in the input type"},
     }
     if alu:
         mhz = peaks.get("sm_max_mhz", 2070.0)

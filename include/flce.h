@@ -95,9 +95,9 @@ typedef enum flce_reduction {
  *   grad_weight_dtype  dtype of grad_weight: FLCE_F32, or equal to dtype
  *   vocab_chunk        backward vocabulary chunk width; 0 picks the default:
  *                      equal chunks of whole 256-column tiles, at least five
- *                      of them (each at least 2048 columns wide; fewer for a
- *                      narrower vocabulary), more where an N x chunk dlogits
- *                      buffer would exceed 512 MiB. The buffer is the largest
+ *                      of them (one per tile for a vocabulary of fewer than
+ *                      five tiles), more where an N x chunk dlogits buffer
+ *                      would exceed 512 MiB. The buffer is the largest
  *                      workspace item, so a smaller chunk lowers peak memory
  *                      at some cost in speed. Rounded up to a multiple of 256
  *   flags              OR of FLCE_SKIP_IGNORED_ROWS; 0 for none

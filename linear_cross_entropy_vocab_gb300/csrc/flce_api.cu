@@ -89,10 +89,12 @@ thread_local CUtensorMapDataType g_map_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
 // 2-D tensor of 16-bit elements (of type g_map_type: the input type of the
 // current call) [outer][inner] with row pitch `pitch_elems`, box
-// {box_inner, box_outer}, 128-byte swizzle, zero fill out of bounds.
+// {box_inner, box_outer}, 128-byte swizzle (the GEMM operands) or none (the
+// epilogues' stores), zero fill out of bounds.
 // On failure records the driver's result in the thread's error text.
 bool make_map(CUtensorMap* map, const char* what, const void* base, int64_t inner,
-              int64_t outer, int64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+              int64_t outer, int64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
+              bool swizzle = true) {
   EncodeFn enc = encoder();
   if (!enc) {
     fail(FLCE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -104,7 +106,8 @@ bool make_map(CUtensorMap* map, const char* what, const void* base, int64_t inne
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
       enc(map, g_map_type, 2, const_cast<void*>(base), dims, strides, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     fail(FLCE_ERR_CUDA,
@@ -172,15 +175,13 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Default backward vocabulary chunking: the dlogits buffer D of one chunk is
 // at most 512 MiB and spans at most about a fifth of the vocabulary (V/5
-// rounded up to whole 256-column tiles), so that together with grad_weight
-// (V x H), grad_hidden and its fp32 accumulator the backward stays below
-// the N x V logits of a plain implementation even where H is half of N (the
-// 4096-token, 2048-wide, 32000-word head: peak 0.96 x N V 2 bytes). Chunks
-// narrower than 2048 columns are not made for the sake of the fifth: small
-// vocabularies keep fewer, wider chunks.
+// rounded up to whole 256-column tiles; a vocabulary of fewer than five tiles
+// gets one chunk per tile), so that together with grad_weight (V x H),
+// grad_hidden and its fp32 accumulator the backward stays below the N x V
+// logits of a plain implementation even where H is half of N (the
+// 4096-token, 2048-wide, 32000-word head: peak 0.96 x N V 2 bytes).
 constexpr int64_t kDefaultDlogitsBudget = int64_t(512) << 20;  // bytes of one dlogits chunk
 constexpr int64_t kMinDefaultChunks = 5;
-constexpr int64_t kMinDefaultChunkWidth = 2048;
 
 // Tile bands (GemmGeom::group) of the row-tile-fastest GEMMs. With bands of
 // 16 pair row tiles (4096 rows) the forward and dlogits kernels re-read
@@ -188,6 +189,16 @@ constexpr int64_t kMinDefaultChunkWidth = 2048;
 // 6.5 -> 2.7-4.2 GB, dlogits 7.0 -> 3.1-3.4 GB per step); grad_hidden does
 // best with 8 (19.7 -> 11.6-13.5 GB). grad_weight is fastest along H and is
 // left unbanded (banding it raised its reads).
+// Tile order of the forward GEMM and of the dlogits GEMMs: dynamic (drawn
+// from a device counter, as the gradient launches always are) or static.
+// Static order lets pairs drift apart in the tile sequence, which widens the
+// window of weight tiles in flight; with dynamic order the forward read W
+// exactly twice (2.17 GB per launch at the Llama-3 head shape, against
+// 2.9-3.1 GB static on the same box), within 0.4 % of the static time. The
+// dlogits launches gain less (0.59 -> 0.52 GB) and cost more at the
+// 2048-wide head (+2 %), so they stay static.
+constexpr bool kDynamicForward = true;
+constexpr bool kDynamicDlogits = false;
 constexpr int kBandForward = 16;
 constexpr int kBandDlogits = 16;
 constexpr int kBandGradHidden = 8;
@@ -201,7 +212,7 @@ struct CompactPlan {
 
 struct FwdPlan {
   int64_t n_vt = 0;
-  size_t partials = 0, zsum = 0, zt = 0, correct = 0, entropy = 0, total = 0;
+  size_t partials = 0, zsum = 0, zt = 0, correct = 0, entropy = 0, sched = 0, total = 0;
   bool has_zsum = false;
   CompactPlan cp;
 };
@@ -304,6 +315,8 @@ FwdPlan plan_forward(const flce_problem* p) {
   off = align_up(off + static_cast<size_t>(p->n) * 4);
   f.entropy = off;
   off = align_up(off + static_cast<size_t>(p->n) * 4);
+  f.sched = off;  // tile counter of the forward GEMM
+  if (is_tc(p)) off = align_up(off + sizeof(int));
   off = plan_compaction(p, false, false, off, &f.cp);
   f.total = off;
   return f;
@@ -317,14 +330,13 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   if (c > 0) {
     c = cdiv(c, 256) * 256;
   } else {
-    // balanced chunks: at least kMinDefaultChunks (while each stays at least
-    // kMinDefaultChunkWidth wide), more when one would exceed the budget
+    // balanced chunks: at least kMinDefaultChunks (at most one per tile),
+    // more when one would exceed the budget
     const int64_t rows = p->n > 0 ? p->n : 1;
     int64_t nch = cdiv(rows * elem * v_round, kDefaultDlogitsBudget);
-    const int64_t wide_enough = v_round / kMinDefaultChunkWidth;
-    const int64_t floor_chunks = wide_enough < kMinDefaultChunks ? wide_enough : kMinDefaultChunks;
+    const int64_t tiles = v_round / 256;
+    const int64_t floor_chunks = tiles < kMinDefaultChunks ? tiles : kMinDefaultChunks;
     if (nch < floor_chunks) nch = floor_chunks;
-    if (nch < 1) nch = 1;
     c = cdiv(cdiv(p->v, nch), 256) * 256;
     while (c > 256 && c * rows * elem > kDefaultDlogitsBudget) {
       ++nch;
@@ -345,11 +357,11 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   if (p->has_bias) off = align_up(off + static_cast<size_t>(b.gb_parts) * p->v * 4);
   b.scales = off;
   if (p->dtype == FLCE_F16) off = align_up(off + 2 * sizeof(float));
-  // tile counters of the dynamically scheduled gradient launches, one per
-  // chunk, zeroed at the start of every backward call
+  // tile counters of the dynamically scheduled launches, two per chunk
+  // (dlogits, gradients), zeroed at the start of every backward call
   b.sched = off;
   if (is_tc(p)) {
-    b.sched_bytes = align_up(static_cast<size_t>(b.n_chunks) * sizeof(int));
+    b.sched_bytes = align_up(static_cast<size_t>(2 * b.n_chunks) * sizeof(int));
     off += b.sched_bytes;
   }
   off = plan_compaction(p, true, kl, off, &b.cp);
@@ -486,7 +498,7 @@ flce_status check_kl_problem(const flce_kl_problem* k, flce_problem* ce) {
 
 struct KLFwdPlan {
   int64_t n_vt = 0;
-  size_t partials = 0, total = 0;
+  size_t partials = 0, sched = 0, total = 0;
   CompactPlan cp;
 };
 
@@ -494,6 +506,8 @@ KLFwdPlan plan_kl_forward(const flce_problem* ce) {
   KLFwdPlan f;
   f.n_vt = cdiv(ce->v, is_tc(ce) ? flce::kBN : flce::kSimtTileV);
   size_t off = align_up(static_cast<size_t>(ce->n) * f.n_vt * 16);
+  f.sched = off;  // tile counter of the forward GEMM
+  if (is_tc(ce)) off = align_up(off + sizeof(int));
   off = plan_compaction(ce, false, true, off, &f.cp);
   f.total = off;
   return f;
@@ -628,9 +642,10 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
     for (int64_t c = 0; c < plan.n_chunks; ++c) {
       const int64_t c0 = c * plan.chunk;
       const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
-      CUtensorMap tm_d_k, tm_d_mn;
+      CUtensorMap tm_d_k, tm_d_mn, tm_d_st;
       if (!make_map(&tm_d_k, "dlogits", dbuf, width, p->n, plan.chunk, flce::kBK, flce::kBM) ||
-          !make_map(&tm_d_mn, "dlogits^T", dbuf, width, p->n, plan.chunk, 64, flce::kBK))
+          !make_map(&tm_d_mn, "dlogits^T", dbuf, width, p->n, plan.chunk, 64, flce::kBK) ||
+          !make_map(&tm_d_st, "dlogits store", dbuf, width, p->n, plan.chunk, 32, 32, false))
         return FLCE_ERR_CUDA;
 
       // 1. recompute the chunk's logits and form D
@@ -651,8 +666,10 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       // thus completes after its predecessor, so the fp32 grad_hidden
       // accumulator is updated one chunk after another.
       g1.pdl = flce::kPdlWaitEpilogue;
+      if (kDynamicDlogits) g1.sched = sched + plan.n_chunks + c;
       if (kl != nullptr) {
         flce::DlogitsKLParams dp{};
+        dp.d_map = tm_d_st;
         dp.bias = bias;
         dp.q = kl->q;
         dp.q_vec = (p->v % 8 == 0 && aligned(kl->q, 16)) ? 1 : 0;
@@ -662,8 +679,6 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
         dp.qsum = rows_qsum;
         dp.grad_out = rows_grad;
         dp.n_counted = n_valid;
-        dp.d = dbuf;
-        dp.ldd = plan.chunk;
         dp.dscale = scales;
         dp.gb_partial = gb_partial;
         dp.gb_ld = p->v;
@@ -680,13 +695,12 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
                                        flce::dlogits_epi_warps(p->h), dev.sms, s);
       } else {
         flce::DlogitsParams dp{};
+        dp.d_map = tm_d_st;
         dp.bias = bias;
         dp.targets = rows_targets;
         dp.lse = rows_lse;
         dp.grad_out = rows_grad;
         dp.n_valid = n_valid;
-        dp.d = dbuf;
-        dp.ldd = plan.chunk;
         dp.dscale = scales;
         dp.gb_partial = gb_partial;
         dp.gb_ld = p->v;
@@ -1052,6 +1066,11 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       g.dyn_rows = n_kept;
       g.dyn_axis = 0;
       g.err_word = err_word;
+      if (kDynamicForward) {
+        g.sched = reinterpret_cast<int*>(ws + plan.sched);
+        e = cudaMemsetAsync(g.sched, 0, sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (tile counter)");
+      }
       flce::FwdStatsParams fp{};
       fp.bias = bias;
       fp.targets = rows_targets;
@@ -1237,6 +1256,11 @@ flce_status flce_kl_forward(const flce_kl_problem* k, const void* hidden, const 
       g.dyn_rows = n_kept;
       g.dyn_axis = 0;
       g.err_word = err_word;
+      if (kDynamicForward) {
+        g.sched = reinterpret_cast<int*>(ws + plan.sched);
+        e = cudaMemsetAsync(g.sched, 0, sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (tile counter)");
+      }
       flce::FwdKLParams fp{};
       fp.bias = bias;
       fp.q = target_probs;

@@ -44,14 +44,17 @@ struct FwdStatsParams {
   LogitXform xf;
 };
 
+// Bytes of one epilogue warp's staging buffer for the D tensor stores: a
+// 32 x 32 box of 16-bit values.
+constexpr int kDlogitsStageBytes = 32 * 32 * 2;
+
 struct DlogitsParams {
+  CUtensorMap d_map;  // D of the chunk [N][width] (pitch ldd), box {32, 32}, for the stores
   const void* bias;
   const int64_t* targets;
   const float* lse;
   const float* grad_out;
   const int32_t* n_valid;
-  void* d;  // [N][ldd] dlogits of this chunk, input type, times *dscale
-  int64_t ldd;
   const float* dscale;  // device scalar multiplying the stored D, or null (1)
   float* gb_partial;  // [m_tiles][gb_ld] or null
   int64_t gb_ld;
@@ -85,6 +88,7 @@ struct FwdKLParams {
 };
 
 struct DlogitsKLParams {
+  CUtensorMap d_map;  // as in DlogitsParams
   const void* bias;
   const void* q;
   int q_vec;
@@ -94,8 +98,6 @@ struct DlogitsKLParams {
   const float* qsum;
   const float* grad_out;      // scalar, or per (compacted) row for reduction none
   const int32_t* n_counted;
-  void* d;
-  int64_t ldd;
   const float* dscale;
   float* gb_partial;
   int64_t gb_ld;

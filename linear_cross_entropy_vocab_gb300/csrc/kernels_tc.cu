@@ -212,16 +212,35 @@ struct RowChunk32 {
   }
 };
 
-// The tail every dlogits epilogue shares, per 32-column chunk `ch`: store
-// the 32 values of D (times dscale, rounded to T) for every buffer row (rows
-// past the present ones hold d = 0) and, when grad_bias partials are wanted,
-// leave this warp's 32 column sums of D over its 32 rows in ctl->red.
+// The tail every dlogits epilogue shares, per 32-column chunk `ch`: the 32
+// values of D of this warp's 32 rows (times dscale, rounded to T; rows past
+// the present ones hold d = 0) go through the warp's 2 KB staging buffer
+// (row-major, 64 bytes a row) to a tensor store of one 32 x 32 box at column
+// cb, row row0 of the chunk's buffer; the store leaves out rows past the
+// buffer and columns past the chunk. When grad_bias partials are wanted,
+// this warp's 32 column sums of D over its rows are left in ctl->red.
 template <typename T>
-__device__ __forceinline__ void emit_dlogits(float (&d)[32], int nv, int64_t row, int64_t buf_rows,
-                                             void* dbuf, int64_t ldd, int cb, float dscale,
-                                             bool bias_sums, int ch, int quarter, int lane,
-                                             GemmCtl* ctl) {
-  if (row < buf_rows) store32<T>(static_cast<T*>(dbuf) + row * ldd + cb, d, nv, dscale);
+__device__ __forceinline__ void emit_dlogits(float (&d)[32], const CUtensorMap* dmap,
+                                             int64_t row0, int64_t buf_rows, int cb,
+                                             float dscale, bool bias_sums, int ch, int quarter,
+                                             int part, int lane, GemmCtl* ctl) {
+  uint8_t* buf = ctl->out_stage + (part * 4 + quarter) * kDlogitsStageBytes;
+  if (lane == 0) tma_store_wait_read();  // the warp's previous box has left the buffer
+  __syncwarp();
+  uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    dst[q] = make_uint4(Elem<T>::pack2(d[q * 8 + 0] * dscale, d[q * 8 + 1] * dscale),
+                        Elem<T>::pack2(d[q * 8 + 2] * dscale, d[q * 8 + 3] * dscale),
+                        Elem<T>::pack2(d[q * 8 + 4] * dscale, d[q * 8 + 5] * dscale),
+                        Elem<T>::pack2(d[q * 8 + 6] * dscale, d[q * 8 + 7] * dscale));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < buf_rows) {  // no box starts past the buffer's rows
+    tma_store_2d(dmap, smem_addr(buf), cb, static_cast<int32_t>(row0));
+    tma_store_commit();
+  }
   if (bias_sums) ctl->red[quarter][ch][lane] = transpose_reduce32(d, lane);
 }
 
@@ -316,6 +335,7 @@ template <typename T, int W = 4>
 struct EpiDlogits {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
+  static constexpr int kOutStageBytes = 8 * kDlogitsStageBytes;  // one buffer per warp (<= 8)
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
@@ -383,8 +403,8 @@ struct EpiDlogits {
 #pragma unroll
         for (int k = 0; k < 32; ++k) d[k] = d[k] * gs * p.xf.dz_du(z[k]);
       }
-      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, bias_sums, ch, quarter,
-                      lane, ctl);
+      emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows,
+                      cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
     }
     if (bias_sums)
       flush_bias_sums<W>(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, part,
@@ -457,6 +477,7 @@ template <typename T, int W = 4>
 struct EpiDlogitsKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
+  static constexpr int kOutStageBytes = 8 * kDlogitsStageBytes;
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsKLParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
@@ -513,8 +534,8 @@ struct EpiDlogitsKL {
           f2_unpack(f2_mul(pq, g2), d[k], d[k + 1]);
         }
       }
-      emit_dlogits<T>(d, nv, row, p.n_rows, p.d, p.ldd, cb, dscale, bias_sums, ch, quarter,
-                      lane, ctl);
+      emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows,
+                      cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
       cur = nxt;
     }
     if (bias_sums)
@@ -679,7 +700,7 @@ namespace {
 template <int CG, class S0, class S1>
 cudaError_t launch_gemm_args(const GemmArgs<S0, S1>& a, int sms, cudaStream_t stream) {
   auto kern = tc_gemm_kernel<CG, S0, S1>;
-  constexpr int smem = gemm_smem_bytes<CG>();
+  constexpr int smem = gemm_smem_bytes<CG, typename S0::Epi, typename S1::Epi>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

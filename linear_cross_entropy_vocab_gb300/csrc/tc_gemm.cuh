@@ -74,14 +74,29 @@ struct GemmCtl {
   uint64_t sched_full[kSchedSlots];   // slot holds a tile index (count 1: the fetching thread)
   uint64_t sched_empty[kSchedSlots];  // every reading role has taken it (even CTA's barriers)
   int sched_tile[kSchedSlots];        // tile index, or -1: no tiles left
+  uint8_t* out_stage;  // the epilogue's staging area for tensor stores (Epi::kOutStageBytes)
   uint32_t tmem_base;
   int abort;
   float red[4][kBN / 32][32];  // epilogue scratch: per-warp column sums, [quarter][chunk][lane]
 };
 
-template <int CG>
+// Shared memory an epilogue stages its tensor stores in: Epi::kOutStageBytes
+// where it declares them (a multiple of 1024), else none. The area follows
+// the stage ring, 1024-byte aligned.
+template <class Epi, class = void>
+struct OutStage {
+  static constexpr int bytes = 0;
+};
+template <class Epi>
+struct OutStage<Epi, std::void_t<decltype(Epi::kOutStageBytes)>> {
+  static constexpr int bytes = Epi::kOutStageBytes;
+};
+
+template <int CG, class E0, class E1>
 constexpr int gemm_smem_bytes() {
-  return TileCfg<CG>::kStages * TileCfg<CG>::kStageBytes + 1024 /* alignment slack */ +
+  constexpr int out = OutStage<E0>::bytes > OutStage<E1>::bytes ? OutStage<E0>::bytes
+                                                                 : OutStage<E1>::bytes;
+  return TileCfg<CG>::kStages * TileCfg<CG>::kStageBytes + 1024 /* alignment slack */ + out +
          ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
 }
 
@@ -333,7 +348,10 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes);
+  constexpr int kOut = OutStage<E0>::bytes > OutStage<E1>::bytes ? OutStage<E0>::bytes
+                                                                 : OutStage<E1>::bytes;
+  uint8_t* const out_stage = smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes;
+  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(out_stage + kOut);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int m_tiles0, k_iters0, m_tiles1 = 0, k_iters1 = 0;
@@ -369,6 +387,7 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
       mbar_init(smem_addr(&ctl->sched_empty[s]), CG * (1 + W));
     }
     mbar_init(smem_addr(&ctl->mma_done), 1);
+    ctl->out_stage = out_stage;
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -407,9 +426,11 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
   // reads the slot and releases it on the even CTA's sched_empty barrier.
   auto slot_of = [](int it) { return it % kSchedSlots; };
   auto phase_of = [](int it) { return static_cast<uint32_t>(it / kSchedSlots) & 1u; };
+  // the even CTA's readers release a slot with a CTA-scope arrive, the odd
+  // CTA's with a cluster-scope one on the even CTA's barrier
   auto sched_ack = [&](int slot) {
     const uint32_t bar = smem_addr(&ctl->sched_empty[slot]);
-    if constexpr (CG == 2)
+    if (CG == 2 && !leader)
       mbar_arrive_cluster(map_to_rank(bar, 0));
     else
       mbar_arrive(bar);
@@ -429,14 +450,11 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
     const int slot = slot_of(it);
     const uint32_t tile_addr = smem_addr(&ctl->sched_tile[slot]);
     const uint32_t bar = smem_addr(&ctl->sched_full[slot]);
+    *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]) = u;
+    mbar_arrive(bar);  // release (CTA scope): the store comes first
     if constexpr (CG == 2) {
-      st_shared_cluster(map_to_rank(tile_addr, 0), u);
       st_shared_cluster(map_to_rank(tile_addr, 1), u);
-      mbar_arrive_cluster(map_to_rank(bar, 0));  // release: the stores come first
-      mbar_arrive_cluster(map_to_rank(bar, 1));
-    } else {
-      *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]) = u;
-      mbar_arrive(bar);
+      mbar_arrive_cluster(map_to_rank(bar, 1));  // release (cluster scope) to the odd CTA
     }
   };
 
@@ -477,24 +495,39 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
         return true;
       };
       if (pdl & kPdlWaitLoads) grid_dependency_wait();
-      // the fetcher keeps one ticket in flight: it is drawn while the
-      // current tile's loads are issued
-      int ticket = (dynamic && leader) ? atomicAdd(sched, 1) : 0;
+      // Dynamic: the even CTA's producer publishes each tile index one tile
+      // ahead of its own loads, so that the odd CTA's producer knows it a
+      // whole tile before its copies are due; it keeps one ticket drawn
+      // ahead, drawn after the previous publication so that the release
+      // does not wait for the atomic.
+      int ticket = 0, cur = -1;
+      auto publish_next = [&](int it) -> bool {
+        if (!wait_bar<CG>(smem_addr(&ctl->sched_empty[slot_of(it)]), phase_of(it) ^ 1u,
+                          abort_flag, err_word))
+          return false;
+        const int u = ticket < total ? ticket : -1;
+        sched_publish(it, u);
+        if (u >= 0) ticket = atomicAdd(sched, 1);
+        return true;
+      };
+      if (dynamic && leader) {
+        ticket = atomicAdd(sched, 1);
+        ok = publish_next(0);
+        cur = *reinterpret_cast<volatile int*>(&ctl->sched_tile[0]);
+      }
       for (int it = 0; ok; ++it) {
         int u;
         if (!dynamic) {
           u = unit0 + it * units;
           if (u >= total) break;
         } else if (leader) {
-          if (!wait_bar<CG>(smem_addr(&ctl->sched_empty[slot_of(it)]), phase_of(it) ^ 1u,
-                            abort_flag, err_word)) {
+          u = cur;
+          if (u < 0) break;
+          if (!publish_next(it + 1)) {
             ok = false;
             break;
           }
-          u = ticket < total ? ticket : -1;
-          if (u >= 0) ticket = atomicAdd(sched, 1);
-          sched_publish(it, u);
-          if (u < 0) break;
+          cur = *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot_of(it + 1)]);
         } else {
           if (!sched_read(it, u)) {
             ok = false;
@@ -641,6 +674,11 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
         else
           mbar_arrive_cluster(bar);
       }
+    }
+    // an epilogue that stages tensor stores issues them from lane 0 of each
+    // warp: they complete before the CTA leaves
+    if constexpr (kOut > 0) {
+      if (lane == 0) tma_store_wait_all();
     }
   }
 

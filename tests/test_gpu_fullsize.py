@@ -31,11 +31,11 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 def default_chunk(n, v, elem=2, budget=512 << 20):
     """The library's default backward chunk width (include/flce.h, vocab_chunk):
-    at least five equal chunks of whole 256-column tiles, each at least 2048
-    wide, more while a chunk's n x width buffer exceeds 512 MiB. Used only to
-    place sampled vocabulary rows at chunk boundaries."""
+    at least five equal chunks of whole 256-column tiles (one per tile below
+    five tiles), more while a chunk's n x width buffer exceeds 512 MiB. Used
+    only to place sampled vocabulary rows at chunk boundaries."""
     v_round = -(-v // 256) * 256
-    nch = max(-(-(max(n, 1) * elem * v_round) // budget), min(5, v_round // 2048), 1)
+    nch = max(-(-(max(n, 1) * elem * v_round) // budget), min(5, v_round // 256))
     width = -(-(-(-v // nch)) // 256) * 256
     while width > 256 and width * max(n, 1) * elem > budget:
         nch += 1
