@@ -502,9 +502,13 @@ struct KLFwdPlan {
   CompactPlan cp;
 };
 
+// Per-row statistics entries of the KL forward: one per 256-column tile on
+// the tensor cores (two, per 128-column half, when it runs 8 epilogue warps),
+// one per kSimtTileV columns on the fp32 path.
 KLFwdPlan plan_kl_forward(const flce_problem* ce) {
   KLFwdPlan f;
-  f.n_vt = cdiv(ce->v, is_tc(ce) ? flce::kBN : flce::kSimtTileV);
+  f.n_vt = is_tc(ce) ? cdiv(ce->v, flce::kBN) * flce::kl_fwd_parts_per_tile(ce->h)
+                     : cdiv(ce->v, flce::kSimtTileV);
   size_t off = align_up(static_cast<size_t>(ce->n) * f.n_vt * 16);
   f.sched = off;  // tile counter of the forward GEMM
   if (is_tc(ce)) off = align_up(off + sizeof(int));
@@ -1274,7 +1278,8 @@ flce_status flce_kl_forward(const flce_kl_problem* k, const void* hidden, const 
       fp.eps = k->eps;
       fp.xf = xf;
       ProfScope ps("fwd_kl", s);
-      e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, dev.sms, s);
+      e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, flce::kl_fwd_epi_warps(p->h),
+                                 dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "KL forward kernel");
     } else {
       flce::SimtFwdParams fp{};

@@ -413,12 +413,16 @@ struct EpiDlogits {
 };
 
 // ------------------------------------------------------------ KL forward
-template <typename T>
+// W = 8: two warps per TMEM lane quarter, one per 128-column half, each with
+// its own statistics (partials per 128 columns), as in EpiFwdStats.
+template <typename T, int W = 4>
 struct EpiFwdKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  static constexpr int kEpiWarps = W;
+  static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = FwdKLParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*part*/,
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int part,
                               int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
@@ -427,20 +431,25 @@ struct EpiFwdKL {
     const int64_t orig = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
     const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v;
     const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
+    const int64_t slot = static_cast<int64_t>(n_tile) * (W / 4) + part;  // partials index
     RowStats st;
     st.init();
     float a_sum = 0.0f;  // sum q (log max(q, eps) - z)
     float q_sum = 0.0f;  // sum q
     const bool vec = p.q_vec != 0;
     RowChunk32<T> cur, nxt;
-    cur.issue(qrow, col0, p.v - col0 < 32 ? static_cast<int>(p.v - col0) : 32, vec, row_ok);
+    const int ch_end = (part + 1) * kChunks;
+    const int64_t c_first = col0 + part * kChunks * 32;
+    if (c_first < p.v)
+      cur.issue(qrow, c_first, p.v - c_first < 32 ? static_cast<int>(p.v - c_first) : 32, vec,
+                row_ok);
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = part * kChunks; ch < ch_end; ++ch) {
       const int64_t cb = col0 + ch * 32;
       if (cb >= p.v) break;
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
-      const int64_t cn = cb + 32;  // next chunk of this tile
-      if (ch + 1 < kBN / 32 && cn < p.v)
+      const int64_t cn = cb + 32;  // next chunk of this warp
+      if (ch + 1 < ch_end && cn < p.v)
         nxt.issue(qrow, cn, p.v - cn < 32 ? static_cast<int>(p.v - cn) : 32, vec, row_ok);
       float z[32], b[32];
       load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
@@ -467,7 +476,7 @@ struct EpiFwdKL {
       }
       cur = nxt;
     }
-    if (row_ok) p.partials[row * p.n_vt + n_tile] = make_float4(st.m, st.s, a_sum, q_sum);
+    if (row_ok) p.partials[row * p.n_vt + slot] = make_float4(st.m, st.s, a_sum, q_sum);
   }
 };
 
@@ -831,12 +840,19 @@ cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
 
 cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
                              const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                             const FwdKLParams& p, int sms, cudaStream_t s) {
-  if (type == kTcF16)
-    return launch_gemm<kPairCG, false, false, EpiFwdKL<__half>>(tm_hidden_k, tm_weight_k, g, p,
-                                                                 sms, s);
-  return launch_gemm<kPairCG, false, false, EpiFwdKL<__nv_bfloat16>>(tm_hidden_k, tm_weight_k,
-                                                                      g, p, sms, s);
+                             const FwdKLParams& p, int epi_warps, int sms, cudaStream_t s) {
+  const bool f16 = type == kTcF16;
+  if (epi_warps == 8)
+    return f16 ? launch_gemm<kPairCG, false, false, EpiFwdKL<__half, 8>>(tm_hidden_k,
+                                                                          tm_weight_k, g, p,
+                                                                          sms, s)
+               : launch_gemm<kPairCG, false, false, EpiFwdKL<__nv_bfloat16, 8>>(
+                     tm_hidden_k, tm_weight_k, g, p, sms, s);
+  return f16 ? launch_gemm<kPairCG, false, false, EpiFwdKL<__half>>(tm_hidden_k, tm_weight_k, g,
+                                                                     p, sms, s)
+             : launch_gemm<kPairCG, false, false, EpiFwdKL<__nv_bfloat16>>(tm_hidden_k,
+                                                                            tm_weight_k, g, p,
+                                                                            sms, s);
 }
 
 cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
