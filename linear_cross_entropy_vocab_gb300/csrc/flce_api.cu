@@ -300,9 +300,17 @@ flce_status check_problem(const flce_problem* p) {
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+// Per-row statistics entries of the forward: one per 256-column tile on the
+// tensor cores (two, per 128-column half, when the forward runs 8 epilogue
+// warps), one per kSimtTileV columns on the fp32 path.
+int64_t forward_parts(const flce_problem* p) {
+  if (!is_tc(p)) return cdiv(p->v, flce::kSimtTileV);
+  return cdiv(p->v, flce::kBN) * flce::fwd_parts_per_tile(p->h);
+}
+
 FwdPlan plan_forward(const flce_problem* p) {
   FwdPlan f;
-  f.n_vt = cdiv(p->v, is_tc(p) ? flce::kBN : flce::kSimtTileV);
+  f.n_vt = forward_parts(p);
   size_t off = 0;
   f.partials = off;
   off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 16);
@@ -502,13 +510,9 @@ struct KLFwdPlan {
   CompactPlan cp;
 };
 
-// Per-row statistics entries of the KL forward: one per 256-column tile on
-// the tensor cores (two, per 128-column half, when it runs 8 epilogue warps),
-// one per kSimtTileV columns on the fp32 path.
 KLFwdPlan plan_kl_forward(const flce_problem* ce) {
   KLFwdPlan f;
-  f.n_vt = is_tc(ce) ? cdiv(ce->v, flce::kBN) * flce::kl_fwd_parts_per_tile(ce->h)
-                     : cdiv(ce->v, flce::kSimtTileV);
+  f.n_vt = forward_parts(ce);
   size_t off = align_up(static_cast<size_t>(ce->n) * f.n_vt * 16);
   f.sched = off;  // tile counter of the forward GEMM
   if (is_tc(ce)) off = align_up(off + sizeof(int));
@@ -1090,7 +1094,8 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
                        ? 1 : 0;
       fp.xf = xf;
       ProfScope ps("fwd_stats", s);
-      e = flce::launch_tc_fwd_stats(tc_type(p), tm_h, tm_w, g, fp, dev.sms, s);
+      e = flce::launch_tc_fwd_stats(tc_type(p), tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h),
+                                    dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
     } else {
       flce::SimtFwdParams fp{};
@@ -1278,7 +1283,7 @@ flce_status flce_kl_forward(const flce_kl_problem* k, const void* hidden, const 
       fp.eps = k->eps;
       fp.xf = xf;
       ProfScope ps("fwd_kl", s);
-      e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, flce::kl_fwd_epi_warps(p->h),
+      e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h),
                                  dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "KL forward kernel");
     } else {

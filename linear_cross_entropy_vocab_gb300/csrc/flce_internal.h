@@ -136,8 +136,6 @@ struct AccRowsParams {
 };
 
 // ---------------------------------------------------------------- launchers
-// epi_warps (4 or 8): see kl_fwd_epi_warps; with 8 the forward statistics are
-// kept per 128 columns (kl_fwd_parts_per_tile entries per 256-column tile).
 cudaError_t launch_tc_fwd_kl(int type, const CUtensorMap& tm_hidden_k,
                              const CUtensorMap& tm_weight_k, const GemmGeom& g,
                              const FwdKLParams& p, int epi_warps, int sms, cudaStream_t s);
@@ -147,9 +145,11 @@ cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
                                  cudaStream_t s);
 
 // `type` is a TcType; every launcher runs the CTA-pair GEMM of that type.
+// epi_warps (4 or 8): epilogue warps of the forward GEMMs, see fwd_epi_warps;
+// with 8 the statistics are kept per 128 columns (fwd_parts_per_tile).
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                                const FwdStatsParams& p, int sms, cudaStream_t s);
+                                const FwdStatsParams& p, int epi_warps, int sms, cudaStream_t s);
 // epi_warps (4 or 8): epilogue warps of the dlogits GEMMs, see dlogits_epi_warps.
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
                               const CUtensorMap& tm_weight_k, const GemmGeom& g,
@@ -161,12 +161,14 @@ cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
 // warps per TMEM lane quarter keep the epilogue under the MMAs.
 constexpr int64_t kDlogitsEpi8MaxH = 2048;
 inline int dlogits_epi_warps(int64_t h) { return h <= kDlogitsEpi8MaxH ? 8 : 4; }
-// The KL forward follows the same rule (its epilogue also reads a teacher
-// row chunk per 32 columns); its per-row statistics are then kept per
-// 128-column half of a 256-column tile. The cross-entropy forward's lighter
-// epilogue keeps 4 warps (8 measured no faster at H = 2048).
-inline int kl_fwd_epi_warps(int64_t h) { return h <= kDlogitsEpi8MaxH ? 8 : 4; }
-inline int64_t kl_fwd_parts_per_tile(int64_t h) { return kl_fwd_epi_warps(h) / 4; }
+// The forward GEMMs of both losses follow the same rule; their per-row
+// statistics are then kept per 128-column half of a 256-column tile. It gains
+// the KL forward, whose epilogue also reads a teacher row chunk per 32
+// columns, and costs the cross-entropy forward nothing; one rule for both
+// keeps their folds identical, so that a one-hot teacher reproduces the
+// cross-entropy bitwise.
+inline int fwd_epi_warps(int64_t h) { return h <= kDlogitsEpi8MaxH ? 8 : 4; }
+inline int64_t fwd_parts_per_tile(int64_t h) { return fwd_epi_warps(h) / 4; }
 
 // Both gradient GEMMs of one vocabulary chunk in one launch, tiles drawn
 // from the device counter `sched` (zero before the launch):

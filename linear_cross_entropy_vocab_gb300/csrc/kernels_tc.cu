@@ -274,12 +274,17 @@ __device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld
 // METRICS: also fold what the metrics need (the argmax and the entropy sum);
 // without them the statistics are (m, s) only, and a and t stay at their
 // initial values (the per-row correctness and entropy are then not computed).
-template <typename T, bool METRICS = true>
+// W = 8: two warps per TMEM lane quarter, each folding one 128-column half
+// of the tile into its own statistics (partials per 128 columns; for short
+// contractions, where the epilogue would outlast the MMAs).
+template <typename T, bool METRICS = true, int W = 4>
 struct EpiFwdStats {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
+  static constexpr int kEpiWarps = W;
+  static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = FwdStatsParams;
   __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int /*part*/,
+                              bool acc_zero, int row_in_tile, int /*quarter*/, int part,
                               int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
@@ -287,13 +292,14 @@ struct EpiFwdStats {
     const bool row_ok = row < n_eff;
     const int64_t t = row_ok ? __ldg(p.targets + row) : INT64_MIN;
     const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
+    const int64_t slot = static_cast<int64_t>(n_tile) * (W / 4) + part;  // partials index
     RowStats st;
     st.init();
     float zt = 0.0f;
-    float zs = 0.0f;  // sum of this tile's logits (used for label smoothing)
+    float zs = 0.0f;  // sum of this part's logits (used for label smoothing)
     bool has_zt = false;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = part * kChunks; ch < (part + 1) * kChunks; ++ch) {
       const int64_t cb = col0 + ch * 32;
       if (cb >= p.v) break;
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
@@ -321,8 +327,8 @@ struct EpiFwdStats {
       }
     }
     if (row_ok) {
-      p.partials[row * p.n_vt + n_tile] = st.pack();
-      if (p.zsum != nullptr) p.zsum[row * p.n_vt + n_tile] = zs;
+      p.partials[row * p.n_vt + slot] = st.pack();
+      if (p.zsum != nullptr) p.zsum[row * p.n_vt + slot] = zs;
       if (has_zt) p.zt[row] = zt;
     }
   }
@@ -806,19 +812,28 @@ cudaError_t launch_grads_typed(const GradsLaunch& l, int sms, cudaStream_t s) {
 
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
-                                const FwdStatsParams& p, int sms, cudaStream_t s) {
-  if (p.metrics) {
-    if (type == kTcF16)
-      return launch_gemm<kPairCG, false, false, EpiFwdStats<__half, true>>(tm_hidden_k,
-                                                                          tm_weight_k, g, p, sms, s);
-    return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, true>>(
-        tm_hidden_k, tm_weight_k, g, p, sms, s);
+                                const FwdStatsParams& p, int epi_warps, int sms, cudaStream_t s) {
+  const bool f16 = type == kTcF16;
+  if (epi_warps == 8) {
+    if (p.metrics)
+      return f16 ? launch_gemm<kPairCG, false, false, EpiFwdStats<__half, true, 8>>(
+                       tm_hidden_k, tm_weight_k, g, p, sms, s)
+                 : launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, true, 8>>(
+                       tm_hidden_k, tm_weight_k, g, p, sms, s);
+    return f16 ? launch_gemm<kPairCG, false, false, EpiFwdStats<__half, false, 8>>(
+                     tm_hidden_k, tm_weight_k, g, p, sms, s)
+               : launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, false, 8>>(
+                     tm_hidden_k, tm_weight_k, g, p, sms, s);
   }
-  if (type == kTcF16)
-    return launch_gemm<kPairCG, false, false, EpiFwdStats<__half, false>>(tm_hidden_k,
-                                                                         tm_weight_k, g, p, sms, s);
-  return launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, false>>(
-      tm_hidden_k, tm_weight_k, g, p, sms, s);
+  if (p.metrics)
+    return f16 ? launch_gemm<kPairCG, false, false, EpiFwdStats<__half, true>>(
+                     tm_hidden_k, tm_weight_k, g, p, sms, s)
+               : launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, true>>(
+                     tm_hidden_k, tm_weight_k, g, p, sms, s);
+  return f16 ? launch_gemm<kPairCG, false, false, EpiFwdStats<__half, false>>(
+                   tm_hidden_k, tm_weight_k, g, p, sms, s)
+             : launch_gemm<kPairCG, false, false, EpiFwdStats<__nv_bfloat16, false>>(
+                   tm_hidden_k, tm_weight_k, g, p, sms, s);
 }
 
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
