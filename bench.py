@@ -527,7 +527,8 @@ def bench_ours(args, rank, world, dev):
         "config": {"workload": describe_kl(w) if args.kl else describe(w),
                    "global_batch": n * world, "seq_len": None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (weight 1.05 GB), no flush",
+                   "l2": (f"inputs {input_bytes(x) / 1e6:.0f} MB, L2 {L2_BYTES / 1e6:.0f} MB: "
+                          "no flush between steps"),
                    "skip_ignored_rows": not args.all_rows,
                    "vocab_chunk": args.vocab_chunk or "library default",
                    "step": "forward only" if args.forward_only else "forward+backward"},
@@ -578,6 +579,11 @@ L2_BYTES = 129 << 20
 PER_CONFIG_TIMED_S = 0.4  # device time per workload's timed region (at least `steps` steps)
 
 
+def input_bytes(x) -> int:
+    """Bytes of a step's input tensors (a dict of tensors or None)."""
+    return sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+
+
 def _flush_l2(buf):
     buf.add_(1)  # writes 2 x L2 of memory: nothing of the last step stays in L2
 
@@ -595,7 +601,7 @@ def measure_config(w, dev, steps, warmup, peaks, peak_src, forward_only=False, k
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     step = (KLStep if kl else Step)(x, w, dev, skip_ignored=True, forward_only=forward_only)
-    in_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+    in_bytes = input_bytes(x)
     flush = None
     if in_bytes < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
