@@ -325,6 +325,15 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// One 32-byte streaming (evict-first) global load; src must be 32-byte
+// aligned. The low 16 bytes land in lo, the high 16 in hi.
+__device__ __forceinline__ void ld_cs_32B(const uint4* src, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(src));
+}
+
 // Hardware base-2 exponential (MUFU), flushes subnormal results to zero.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
