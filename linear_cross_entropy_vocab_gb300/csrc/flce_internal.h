@@ -48,6 +48,12 @@ struct FwdStatsParams {
 // 32 x 32 box of 16-bit values.
 constexpr int kDlogitsStageBytes = 32 * 32 * 2;
 
+// The 4-warp forms of the epilogues with per-element arithmetic (both
+// forwards, both dlogits) run lane quarters 0 and 1 through the relay of the
+// GEMM kernel: their arithmetic then runs on the schedulers that do not issue
+// the TMA loads and the MMAs.
+constexpr bool kEpiRelay = true;
+
 struct DlogitsParams {
   CUtensorMap d_map;  // D of the chunk [N][width] (pitch ldd), box {32, 32}, for the stores
   const void* bias;

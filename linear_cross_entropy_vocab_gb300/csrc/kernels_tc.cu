@@ -264,7 +264,7 @@ __device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld
                                                 int c0, int col0, int width, int quarter,
                                                 int part, int lane, GemmCtl* ctl) {
   constexpr int kPer = (kBN / 32) / W;
-  named_bar_sync(1, 32 * W);
+  named_bar_sync(kEpiBar, 32 * W);
   const int first = (4 * part + quarter) * kPer;
 #pragma unroll
   for (int ch = first; ch < first + kPer; ++ch) {
@@ -290,10 +290,11 @@ template <typename T, bool METRICS = true, int W = 4>
 struct EpiFwdStats {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
+  static constexpr bool kRelay = kEpiRelay && W == 4;
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = FwdStatsParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int part,
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int /*quarter*/, int part,
                               int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
@@ -313,7 +314,7 @@ struct EpiFwdStats {
       if (cb >= p.v) break;
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
       float z[32], b[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       load_bias32<T>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
@@ -350,11 +351,12 @@ template <typename T, int W = 4>
 struct EpiDlogits {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
-  static constexpr int kOutStageBytes = 8 * kDlogitsStageBytes;  // one buffer per warp (<= 8)
+  static constexpr bool kRelay = kEpiRelay && W == 4;
+  static constexpr int kOutStageBytes = W * kDlogitsStageBytes;  // one buffer per warp
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int quarter, int part,
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int quarter, int part,
                               int lane, GemmCtl* ctl) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
@@ -380,7 +382,7 @@ struct EpiDlogits {
       if (cb >= p.width) break;
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
       float z[32], b[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       load_bias32<T>(p.bias, p.c0 + cb, nv, b);
       float d[32];
       p.xf.apply32(z, b);
@@ -434,10 +436,11 @@ template <typename T, int W = 4>
 struct EpiFwdKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
+  static constexpr bool kRelay = kEpiRelay && W == 4;
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = FwdKLParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int /*quarter*/, int part,
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int /*quarter*/, int part,
                               int /*lane*/,
                               GemmCtl* /*ctl*/) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
@@ -467,7 +470,7 @@ struct EpiFwdKL {
       if (ch + 1 < ch_end && cn < p.v)
         nxt.issue(qrow, cn, p.v - cn < 32 ? static_cast<int>(p.v - cn) : 32, vec, row_ok);
       float z[32], b[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       load_bias32<T>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
@@ -501,11 +504,12 @@ template <typename T, int W = 4>
 struct EpiDlogitsKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
-  static constexpr int kOutStageBytes = 8 * kDlogitsStageBytes;
+  static constexpr bool kRelay = kEpiRelay && W == 4;
+  static constexpr int kOutStageBytes = W * kDlogitsStageBytes;
   static constexpr int kChunks = (kBN / 32) * 4 / W;  // 32-column chunks per warp
   using Params = DlogitsKLParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int quarter, int part,
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int quarter, int part,
                               int lane, GemmCtl* ctl) {
     const int64_t n_eff = p.n_rows_dyn != nullptr ? *p.n_rows_dyn : p.n_rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
@@ -536,7 +540,7 @@ struct EpiDlogitsKL {
       if (ch + 1 < ch_end && cn < p.width)
         nxt.issue(qrow, cn, p.width - cn < 32 ? p.width - cn : 32, vec, row_ok);
       float z[32], b[32], q[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       load_bias32<T>(p.bias, p.c0 + cb, nv, b);
       cur.get(qrow, cb, nv, row_ok, q);
       float d[32];
@@ -573,8 +577,8 @@ template <typename T>
 struct EpiStoreRows {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = StoreRowsParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int, int, int, GemmCtl*) {
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int, int, int, GemmCtl*) {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < p.rows;
     const float scale = p.out_scale != nullptr ? *p.out_scale : 1.0f;
@@ -583,7 +587,7 @@ struct EpiStoreRows {
       const int cb = n_tile * kBN + ch * 32;
       if (cb >= p.cols) break;
       float z[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       if (!row_ok) continue;
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = (p.row0 + row) * p.ld + cb;
@@ -612,8 +616,8 @@ template <typename T>
 struct EpiAccRows {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   using Params = AccRowsParams;
-  __device__ static void tile(const Params& p, int m_tile, int n_tile, uint32_t taddr,
-                              bool acc_zero, int row_in_tile, int, int, int, GemmCtl*) {
+  __device__ static void tile(const Params& p, int m_tile, int n_tile, AccSrc& acc,
+                              int row_in_tile, int, int, int, GemmCtl*) {
     const int64_t n_eff = p.rows_dyn != nullptr ? *p.rows_dyn : p.rows;
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
@@ -626,7 +630,7 @@ struct EpiAccRows {
       const int cb = n_tile * kBN + ch * 32;
       if (cb >= p.cols) break;
       float z[32];
-      load_acc(taddr + static_cast<uint32_t>(ch * 32), z, acc_zero);
+      acc.load(ch, z);
       if (!row_ok) continue;
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = row * p.ld + cb;
@@ -725,6 +729,7 @@ template <int CG, class S0, class S1>
 cudaError_t launch_gemm_args(const GemmArgs<S0, S1>& a, int sms, cudaStream_t stream) {
   auto kern = tc_gemm_kernel<CG, S0, S1>;
   constexpr int smem = gemm_smem_bytes<CG, typename S0::Epi, typename S1::Epi>();
+  static_assert(smem <= 227 * 1024, "more shared memory than a CTA may have");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

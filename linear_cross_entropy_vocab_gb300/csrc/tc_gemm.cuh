@@ -19,6 +19,13 @@
 //            to the epilogue policy.
 // An epilogue may ask for 8 warps (320 threads): warps 2-9, two per TMEM lane
 // quarter, each pulling one 128-column half of its rows.
+// A 4-warp epilogue may ask for a relay (256 threads): a TMEM lane quarter can
+// only be read by warps of its own scheduler (warp id mod 4), and schedulers 0
+// and 1 also run the TMA and MMA threads, whose issue the epilogue's
+// arithmetic delays. So warps 4 and 5 (schedulers 0, 1) only copy quarters 0
+// and 1 from TMEM into shared memory, 32 columns at a time, and warps 6 and 7
+// (schedulers 2, 3) run the epilogue on those rows; warps 2 and 3 run it on
+// quarters 2 and 3 as before.
 // The 512 TMEM columns hold two 128 x 256 fp32 accumulators per CTA, so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 //
@@ -92,14 +99,6 @@ struct OutStage<Epi, std::void_t<decltype(Epi::kOutStageBytes)>> {
   static constexpr int bytes = Epi::kOutStageBytes;
 };
 
-template <int CG, class E0, class E1>
-constexpr int gemm_smem_bytes() {
-  constexpr int out = OutStage<E0>::bytes > OutStage<E1>::bytes ? OutStage<E0>::bytes
-                                                                 : OutStage<E1>::bytes;
-  return TileCfg<CG>::kStages * TileCfg<CG>::kStageBytes + 1024 /* alignment slack */ + out +
-         ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
-}
-
 // Tile grid and TMA coordinate offsets of one GEMM launch. m_tiles counts
 // tiles of TileCfg<CG>::kTileRows rows.
 struct GemmGeom {
@@ -162,16 +161,6 @@ __device__ __forceinline__ void tile_coords(const GemmGeom& g, int m_tiles, int 
   }
 }
 
-// 32 accumulator columns, or zeros when the contraction was empty (K = 0).
-__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[32], bool zero) {
-  if (zero) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-  } else {
-    tmem_load_32cols(taddr, v);
-  }
-}
-
 template <int CG, bool MN, int ROWS>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                              int mn0, int k0) {
@@ -202,10 +191,104 @@ template <class Epi>
 struct EpiWarps<Epi, std::void_t<decltype(Epi::kEpiWarps)>> {
   static constexpr int value = Epi::kEpiWarps;
 };
+// Whether Epi asks for the relay (Epi::kRelay; 4 epilogue warps only).
+template <class Epi, class = void>
+struct EpiRelay {
+  static constexpr bool value = false;
+};
+template <class Epi>
+struct EpiRelay<Epi, std::void_t<decltype(Epi::kRelay)>> {
+  static constexpr bool value = Epi::kRelay;
+};
+// Warps that run epilogue code: the epilogue's own, plus the two relay
+// readers.
+template <class Epi>
+__host__ __device__ constexpr int epi_phys_warps() {
+  return EpiWarps<Epi>::value + (EpiRelay<Epi>::value ? 2 : 0);
+}
 // Threads per CTA: the TMA warp, the MMA warp and the epilogue warps.
 template <class Epi>
 constexpr int gemm_threads() {
-  return 64 + 32 * EpiWarps<Epi>::value;
+  return 64 + 32 * epi_phys_warps<Epi>();
+}
+
+// ---- the relay (see the top of this file)
+// Per relayed quarter, two slots of 32 rows x 32 fp32 columns. Row r (the
+// lane) holds its 8 16-byte groups at r*128 + 16*(g ^ (r & 7)), so that the
+// 16-byte accesses of any 8 consecutive lanes fall in distinct banks.
+constexpr int kRelaySlotBytes = 32 * 32 * 4;
+constexpr int kRelayBytes = 2 /* quarters */ * 2 /* slots */ * kRelaySlotBytes;
+// Named barriers of the hand-off, per relayed quarter q: slot s full
+// kRelayBar + 4q + s, slot s empty kRelayBar + 4q + 2 + s (64 threads: the
+// reader warp and the computing warp). Barrier 1 is the epilogue-wide one.
+constexpr uint32_t kRelayBar = 2;
+
+__device__ __forceinline__ void relay_put(uint8_t* slot, int lane, const float (&v)[32]) {
+  float4* row = reinterpret_cast<float4*>(slot + lane * 128);
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    row[g ^ (lane & 7)] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+__device__ __forceinline__ void relay_get(const uint8_t* slot, int lane, float (&v)[32]) {
+  const float4* row = reinterpret_cast<const float4*>(slot + lane * 128);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 x = row[g ^ (lane & 7)];
+    v[4 * g] = x.x;
+    v[4 * g + 1] = x.y;
+    v[4 * g + 2] = x.z;
+    v[4 * g + 3] = x.w;
+  }
+}
+
+// Where an epilogue warp's accumulator columns come from: its own TMEM lanes,
+// or, for the warps that compute on relayed quarters, the two shared-memory
+// slots that the quarter's reader fills. Relayed chunks arrive in column
+// order; load() may skip chunks but not go back.
+struct AccSrc {
+  uint32_t taddr;  // this warp's TMEM lanes, column 0 of the tile's accumulator
+  bool zero;       // the contraction was empty: every column reads 0
+  uint8_t* relay;  // null: read TMEM; else the quarter's two relay slots
+  uint32_t bar;    // the quarter's first relay barrier
+  int taken;       // relayed chunks taken (or skipped) in this tile
+
+  // 32 columns from column 32 * ch.
+  __device__ __forceinline__ void load(int ch, float (&v)[32]) {
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      return;
+    }
+    if (relay == nullptr) {
+      tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), v);
+      return;
+    }
+    skip_to(ch);
+    const int slot = taken & 1;
+    named_bar_sync(bar + slot, 64);
+    relay_get(relay + slot * kRelaySlotBytes, threadIdx.x & 31, v);
+    named_bar_arrive(bar + 2 + slot, 64);
+    ++taken;
+  }
+  // Release the relayed chunks before ch without reading them.
+  __device__ __forceinline__ void skip_to(int ch) {
+    if (zero || relay == nullptr) return;
+    while (taken < ch) {
+      const int slot = taken & 1;
+      named_bar_sync(bar + slot, 64);
+      named_bar_arrive(bar + 2 + slot, 64);
+      ++taken;
+    }
+  }
+};
+
+template <int CG, class E0, class E1>
+constexpr int gemm_smem_bytes() {
+  constexpr int out = OutStage<E0>::bytes > OutStage<E1>::bytes ? OutStage<E0>::bytes
+                                                                 : OutStage<E1>::bytes;
+  constexpr int relay = EpiRelay<E0>::value ? kRelayBytes : 0;
+  return TileCfg<CG>::kStages * TileCfg<CG>::kStageBytes + 1024 /* alignment slack */ + out +
+         relay + ((static_cast<int>(sizeof(GemmCtl)) + 127) / 128) * 128;
 }
 
 // Descriptor of the kk-th K=16 slice of a staged operand.
@@ -248,6 +331,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 1000000000ull) break;
   }
 }
+
+// Named barrier of the warps that run the epilogue policy (after the relay's).
+constexpr uint32_t kEpiBar = kRelayBar + 8;
 
 // AND of `ok` over the kThreads epilogue threads (named barrier 1).
 template <int kThreads>
@@ -293,14 +379,16 @@ __device__ __forceinline__ void st_shared_cluster(uint32_t addr, int v) {
 //   static constexpr uint32_t kABFormat;  // operand type: 1 bf16, 0 fp16
 //   struct Params;
 //   static __device__ void tile(const Params&, int m_block, int n_tile,
-//                               uint32_t taddr, bool acc_zero, int row_in_tile,
-//                               int quarter, int part, int lane, GemmCtl* ctl);
-// and may declare static constexpr int kEpiWarps = 8 (see EpiWarps).
+//                               AccSrc& acc, int row_in_tile, int quarter,
+//                               int part, int lane, GemmCtl* ctl);
+// and may declare static constexpr int kEpiWarps = 8 (see EpiWarps) or, with
+// 4 warps, static constexpr bool kRelay = true (see EpiRelay).
 // m_block indexes 128-row blocks of M (this CTA's rows are
-// m_block*128 + [0, 128)). `taddr` addresses this warp's 32 TMEM lanes at
-// column 0 of the tile's accumulator (read it with load_acc(..., acc_zero));
-// `part` is this warp's column half with 8 epilogue warps, else 0; the
-// epilogue threads may use named barrier 1.
+// m_block*128 + [0, 128)). `acc` gives this warp's 32 accumulator rows, 32
+// columns at a time, in increasing column order (acc.load(chunk, v));
+// `part` is this warp's column half with 8 epilogue warps, else 0. The
+// warps that run tile() may use named barrier kEpiBar (32 * kEpiWarps
+// threads).
 
 // One GEMM of a launch: operand majorness and epilogue.
 template <bool A_MN_, bool B_MN_, class Epi_>
@@ -315,8 +403,7 @@ struct Seg {
 struct NoEpi {
   static constexpr uint32_t kABFormat = 1;
   struct Params {};
-  __device__ static void tile(const Params&, int, int, uint32_t, bool, int, int, int, int,
-                              GemmCtl*) {}
+  __device__ static void tile(const Params&, int, int, AccSrc&, int, int, int, int, GemmCtl*) {}
 };
 struct NoSeg {
   static constexpr bool kPresent = false;
@@ -342,8 +429,12 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
   using Cfg = TileCfg<CG>;
   using E0 = typename S0::Epi;
   using E1 = typename S1::Epi;
-  constexpr int W = EpiWarps<E0>::value;
+  constexpr int W = EpiWarps<E0>::value;   // warps that run the epilogue policy
+  constexpr bool kRelay = EpiRelay<E0>::value;
+  constexpr int WP = epi_phys_warps<E0>();  // warps in the epilogue branch
   static_assert(!S1::kPresent || EpiWarps<E1>::value == W, "segments differ in epilogue warps");
+  static_assert(!S1::kPresent || EpiRelay<E1>::value == kRelay, "segments differ in relay");
+  static_assert(!kRelay || W == 4, "the relay serves a 4-warp epilogue");
   static_assert(!S1::kPresent || E1::kABFormat == E0::kABFormat, "segments differ in type");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -351,7 +442,8 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
   constexpr int kOut = OutStage<E0>::bytes > OutStage<E1>::bytes ? OutStage<E0>::bytes
                                                                  : OutStage<E1>::bytes;
   uint8_t* const out_stage = smem_raw + (base - raw) + Cfg::kStages * Cfg::kStageBytes;
-  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(out_stage + kOut);
+  uint8_t* const relay_slots = out_stage + kOut;
+  GemmCtl* ctl = reinterpret_cast<GemmCtl*>(relay_slots + (kRelay ? kRelayBytes : 0));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int m_tiles0, k_iters0, m_tiles1 = 0, k_iters1 = 0;
@@ -378,13 +470,15 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
+      // the warps that read TMEM: W per CTA (with the relay, its two readers
+      // stand in for the two warps they serve)
       mbar_init(smem_addr(&ctl->acc_empty[b]), W * CG);
     }
     // readers of a schedule slot: the MMA thread and the epilogue warps of
     // the even CTA, the producer and the epilogue warps of the odd one
     for (int s = 0; s < kSchedSlots; ++s) {
       mbar_init(smem_addr(&ctl->sched_full[s]), 1);
-      mbar_init(smem_addr(&ctl->sched_empty[s]), CG * (1 + W));
+      mbar_init(smem_addr(&ctl->sched_empty[s]), CG * (1 + WP));
     }
     mbar_init(smem_addr(&ctl->mma_done), 1);
     ctl->out_stage = out_stage;
@@ -626,9 +720,18 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
     }
   } else {
     // -------------------------------------------------- epilogue warps
-    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
-    const int part = (warp - 2) >> 2;  // column half with 8 epilogue warps, else 0
+    // Roles: without the relay, warp w runs the policy on TMEM lane quarter
+    // w % 4 (column half (w - 2) / 4). With it (warps 2-7): warps 2, 3 run the
+    // policy on quarters 2, 3; warps 4, 5 read quarters 0, 1 into the relay
+    // slots; warps 6, 7 run the policy on quarters 0, 1 from those slots.
+    const bool reader = kRelay && (warp == 4 || warp == 5);
+    const bool relayed = kRelay && warp >= 6;
+    const int quarter = relayed ? (warp & 3) - 2 : (warp & 3);  // TMEM lanes [32q, 32q+32)
+    const int part = kRelay ? 0 : (warp - 2) >> 2;  // column half with 8 epilogue warps, else 0
     const int row_in_tile = quarter * 32 + lane;
+    const uint32_t relay_bar = kRelayBar + 4u * static_cast<uint32_t>(quarter);
+    uint8_t* const relay = relay_slots + quarter * 2 * kRelaySlotBytes;
+    uint32_t relay_used = 0;  // reader: bit s set once slot s has been filled
     uint32_t acc_empty_leader = smem_addr(&ctl->acc_empty[0]);
     if constexpr (CG == 2) acc_empty_leader = map_to_rank(acc_empty_leader, 0);
     if (pdl & kPdlWaitEpilogue) grid_dependency_wait();
@@ -644,37 +747,67 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
         if (lane == 0) got_s = sched_read(it, uu);
         got_s = __shfl_sync(0xffffffffu, got_s ? 1 : 0, 0) != 0;
         uu = __shfl_sync(0xffffffffu, uu, 0);
-        if (!epi_all<32 * W>(got_s)) break;
+        if (!epi_all<32 * WP>(got_s)) break;
         u = uu;
         if (u < 0) break;
       }
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-      const bool got = wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, err_word);
-      if (!epi_all<32 * W>(got)) break;
+      // the relayed warps take their columns from the slots, not from TMEM
+      const bool got =
+          relayed || wait_bar<CG>(smem_addr(&ctl->acc_full[buf]), use, abort_flag, err_word);
+      if (!epi_all<32 * WP>(got)) break;
       tc_fence_after_sync();
       const uint32_t taddr =
           tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * kBN);
-      int m, n;
-      if (!S1::kPresent || u < total0) {
-        tile_coords(args.g0, m_tiles0, u, m, n);
-        E0::tile(args.ep0, m * CG + static_cast<int>(rank), n, taddr, k_iters0 == 0, row_in_tile,
-                 quarter, part, lane, ctl);
+      const bool seg0 = !S1::kPresent || u < total0;
+      const bool acc_zero = seg0 ? k_iters0 == 0 : k_iters1 == 0;
+      if (reader) {
+        // all 8 chunks of the quarter, in column order; the computing warp
+        // takes or skips each one
+        if (!acc_zero) {
+#pragma unroll 1
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            float v[32];
+            tmem_load_32cols(taddr + static_cast<uint32_t>(ch * 32), v);
+            const int slot = ch & 1;
+            if (relay_used & (1u << slot)) named_bar_sync(relay_bar + 2 + slot, 64);
+            relay_used |= 1u << slot;
+            relay_put(relay + slot * kRelaySlotBytes, lane, v);
+            named_bar_arrive(relay_bar + slot, 64);
+          }
+        }
       } else {
-        tile_coords(args.g1, m_tiles1, u - total0, m, n);
-        E1::tile(args.ep1, m * CG + static_cast<int>(rank), n, taddr, k_iters1 == 0, row_in_tile,
-                 quarter, part, lane, ctl);
+        AccSrc acc{taddr, acc_zero, relayed ? relay : nullptr, relay_bar, 0};
+        int m, n;
+        if (seg0) {
+          tile_coords(args.g0, m_tiles0, u, m, n);
+          E0::tile(args.ep0, m * CG + static_cast<int>(rank), n, acc, row_in_tile, quarter, part,
+                   lane, ctl);
+        } else {
+          tile_coords(args.g1, m_tiles1, u - total0, m, n);
+          E1::tile(args.ep1, m * CG + static_cast<int>(rank), n, acc, row_in_tile, quarter, part,
+                   lane, ctl);
+        }
+        acc.skip_to(kBN / 32);  // chunks the policy did not take
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t bar = acc_empty_leader + static_cast<uint32_t>(buf * sizeof(uint64_t));
-        if constexpr (CG == 1)
-          mbar_arrive(bar);
-        else
-          mbar_arrive_cluster(bar);
+      if (!relayed) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bar = acc_empty_leader + static_cast<uint32_t>(buf * sizeof(uint64_t));
+          if constexpr (CG == 1)
+            mbar_arrive(bar);
+          else
+            mbar_arrive_cluster(bar);
+        }
       }
     }
+    // a reader waits until its last slots have been taken: every arrival on
+    // the relay barriers is then matched
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot)
+      if (relay_used & (1u << slot)) named_bar_sync(relay_bar + 2 + slot, 64);
     // an epilogue that stages tensor stores issues them from lane 0 of each
     // warp: they complete before the CTA leaves
     if constexpr (kOut > 0) {

@@ -325,6 +325,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on named barrier `id` (of `nthreads` threads) without waiting: the
+// producer side of a hand-off whose consumers wait with named_bar_sync. The
+// arriving threads' earlier shared-memory accesses are ordered before the
+// accesses that follow the consumers' wait.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // One 32-byte streaming (evict-first) global load; src must be 32-byte
 // aligned. The low 16 bytes land in lo, the high 16 in hi.
 __device__ __forceinline__ void ld_cs_32B(const uint4* src, uint4& lo, uint4& hi) {

@@ -56,6 +56,12 @@ CASES = [
      "batchmean", True, None, 256, True),
     (_w("f16_narrow_last_chunk", 300, 128, 868, "f16", bias_var=0.02), 0.8, "sum", False,
      None, 256, False),
+    # H > 2048: 4 epilogue warps, lane quarters 0 and 1 relayed through shared memory to
+    # warps of the other two schedulers; ragged N, H and V (the last tile's relayed chunks
+    # past V are skipped) and a 100-column last chunk
+    (_w("h2312_relay_skip_bias", 300, 2312, 1000, bias_var=0.02, ignore_frac=0.1), 1.0,
+     "batchmean", True, None, 0, True),
+    (_w("h2304_relay_f16_topk", 257, 2304, 868, "f16"), 0.8, "none", False, 10, 256, False),
 ]
 
 

@@ -34,6 +34,9 @@ CASES = [
     _case("n4097_none", 4097, 512, 4096, ignore_frac=0.1, reduction="none"),
     _case("h3592_cap", 256, 3592, 2048, softcap=30.0, logit_scale=0.5, hidden_var=2.0,
           ignore_frac=0.3, reduction="sum"),
+    # H > 2048 runs the relayed 4-warp epilogues; ragged N, H and V, metrics on
+    _case("h2312_relay_bias", 300, 2312, 1000, bias_var=0.02, ignore_frac=0.1,
+          return_metrics=True),
     _case("v152063", 256, 128, 152063, ignore_frac=0.02, return_metrics=True),
     _case("zipf_bias_mean", 640, 192, 5000, bias_var=0.02, targets="zipf", ignore_frac=0.1),
     _case("peaked_rows", 384, 256, 3000, peaked_frac=0.01, ignore_frac=0.05),
@@ -92,6 +95,18 @@ def test_parity_narrow_last_chunk(dtype, skip):
     column but still take part in the grad_bias flush and the tile barriers."""
     w = _case("narrow_last_chunk", 700, 192, 868, dtype=dtype, bias_var=0.02, softcap=15.0,
               ignore_frac=0.1)
+    _check_case(w, vocab_chunk=256, skip_ignored=skip)
+
+
+@pytest.mark.parametrize("dtype,skip", [("bf16", True), ("f16", False)])
+def test_parity_relay_narrow_last_chunk(dtype, skip):
+    """H = 2112 > 2048: the forward and dlogits GEMMs run 4 epilogue warps with
+    lane quarters 0 and 1 relayed through shared memory. V = 868 in chunks of
+    256 leaves a 100-column last chunk, whose relayed chunks past the chunk's
+    width are skipped, not read; a bias sends grad_bias partials through the
+    relayed warps too."""
+    w = _case("relay_narrow_last_chunk", 300, 2112, 868, dtype=dtype, bias_var=0.02,
+              softcap=15.0, ignore_frac=0.1)
     _check_case(w, vocab_chunk=256, skip_ignored=skip)
 
 
