@@ -339,6 +339,10 @@ OPT_CASES = [
           label_smoothing=0.05, z_loss=1e-3),
     _case("ls_zl_f32", 257, 96, 2100, dtype="f32", bias_var=0.5, reduction="sum",
           label_smoothing=0.1, z_loss=1e-3),
+    # H > 2048: the relayed 4-warp epilogues carry the per-tile logit sums and the smoothed,
+    # z-loss D for lane quarters 0 and 1
+    _case("ls_zl_relay_h2112", 300, 2112, 1000, bias_var=0.02, softcap=15.0, ignore_frac=0.1,
+          label_smoothing=0.1, z_loss=1e-3, return_metrics=True),
 ]
 
 
