@@ -202,6 +202,14 @@ constexpr bool kDynamicDlogits = false;
 constexpr int kBandForward = 16;
 constexpr int kBandDlogits = 16;
 constexpr int kBandGradHidden = 8;
+// grad_weight tiles (vocabulary rows x H columns, contraction over the kept
+// rows) run in bands of 8 H tiles: hidden's columns of a band stay in L2 while
+// D is read once per band. At the Llama-3 head shape this cuts the fused
+// gradient launch's DRAM reads from 3.9 to 3.3 GB. Single interleaved steps
+// ran 1 % slower, but runs of back-to-back steps, which hold the GPU at its
+// power cap, ran 1 % faster: there a step's speed follows its energy, and DRAM
+// traffic is part of it.
+constexpr int kBandGradWeight = 8;
 
 // Workspace items of valid-row compaction (FLCE_SKIP_IGNORED_ROWS).
 struct CompactPlan {
@@ -742,6 +750,7 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
       g2.n_tiles = h_tiles;
       g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
       g2.m_fastest = 0;
+      g2.group = kBandGradWeight;
       g2.dyn_rows = n_kept;  // the contraction runs over the kept rows
       g2.dyn_axis = 1;
       g2.err_word = err_word;
