@@ -62,6 +62,7 @@ CASES = [
     (_w("h2312_relay_skip_bias", 300, 2312, 1000, bias_var=0.02, ignore_frac=0.1), 1.0,
      "batchmean", True, None, 0, True),
     (_w("h2304_relay_f16_topk", 257, 2304, 868, "f16"), 0.8, "none", False, 10, 256, False),
+    (_w("relay_n1_v513", 1, 2112, 513, bias_var=0.02), 1.0, "sum", False, None, 0, False),
 ]
 
 

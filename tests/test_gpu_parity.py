@@ -37,6 +37,10 @@ CASES = [
     # H > 2048 runs the relayed 4-warp epilogues; ragged N, H and V, metrics on
     _case("h2312_relay_bias", 300, 2312, 1000, bias_var=0.02, ignore_frac=0.1,
           return_metrics=True),
+    # the relay with a single row, and with a last vocabulary tile of one column (the
+    # computing warps take one chunk and release the other seven unread)
+    _case("relay_n1", 1, 2112, 777, bias_var=0.02, return_metrics=True),
+    _case("relay_v513_none", 129, 2112, 513, ignore_frac=0.1, reduction="none"),
     _case("v152063", 256, 128, 152063, ignore_frac=0.02, return_metrics=True),
     _case("zipf_bias_mean", 640, 192, 5000, bias_var=0.02, targets="zipf", ignore_frac=0.1),
     _case("peaked_rows", 384, 256, 3000, peaked_frac=0.01, ignore_frac=0.05),
