@@ -529,7 +529,7 @@ def bench_ours(args, rank, world, dev):
         "config": {"workload": describe_kl(w) if args.kl else describe(w),
                    "global_batch": n * world, "seq_len": None,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": (f"inputs {input_bytes(x) / 1e6:.0f} MB, L2 {L2_BYTES / 1e6:.0f} MB: "
+                   "l2": (f"inputs {input_bytes(x) / 2**20:.0f} MiB, L2 {L2_BYTES >> 20} MiB: "
                           "no flush between steps"),
                    "skip_ignored_rows": not args.all_rows,
                    "vocab_chunk": args.vocab_chunk or "library default",
