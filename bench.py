@@ -39,7 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # contractions of N x H x V per step of each tensor-core role: bwd_grads runs
 # both gradient GEMMs (grad_hidden and grad_weight) in one launch per chunk
 GEMM_ROLES = {"fwd_stats": 1, "fwd_kl": 1, "bwd_dlogits": 1, "bwd_dlogits_kl": 1,
-              "bwd_grads": 2}
+              "bwd_grads": 2, "fwd_stats_split": 1, "bwd_dlogits_split": 1, "bwd_grads_split": 2,
+              "fwd_kl_split": 1, "bwd_dlogits_kl_split": 1}
+# fp32 inputs whose rows are a multiple of 16 bytes run on the tensor cores with
+# each operand split into three bf16 parts: six bf16 products per fp32 product,
+# so their peak is the bf16 peak / 6
+SPLIT_ROLES = ("fwd_stats_split", "bwd_dlogits_split", "bwd_grads_split", "fwd_kl_split",
+               "bwd_dlogits_kl_split")
+SPLIT_PASSES = 6
+
 # the fp32 path's contractions run on the FP32 FMA units (ALU-bound)
 ALU_ROLES = ("fwd_stats_f32", "fwd_kl_f32", "bwd_dlogits_f32", "bwd_grad_weight_f32",
              "bwd_grad_hidden_f32")
@@ -498,7 +506,7 @@ def bench_ours(args, rank, world, dev):
         # algorithmic work of one launch: the rows it computes (ignored rows
         # are left out of every contraction unless --all-rows; the fp32 path
         # computes every row)
-        n_work = n if (args.all_rows or dom in ALU_ROLES) else n_valid
+        n_work = n if (args.all_rows or dom in ALU_ROLES or dom in SPLIT_ROLES) else n_valid
         roofline = roofline_entry(dom, launches, tot_ms, args.steps, n_work, h, v, ms, peaks,
                                   peak_src,
                                   torch.cuda.get_device_properties(dev).multi_processor_count)
@@ -673,7 +681,10 @@ def measure_config(w, dev, steps, warmup, peaks, peak_src, forward_only=False, k
     n, h, v = w.n, w.h, w.v
     flops = gemm_flops(n, h, v) / (4.0 if forward_only else 1.0)
     t_step = ms / k / 1e3
-    alu = w.dtype == "f32"
+    # fp32 inputs run split on the tensor cores or on the FFMA kernels (the
+    # library decides by size); the launches profiled say which
+    split = any(r in SPLIT_ROLES for r in (prof or {}))
+    alu = w.dtype == "f32" and not split
     out = {
         "workload": describe_kl(w) if kl else describe(w),
         "step": "forward only" if forward_only else "forward+backward",
@@ -693,6 +704,13 @@ def measure_config(w, dev, steps, warmup, peaks, peak_src, forward_only=False, k
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         fma_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
         out["fp32_fma_peak_frac"] = round(flops / t_step / 1e12 / fma_peak, 4)
+    elif split:
+        a = flops / t_step / 1e12
+        out["tensor_peak_frac"] = {
+            "of_split_burst": round(a / (peaks["bf16_tflops"] / SPLIT_PASSES), 4),
+            "split": f"fp32 operands as three bf16 parts: {SPLIT_PASSES} bf16 products per "
+                     f"fp32 product, peak = bf16 burst / {SPLIT_PASSES}",
+            "peaks": peak_src}
     else:
         a = flops / t_step / 1e12
         out["tensor_peak_frac"] = {
@@ -850,6 +868,10 @@ def roofline_entry(dom, launches, tot_ms, steps, n_work, h, v, run_ms, peaks, pe
         peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
         peak_kind = (f"bf16 {'sustained' if long_run else 'burst'}, {peak_src} "
                      f"(timed region {run_ms / 1e3:.2f} s)")
+        if dom in SPLIT_ROLES:
+            peak = round(peak / SPLIT_PASSES, 1)
+            peak_kind += (f" / {SPLIT_PASSES}: fp32 operands as three bf16 parts, "
+                          f"{SPLIT_PASSES} bf16 products per fp32 product")
     return {"bound": "alu" if alu else "tensor", "kernel": dom,
             "achieved": round(achieved, 1),
             "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),

@@ -187,8 +187,8 @@ constexpr int64_t kMinDefaultChunks = 5;
 // 16 pair row tiles (4096 rows) the forward and dlogits kernels re-read
 // hidden far less (measured at the Llama-3 head shape: forward DRAM reads
 // 6.5 -> 2.7-4.2 GB, dlogits 7.0 -> 3.1-3.4 GB per step); grad_hidden does
-// best with 8 (19.7 -> 11.6-13.5 GB). grad_weight is fastest along H and is
-// left unbanded (banding it raised its reads).
+// best with 8 (19.7 -> 11.6-13.5 GB). grad_weight runs fastest along H, in
+// bands of H tiles (kBandGradWeight below).
 // Tile order of the forward GEMM and of the dlogits GEMMs: dynamic (drawn
 // from a device counter, as the gradient launches always are) or static.
 // Static order lets pairs drift apart in the tile sequence, which widens the
@@ -223,6 +223,11 @@ struct FwdPlan {
   size_t partials = 0, zsum = 0, zt = 0, correct = 0, entropy = 0, sched = 0, total = 0;
   bool has_zsum = false;
   CompactPlan cp;
+  // fp32 inputs on the tensor cores: hidden's three bf16 parts, and the
+  // parts of one vocabulary chunk of W at a time
+  bool split = false;
+  int64_t split_chunk = 0;
+  size_t split_h = 0, split_w = 0;
 };
 
 struct BwdPlan {
@@ -230,12 +235,56 @@ struct BwdPlan {
   size_t d = 0, acc = 0, gb = 0, scales = 0, sched = 0, sched_bytes = 0, total = 0;
   bool use_acc = false;
   CompactPlan cp;
+  // fp32 inputs on the tensor cores (cross-entropy): D is held as three
+  // bf16 parts; hidden's parts, and the parts of the chunk's W rows
+  bool split = false;
+  size_t split_h = 0, split_w = 0;
 };
 
 // bf16 and fp16 inputs run on the tensor cores; fp32 on FFMA kernels.
 bool is_tc(const flce_problem* p) { return p->dtype == FLCE_BF16 || p->dtype == FLCE_F16; }
 
 int tc_type(const flce_problem* p) { return p->dtype == FLCE_F16 ? flce::kTcF16 : flce::kTcBF16; }
+
+// fp32 inputs whose rows are a multiple of 16 bytes run the cross-entropy
+// forward on the tensor cores with split operands: each value as three bf16
+// parts (hi + mid + lo, exact), each product as the six part products whose
+// dropped companions are below 2^-24 of it, accumulated in fp32.
+constexpr bool kSplitF32 = true;
+int64_t split_chunk(const flce_problem* p, bool caller_chunk = true);
+// Split operands also need their bf16 parts in the workspace: hidden's, one
+// chunk's of W and of D, and the fp32 grad_hidden accumulator. They are used
+// only while that stays under 40 % of one fp32 N x V logit matrix, so that a
+// step's peak memory (with the fp32 gradients) stays under one; smaller
+// problems (a short batch or a small vocabulary) run the FFMA kernels.
+bool is_split(const flce_problem* p) {
+  if (!kSplitF32 || p->dtype != FLCE_F32 || p->h % 8 != 0 || p->n <= 0) return false;
+  const int64_t c = split_chunk(p, false);  // the default chunk: vocab_chunk does not decide
+  const double parts = 6.0 * p->n * p->h + 6.0 * (p->n + p->h) * c + 4.0 * p->n * p->h;
+  return parts <= 0.4 * 4.0 * p->n * p->v;
+}
+// Part pairs (A part, B part) of the six passes: hi.hi, hi.mid, mid.hi,
+// hi.lo, lo.hi, mid.mid (0 hi, 1 mid, 2 lo).
+constexpr uint8_t kSplitPassA[6] = {0, 0, 1, 0, 2, 1};
+constexpr uint8_t kSplitPassB[6] = {0, 1, 0, 2, 0, 1};
+// Default vocabulary chunk of the split path (forward and backward): a
+// chunk's bf16 parts of D (N x c) and of W (c x H), 6 (N + H) c bytes, take at
+// most 512 MiB and at most a fifth of one fp32 N x V logit matrix; a multiple
+// of 256 columns, at least 256. (vocab_chunk, when set and caller_chunk, is
+// taken as given.)
+int64_t split_chunk(const flce_problem* p, bool caller_chunk) {
+  const int64_t v_round = cdiv(p->v, 256) * 256;
+  if (caller_chunk && p->vocab_chunk > 0) {
+    const int64_t c = cdiv(p->vocab_chunk, 256) * 256;
+    return c < v_round ? c : v_round;
+  }
+  const int64_t rows = p->n > 0 ? p->n : 1;
+  int64_t budget = rows * v_round * 4 / 5;
+  if (budget > (int64_t(512) << 20)) budget = int64_t(512) << 20;
+  int64_t c = budget / (6 * (rows + p->h)) / 256 * 256;
+  if (c < 256) c = 256;
+  return c < v_round ? c : v_round;
+}
 
 bool skips_ignored(const flce_problem* p) {
   return is_tc(p) && (p->flags & FLCE_SKIP_IGNORED_ROWS) != 0;
@@ -311,14 +360,15 @@ bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(pt
 // Per-row statistics entries of the forward: one per 256-column tile on the
 // tensor cores (two, per 128-column half, when the forward runs 8 epilogue
 // warps), one per kSimtTileV columns on the fp32 path.
-int64_t forward_parts(const flce_problem* p) {
-  if (!is_tc(p)) return cdiv(p->v, flce::kSimtTileV);
+int64_t forward_parts(const flce_problem* p, bool split = false) {
+  if (!is_tc(p) && !split) return cdiv(p->v, flce::kSimtTileV);
   return cdiv(p->v, flce::kBN) * flce::fwd_parts_per_tile(p->h);
 }
 
 FwdPlan plan_forward(const flce_problem* p) {
   FwdPlan f;
-  f.n_vt = forward_parts(p);
+  f.split = is_split(p);
+  f.n_vt = forward_parts(p, f.split);
   size_t off = 0;
   f.partials = off;
   off = align_up(off + static_cast<size_t>(p->n) * f.n_vt * 16);
@@ -334,16 +384,27 @@ FwdPlan plan_forward(const flce_problem* p) {
   f.sched = off;  // tile counter of the forward GEMM
   if (is_tc(p)) off = align_up(off + sizeof(int));
   off = plan_compaction(p, false, false, off, &f.cp);
+  if (f.split) {
+    f.split_chunk = split_chunk(p);
+    f.split_h = off;
+    off = align_up(off + 3 * static_cast<size_t>(p->n) * p->h * 2);
+    f.split_w = off;
+    off = align_up(off + 3 * static_cast<size_t>(f.split_chunk) * p->h * 2);
+  }
   f.total = off;
   return f;
 }
 
 BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   BwdPlan b;
-  const int64_t elem = is_tc(p) ? 2 : 4;
+  b.split = is_split(p);
+  const bool tc = is_tc(p) || b.split;  // tile shapes and accumulation of the tensor-core GEMMs
+  const int64_t elem = is_tc(p) ? 2 : (b.split ? 6 : 4);  // bytes of one D entry
   const int64_t v_round = cdiv(p->v, 256) * 256;
   int64_t c = p->vocab_chunk;
-  if (c > 0) {
+  if (b.split) {
+    c = split_chunk(p);
+  } else if (c > 0) {
     c = cdiv(c, 256) * 256;
   } else {
     // balanced chunks: at least kMinDefaultChunks (at most one per tile),
@@ -362,8 +423,8 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   if (c > v_round) c = v_round;
   b.chunk = c;
   b.n_chunks = cdiv(p->v, c);
-  b.use_acc = is_tc(p) && b.n_chunks > 1;
-  b.gb_parts = p->has_bias ? cdiv(p->n, is_tc(p) ? flce::kBM : flce::kSimtTileN) : 0;
+  b.use_acc = tc && b.n_chunks > 1;
+  b.gb_parts = p->has_bias ? cdiv(p->n, tc ? flce::kBM : flce::kSimtTileN) : 0;
   size_t off = 0;
   b.d = off;
   off = align_up(off + static_cast<size_t>(p->n) * c * elem);
@@ -376,11 +437,17 @@ BwdPlan plan_backward(const flce_problem* p, bool kl = false) {
   // tile counters of the dynamically scheduled launches, two per chunk
   // (dlogits, gradients), zeroed at the start of every backward call
   b.sched = off;
-  if (is_tc(p)) {
+  if (tc) {
     b.sched_bytes = align_up(static_cast<size_t>(2 * b.n_chunks) * sizeof(int));
     off += b.sched_bytes;
   }
   off = plan_compaction(p, true, kl, off, &b.cp);
+  if (b.split) {
+    b.split_h = off;
+    off = align_up(off + 3 * static_cast<size_t>(p->n) * p->h * 2);
+    b.split_w = off;
+    off = align_up(off + 3 * static_cast<size_t>(c) * p->h * 2);
+  }
   b.total = off;
   return b;
 }
@@ -516,15 +583,26 @@ struct KLFwdPlan {
   int64_t n_vt = 0;
   size_t partials = 0, sched = 0, total = 0;
   CompactPlan cp;
+  bool split = false;  // as in FwdPlan
+  int64_t split_chunk = 0;
+  size_t split_h = 0, split_w = 0;
 };
 
 KLFwdPlan plan_kl_forward(const flce_problem* ce) {
   KLFwdPlan f;
-  f.n_vt = forward_parts(ce);
+  f.split = is_split(ce);
+  f.n_vt = forward_parts(ce, f.split);
   size_t off = align_up(static_cast<size_t>(ce->n) * f.n_vt * 16);
   f.sched = off;  // tile counter of the forward GEMM
   if (is_tc(ce)) off = align_up(off + sizeof(int));
   off = plan_compaction(ce, false, true, off, &f.cp);
+  if (f.split) {
+    f.split_chunk = split_chunk(ce);
+    f.split_h = off;
+    off = align_up(off + 3 * static_cast<size_t>(ce->n) * ce->h * 2);
+    f.split_w = off;
+    off = align_up(off + 3 * static_cast<size_t>(f.split_chunk) * ce->h * 2);
+  }
   f.total = off;
   return f;
 }
@@ -799,6 +877,185 @@ flce_status backward_impl(const flce_problem* p, const KLArgs* kl, const void* h
         e = flce::launch_tc_grads(type, gl, dev.sms, s);
       }
       if (e != cudaSuccess) return cuda_fail(e, "gradient kernel");
+    }
+  } else if (plan.split) {
+    // fp32 operands as three bf16 parts each (see is_split): hidden once, the
+    // chunk's W rows per chunk; D is written and read as three bf16 parts
+    uint8_t* hp = ws + plan.split_h;
+    uint8_t* wp = ws + plan.split_w;
+    uint8_t* dp0 = ws + plan.d;
+    const size_t h_part = static_cast<size_t>(p->n) * p->h * 2;
+    const size_t w_part = static_cast<size_t>(plan.chunk) * p->h * 2;
+    const size_t d_part = static_cast<size_t>(p->n) * plan.chunk * 2;
+    float* acc = plan.use_acc ? reinterpret_cast<float*>(ws + plan.acc) : nullptr;
+    int* sched = reinterpret_cast<int*>(ws + plan.sched);
+    e = cudaMemsetAsync(sched, 0, plan.sched_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (tile counters)");
+    {
+      ProfScope ps("split_f32", s);
+      e = flce::launch_split3(static_cast<const float*>(hidden), p->n * p->h, hp, hp + h_part,
+                              hp + 2 * h_part, dev.sms, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+    CUtensorMap tm_h_k[3], tm_h_mn[3];
+    for (int q = 0; q < 3; ++q)
+      if (!make_map(&tm_h_k[q], "hidden part", hp + q * h_part, p->h, p->n, p->h, flce::kBK,
+                    flce::kBM) ||
+          !make_map(&tm_h_mn[q], "hidden part^T", hp + q * h_part, p->h, p->n, p->h, 64,
+                    flce::kBK))
+        return FLCE_ERR_CUDA;
+    const int h_tiles = static_cast<int>(cdiv(p->h, flce::kBN));
+    auto set_passes = [](GemmGeom& g) {
+      g.passes = 6;
+      for (int q = 0; q < 6; ++q) {
+        g.pass_a[q] = kSplitPassA[q];
+        g.pass_b[q] = kSplitPassB[q];
+      }
+    };
+    for (int64_t c = 0; c < plan.n_chunks; ++c) {
+      const int64_t c0 = c * plan.chunk;
+      const int64_t width = (p->v - c0) < plan.chunk ? (p->v - c0) : plan.chunk;
+      {
+        ProfScope ps("split_f32", s);
+        e = flce::launch_split3(static_cast<const float*>(weight) + c0 * p->h, width * p->h, wp,
+                                wp + w_part, wp + 2 * w_part, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+      CUtensorMap tm_w_k[3], tm_w_mn[3], tm_d_k[3], tm_d_mn[3], tm_d_st[3];
+      for (int q = 0; q < 3; ++q) {
+        uint8_t* wq = wp + q * w_part;
+        uint8_t* dq = dp0 + q * d_part;
+        if (!make_map(&tm_w_k[q], "weight part", wq, p->h, width, p->h, flce::kBK,
+                      flce::kBLoadRowsTC) ||
+            !make_map(&tm_w_mn[q], "weight part^T", wq, p->h, width, p->h, 64, flce::kBK) ||
+            !make_map(&tm_d_k[q], "dlogits part", dq, width, p->n, plan.chunk, flce::kBK,
+                      flce::kBM) ||
+            !make_map(&tm_d_mn[q], "dlogits part^T", dq, width, p->n, plan.chunk, 64,
+                      flce::kBK) ||
+            !make_map(&tm_d_st[q], "dlogits part store", dq, width, p->n, plan.chunk, 32, 32,
+                      false))
+          return FLCE_ERR_CUDA;
+      }
+
+      // 1. the chunk's logits and D, stored as three bf16 parts
+      GemmGeom g1{};
+      g1.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+      g1.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
+      g1.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+      g1.m_fastest = 1;
+      g1.group = kBandDlogits;
+      g1.err_word = err_word;
+      // the split of this chunk's W rows precedes it: loads wait too
+      g1.pdl = flce::kPdlWaitLoads | flce::kPdlWaitEpilogue;
+      set_passes(g1);
+      flce::DlogitsParams dp{};
+      dp.d_map = tm_d_st[0];
+      dp.d_map_x[0] = tm_d_st[1];
+      dp.d_map_x[1] = tm_d_st[2];
+      dp.bias = bias;
+      dp.targets = targets;
+      dp.lse = lse_rows;
+      dp.grad_out = grad_out;
+      dp.n_valid = n_valid;
+      dp.gb_partial = gb_partial;
+      dp.gb_ld = p->v;
+      dp.n_rows = p->n;
+      dp.v = p->v;
+      dp.ignore_index = p->ignore_index;
+      dp.c0 = static_cast<int>(c0);
+      dp.width = static_cast<int>(width);
+      dp.reduction = p->reduction;
+      dp.label_smoothing = p->label_smoothing;
+      dp.z_loss = p->z_loss;
+      dp.xf = xf;
+      if (kl != nullptr) {
+        flce::DlogitsKLParams dk{};
+        dk.d_map = tm_d_st[0];
+        dk.d_map_x[0] = tm_d_st[1];
+        dk.d_map_x[1] = tm_d_st[2];
+        dk.bias = bias;
+        dk.q = kl->q;
+        dk.q_vec = (p->v % 8 == 0 && aligned(kl->q, 16)) ? 1 : 0;
+        dk.labels = targets;
+        dk.lse = lse_rows;
+        dk.qsum = kl->qsum;
+        dk.grad_out = grad_out;
+        dk.n_counted = n_valid;
+        dk.gb_partial = gb_partial;
+        dk.gb_ld = p->v;
+        dk.n_rows = p->n;
+        dk.v = p->v;
+        dk.ignore_index = p->ignore_index;
+        dk.c0 = static_cast<int>(c0);
+        dk.width = static_cast<int>(width);
+        dk.reduction = kl->reduction;
+        dk.xf = xf;
+        ProfScope ps("bwd_dlogits_kl_split", s);
+        e = flce::launch_tc_dlogits_kl_split(tm_h_k, tm_w_k, g1, dk,
+                                             flce::dlogits_epi_warps(p->h), dev.sms, s);
+      } else {
+        ProfScope ps("bwd_dlogits_split", s);
+        e = flce::launch_tc_dlogits_split(tm_h_k, tm_w_k, g1, dp, flce::dlogits_epi_warps(p->h),
+                                          dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "split dlogits kernel");
+
+      // 2. and 3., one launch: grad_weight[c0 : c0+width] = D^T @ hidden and
+      // grad_hidden (+)= D @ weight[c0 : c0+width], six part products each
+      flce::GradsSplitLaunch gl{};
+      for (int q = 0; q < 3; ++q) {
+        gl.d_k[q] = tm_d_k[q];
+        gl.weight_mn[q] = tm_w_mn[q];
+        gl.d_mn[q] = tm_d_mn[q];
+        gl.hidden_mn[q] = tm_h_mn[q];
+      }
+      GemmGeom& g2 = gl.g_gw;
+      g2.m_tiles = static_cast<int>(cdiv(width, flce::kTileRowsTC));
+      g2.n_tiles = h_tiles;
+      g2.k_iters = static_cast<int>(cdiv(p->n, flce::kBK));
+      g2.m_fastest = 0;
+      g2.group = kBandGradWeight;
+      g2.err_word = err_word;
+      set_passes(g2);
+      flce::StoreRowsParams& sp = gl.sp;
+      sp.out = grad_weight;
+      sp.out_f32 = p->grad_weight_dtype == FLCE_F32 ? 1 : 0;
+      sp.ld = p->h;
+      sp.rows = width;
+      sp.row0 = c0;
+      sp.cols = static_cast<int>(p->h);
+      GemmGeom& g3 = gl.g_gh;
+      g3.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+      g3.n_tiles = h_tiles;
+      g3.k_iters = static_cast<int>(cdiv(width, flce::kBK));
+      g3.m_fastest = 1;
+      g3.group = kBandGradHidden;
+      g3.err_word = err_word;
+      set_passes(g3);
+      flce::AccRowsParams& ap = gl.ap;
+      ap.acc = acc;
+      ap.out = grad_hidden;
+      ap.out_f32 = 1;
+      if (plan.n_chunks == 1)
+        ap.mode = flce::kAccStoreOut;
+      else if (c == 0)
+        ap.mode = flce::kAccStore;
+      else if (c == plan.n_chunks - 1)
+        ap.mode = flce::kAccAddOut;
+      else
+        ap.mode = flce::kAccAdd;
+      ap.ld = p->h;
+      ap.rows = p->n;
+      ap.cols = static_cast<int>(p->h);
+      gl.sched = sched + c;
+      g2.pdl = flce::kPdlWaitLoads | flce::kPdlWaitEpilogue;
+      g3.pdl = flce::kPdlWaitLoads | flce::kPdlWaitEpilogue;
+      gl.gh_first = g3.k_iters >= g2.k_iters;
+      {
+        ProfScope ps("bwd_grads_split", s);
+        e = flce::launch_tc_grads_split(gl, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "split gradient kernel");
     }
   } else {
     float* dbuf = reinterpret_cast<float*>(ws + plan.d);
@@ -1106,6 +1363,67 @@ flce_status flce_forward(const flce_problem* p, const void* hidden, const void* 
       e = flce::launch_tc_fwd_stats(tc_type(p), tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h),
                                     dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "forward statistics kernel");
+    } else if (plan.split) {
+      // fp32 operands as three bf16 parts each: hidden once, W one
+      // vocabulary chunk at a time, six part products per tile
+      uint8_t* hp = ws + plan.split_h;
+      uint8_t* wp = ws + plan.split_w;
+      const size_t h_part = static_cast<size_t>(p->n) * p->h * 2;
+      const size_t w_part = static_cast<size_t>(plan.split_chunk) * p->h * 2;
+      {
+        ProfScope ps("split_f32", s);
+        e = flce::launch_split3(static_cast<const float*>(hidden), p->n * p->h, hp, hp + h_part,
+                                hp + 2 * h_part, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+      CUtensorMap tm_h[3];
+      for (int q = 0; q < 3; ++q)
+        if (!make_map(&tm_h[q], "hidden part", hp + q * h_part, p->h, p->n, p->h, flce::kBK,
+                      flce::kBM))
+          return FLCE_ERR_CUDA;
+      for (int64_t c0 = 0; c0 < p->v; c0 += plan.split_chunk) {
+        const int64_t width = (p->v - c0) < plan.split_chunk ? (p->v - c0) : plan.split_chunk;
+        {
+          ProfScope ps("split_f32", s);
+          e = flce::launch_split3(static_cast<const float*>(weight) + c0 * p->h, width * p->h,
+                                  wp, wp + w_part, wp + 2 * w_part, dev.sms, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+        CUtensorMap tm_w[3];
+        for (int q = 0; q < 3; ++q)
+          if (!make_map(&tm_w[q], "weight part", wp + q * w_part, p->h, width, p->h, flce::kBK,
+                        flce::kBLoadRowsTC))
+            return FLCE_ERR_CUDA;
+        GemmGeom g{};
+        g.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+        g.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
+        g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+        g.m_fastest = 1;
+        g.group = kBandForward;
+        g.err_word = err_word;
+        g.passes = 6;
+        for (int q = 0; q < 6; ++q) {
+          g.pass_a[q] = kSplitPassA[q];
+          g.pass_b[q] = kSplitPassB[q];
+        }
+        flce::FwdStatsParams fp{};
+        fp.bias = bias;
+        fp.targets = targets;
+        fp.partials = partials;
+        fp.zsum = zsum;
+        fp.zt = zt;
+        fp.n_rows = p->n;
+        fp.v = p->v;
+        fp.n_vt = plan.n_vt;
+        fp.metrics =
+            (metrics_out != nullptr || correct_rows != nullptr || entropy_rows != nullptr) ? 1 : 0;
+        fp.xf = xf;
+        fp.c0 = c0;
+        ProfScope ps("fwd_stats_split", s);
+        e = flce::launch_tc_fwd_stats_split(tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h),
+                                            dev.sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "split forward statistics kernel");
+      }
     } else {
       flce::SimtFwdParams fp{};
       fp.hidden = static_cast<const float*>(hidden);
@@ -1295,6 +1613,64 @@ flce_status flce_kl_forward(const flce_kl_problem* k, const void* hidden, const 
       e = flce::launch_tc_fwd_kl(tc_type(p), tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h),
                                  dev.sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "KL forward kernel");
+    } else if (plan.split) {
+      // as the cross-entropy's split forward, with the teacher rows in fp32
+      uint8_t* hp = ws + plan.split_h;
+      uint8_t* wp = ws + plan.split_w;
+      const size_t h_part = static_cast<size_t>(p->n) * p->h * 2;
+      const size_t w_part = static_cast<size_t>(plan.split_chunk) * p->h * 2;
+      {
+        ProfScope ps("split_f32", s);
+        e = flce::launch_split3(static_cast<const float*>(hidden), p->n * p->h, hp, hp + h_part,
+                                hp + 2 * h_part, dev.sms, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+      CUtensorMap tm_h[3];
+      for (int q = 0; q < 3; ++q)
+        if (!make_map(&tm_h[q], "hidden part", hp + q * h_part, p->h, p->n, p->h, flce::kBK,
+                      flce::kBM))
+          return FLCE_ERR_CUDA;
+      for (int64_t c0 = 0; c0 < p->v; c0 += plan.split_chunk) {
+        const int64_t width = (p->v - c0) < plan.split_chunk ? (p->v - c0) : plan.split_chunk;
+        {
+          ProfScope ps("split_f32", s);
+          e = flce::launch_split3(static_cast<const float*>(weight) + c0 * p->h, width * p->h,
+                                  wp, wp + w_part, wp + 2 * w_part, dev.sms, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 split kernel");
+        CUtensorMap tm_w[3];
+        for (int q = 0; q < 3; ++q)
+          if (!make_map(&tm_w[q], "weight part", wp + q * w_part, p->h, width, p->h, flce::kBK,
+                        flce::kBLoadRowsTC))
+            return FLCE_ERR_CUDA;
+        GemmGeom g{};
+        g.m_tiles = static_cast<int>(cdiv(p->n, flce::kTileRowsTC));
+        g.n_tiles = static_cast<int>(cdiv(width, flce::kBN));
+        g.k_iters = static_cast<int>(cdiv(p->h, flce::kBK));
+        g.m_fastest = 1;
+        g.group = kBandForward;
+        g.err_word = err_word;
+        g.passes = 6;
+        for (int q = 0; q < 6; ++q) {
+          g.pass_a[q] = kSplitPassA[q];
+          g.pass_b[q] = kSplitPassB[q];
+        }
+        flce::FwdKLParams fp{};
+        fp.bias = bias;
+        fp.q = target_probs;
+        fp.q_vec = (p->v % 8 == 0 && aligned(target_probs, 16)) ? 1 : 0;
+        fp.partials = partials;
+        fp.n_rows = p->n;
+        fp.v = p->v;
+        fp.n_vt = plan.n_vt;
+        fp.eps = k->eps;
+        fp.xf = xf;
+        fp.c0 = c0;
+        ProfScope ps("fwd_kl_split", s);
+        e = flce::launch_tc_fwd_kl_split(tm_h, tm_w, g, fp, flce::fwd_epi_warps(p->h), dev.sms,
+                                         s);
+        if (e != cudaSuccess) return cuda_fail(e, "split KL forward kernel");
+      }
     } else {
       flce::SimtFwdParams fp{};
       fp.hidden = static_cast<const float*>(hidden);

@@ -42,6 +42,7 @@ struct FwdStatsParams {
   int64_t n_vt;
   int metrics;                // 1: also the argmax and entropy terms (t); 0: (m, s) only
   LogitXform xf;
+  int64_t c0;                 // first column of the launch's vocabulary chunk (multiple of 256)
 };
 
 // Bytes of one epilogue warp's staging buffer for the D tensor stores: a
@@ -56,6 +57,9 @@ constexpr bool kEpiRelay = true;
 
 struct DlogitsParams {
   CUtensorMap d_map;  // D of the chunk [N][width] (pitch ldd), box {32, 32}, for the stores
+  // fp32 operands split into bf16 parts: D is stored as its three bf16 parts,
+  // d_map taking hi and these mid and lo (same geometry)
+  CUtensorMap d_map_x[2];
   const void* bias;
   const int64_t* targets;
   const float* lse;
@@ -91,10 +95,12 @@ struct FwdKLParams {
   int64_t n_vt;
   float eps;
   LogitXform xf;              // scale = 1 / temperature
+  int64_t c0;                 // first column of the launch's vocabulary chunk (multiple of 256)
 };
 
 struct DlogitsKLParams {
   CUtensorMap d_map;  // as in DlogitsParams
+  CUtensorMap d_map_x[2];  // as in DlogitsParams
   const void* bias;
   const void* q;
   int q_vec;
@@ -131,7 +137,8 @@ enum AccMode { kAccStore = 0, kAccAdd = 1, kAccAddOut = 2, kAccStoreOut = 3 };
 
 struct AccRowsParams {
   float* acc;
-  void* out;  // input type
+  void* out;  // input type (fp32 when out_f32)
+  int out_f32;
   const float* out_scale;  // device scalar multiplying the results, or null (1)
   int mode;
   int64_t ld;
@@ -153,6 +160,12 @@ cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
 // `type` is a TcType; every launcher runs the CTA-pair GEMM of that type.
 // epi_warps (4 or 8): epilogue warps of the forward GEMMs, see fwd_epi_warps;
 // with 8 the statistics are kept per 128 columns (fwd_parts_per_tile).
+// The forward statistics GEMM over fp32 operands split into three bf16 parts
+// (maps [0] hi, [1] mid, [2] lo; g.passes part pairs); the bias is fp32.
+cudaError_t launch_tc_fwd_stats_split(const CUtensorMap (&tm_hidden_k)[3],
+                                      const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                      const FwdStatsParams& p, int epi_warps, int sms,
+                                      cudaStream_t s);
 cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                                 const CUtensorMap& tm_weight_k, const GemmGeom& g,
                                 const FwdStatsParams& p, int epi_warps, int sms, cudaStream_t s);
@@ -190,6 +203,33 @@ struct GradsLaunch {
   bool gh_first;
 };
 cudaError_t launch_tc_grads(int type, const GradsLaunch& l, int sms, cudaStream_t s);
+
+// The backward's GEMMs over fp32 operands split into three bf16 parts (maps
+// [0] hi, [1] mid, [2] lo; the geometries carry the part pairs): dlogits
+// with an fp32 bias, storing D as three bf16 parts (p.d_map, p.d_map_x), and
+// the fused gradient launch.
+cudaError_t launch_tc_dlogits_split(const CUtensorMap (&tm_hidden_k)[3],
+                                    const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                    const DlogitsParams& p, int epi_warps, int sms,
+                                    cudaStream_t s);
+struct GradsSplitLaunch {
+  CUtensorMap d_k[3], weight_mn[3], d_mn[3], hidden_mn[3];
+  GemmGeom g_gh, g_gw;
+  AccRowsParams ap;
+  StoreRowsParams sp;
+  int* sched;
+  bool gh_first;
+};
+cudaError_t launch_tc_grads_split(const GradsSplitLaunch& l, int sms, cudaStream_t s);
+// The fused linear KL divergence's forward and dlogits GEMMs over split
+// operands (fp32 bias and teacher probabilities).
+cudaError_t launch_tc_fwd_kl_split(const CUtensorMap (&tm_hidden_k)[3],
+                                   const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                   const FwdKLParams& p, int epi_warps, int sms, cudaStream_t s);
+cudaError_t launch_tc_dlogits_kl_split(const CUtensorMap (&tm_hidden_k)[3],
+                                       const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                       const DlogitsKLParams& p, int epi_warps, int sms,
+                                       cudaStream_t s);
 
 // Bounded-wait self-test: result[0] (one CTA) and result[1..2] (a CTA pair).
 cudaError_t launch_wait_selftest(int* err_word, uint64_t budget_ns, int* result, cudaStream_t s);
@@ -354,6 +394,11 @@ struct GatherParams {
   float* qsum_c;
 };
 cudaError_t launch_gather_rows(const GatherParams& p, cudaStream_t s);
+
+// x[0, n) (fp32, 16-byte aligned, n a multiple of 4) -> three bf16 arrays
+// with x = hi + mid + lo exactly (the split-bf16 form of fp32 operands).
+cudaError_t launch_split3(const float* x, int64_t n, void* hi, void* mid, void* lo, int sms,
+                          cudaStream_t s);
 
 // grad_hidden rows of ignored targets := 0 (16-bit elements, [N, h]).
 cudaError_t launch_zero_ignored_rows(const int64_t* targets, int64_t n, int64_t ignore_index,

@@ -407,6 +407,56 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
   }
 }
 
+// fp32 -> three bf16 parts, x = hi + mid + lo: hi = bf16(x), mid = bf16(x - hi),
+// lo = x - hi - mid. Each remainder is exact in fp32 and lo needs at most 8
+// significant bits, so the three parts hold x exactly (no underflow in
+// bf16, whose exponent range is fp32's). Four elements per thread.
+__device__ __forceinline__ void split3_store(const float (&e)[4], uint2* __restrict__ hi,
+                                             uint2* __restrict__ mid, uint2* __restrict__ lo,
+                                             int64_t i) {
+  __nv_bfloat16 h[4], m[4], l[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    h[k] = __float2bfloat16_rn(e[k]);
+    const float r1 = e[k] - __bfloat162float(h[k]);
+    m[k] = __float2bfloat16_rn(r1);
+    l[k] = __float2bfloat16_rn(r1 - __bfloat162float(m[k]));
+  }
+  auto pack = [](const __nv_bfloat16 (&b)[4]) {
+    uint2 w;
+    w.x = static_cast<uint32_t>(__bfloat16_as_ushort(b[0])) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(b[1])) << 16);
+    w.y = static_cast<uint32_t>(__bfloat16_as_ushort(b[2])) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(b[3])) << 16);
+    return w;
+  };
+  hi[i] = pack(h);
+  mid[i] = pack(m);
+  lo[i] = pack(l);
+}
+
+__global__ void __launch_bounds__(256)
+    split3_kernel(const float4* __restrict__ x, int64_t n4, uint2* __restrict__ hi,
+                  uint2* __restrict__ mid, uint2* __restrict__ lo) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldg(x + i);
+    const float e[4] = {v.x, v.y, v.z, v.w};
+    split3_store(e, hi, mid, lo, i);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    split3_scalar_kernel(const float* __restrict__ x, int64_t n4, uint2* __restrict__ hi,
+                         uint2* __restrict__ mid, uint2* __restrict__ lo) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float e[4] = {__ldg(x + 4 * i), __ldg(x + 4 * i + 1), __ldg(x + 4 * i + 2),
+                        __ldg(x + 4 * i + 3)};
+    split3_store(e, hi, mid, lo, i);
+  }
+}
+
 __global__ void __launch_bounds__(kGatherThreads)
     zero_ignored_rows_kernel(const int64_t* __restrict__ targets, int64_t n, int64_t ignore_index,
                              void* out, int64_t h) {
@@ -448,6 +498,23 @@ cudaError_t launch_merge_kl(const MergeKLParams& p, cudaStream_t s) {
 
 cudaError_t launch_finalize_kl(const FinalizeKLParams& p, cudaStream_t s) {
   finalize_kl_kernel<<<1, kFinThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split3(const float* x, int64_t n, void* hi, void* mid, void* lo,
+                          int sms, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int64_t n4 = n / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > 8 * static_cast<int64_t>(sms)) blocks = 8 * static_cast<int64_t>(sms);
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+    split3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(x), n4, static_cast<uint2*>(hi),
+        static_cast<uint2*>(mid), static_cast<uint2*>(lo));
+  } else {  // a caller's fp32 array need only be 4-byte aligned
+    split3_scalar_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, n4, static_cast<uint2*>(hi), static_cast<uint2*>(mid), static_cast<uint2*>(lo));
+  }
   return cudaGetLastError();
 }
 

@@ -38,6 +38,7 @@ namespace flce {
 namespace {
 
 // 32 bias values of columns [c, c+32) (fewer when nv < 32; the rest are 0).
+// T: the bias element type (16-bit, or float for split fp32 operands).
 template <typename T>
 __device__ __forceinline__ void load_bias32(const void* bias_v, int64_t c, int nv,
                                             float (&b)[32]) {
@@ -47,7 +48,24 @@ __device__ __forceinline__ void load_bias32(const void* bias_v, int64_t c, int n
     for (int k = 0; k < 32; ++k) b[k] = 0.0f;
     return;
   }
-  if (nv == 32) {
+  if constexpr (std::is_same_v<T, float>) {
+    // the caller's fp32 bias need only be 4-byte aligned
+    if (nv == 32 && (reinterpret_cast<uintptr_t>(bias + c) & 15u) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(bias + c);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 w = __ldg(src + q);
+        b[4 * q] = w.x;
+        b[4 * q + 1] = w.y;
+        b[4 * q + 2] = w.z;
+        b[4 * q + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) b[k] = (k < nv) ? __ldg(bias + c + k) : 0.0f;
+    }
+    return;
+  } else if (nv == 32) {
     const uint4* src = reinterpret_cast<const uint4*>(bias + c);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -82,6 +100,24 @@ __device__ __forceinline__ void store32(T* dst, const float (&v)[32], int nv, fl
 #pragma unroll
     for (int k = 0; k < 32; ++k)
       if (k < nv) dst[k] = Elem<T>::from(v[k] * scale);
+  }
+}
+
+// 32 fp32 values times scale, with 16-byte stores when dst is 16-byte aligned
+// (a caller's fp32 buffer need only be 4-byte aligned), element by element
+// otherwise or when only nv < 32 are in range.
+__device__ __forceinline__ void store32_f32(float* dst, const float (&v)[32], int nv,
+                                            float scale) {
+  if (nv == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+    float4* dv = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      dv[q] = make_float4(v[4 * q] * scale, v[4 * q + 1] * scale, v[4 * q + 2] * scale,
+                          v[4 * q + 3] * scale);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k < nv) dst[k] = v[k] * scale;
   }
 }
 
@@ -181,7 +217,9 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 // instead. Entries past nv (and every entry of an inactive row) are 0.
 template <typename T>
 struct RowChunk32 {
-  uint4 w[4];
+  static constexpr bool kF32 = std::is_same_v<T, float>;  // fp32 teacher (split operands)
+  static constexpr int kVecs = kF32 ? 8 : 4;               // 16-byte vectors of a chunk
+  uint4 w[kVecs];
   bool raw;
 
   __device__ __forceinline__ void issue(const T* row_ptr, int64_t c, int nv, bool vec,
@@ -191,10 +229,10 @@ struct RowChunk32 {
       const uint4* src = reinterpret_cast<const uint4*>(row_ptr + c);
       if ((reinterpret_cast<uintptr_t>(src) & 31u) == 0) {
 #pragma unroll
-        for (int r = 0; r < 4; r += 2) ld_cs_32B(src + r, w[r], w[r + 1]);
+        for (int r = 0; r < kVecs; r += 2) ld_cs_32B(src + r, w[r], w[r + 1]);
       } else {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) w[r] = __ldcs(src + r);
+        for (int r = 0; r < kVecs; ++r) w[r] = __ldcs(src + r);
       }
     }
   }
@@ -202,18 +240,33 @@ struct RowChunk32 {
   __device__ __forceinline__ void get(const T* row_ptr, int64_t c, int nv, bool active,
                                       float (&q)[32]) const {
     if (raw) {
+      if constexpr (kF32) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t parts[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+        for (int r = 0; r < 8; ++r) {
+          q[4 * r] = __uint_as_float(w[r].x);
+          q[4 * r + 1] = __uint_as_float(w[r].y);
+          q[4 * r + 2] = __uint_as_float(w[r].z);
+          q[4 * r + 3] = __uint_as_float(w[r].w);
+        }
+      } else {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          q[r * 8 + 2 * h] = Elem<T>::lo(parts[h]);
-          q[r * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t parts[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            q[r * 8 + 2 * h] = Elem<T>::lo(parts[h]);
+            q[r * 8 + 2 * h + 1] = Elem<T>::hi(parts[h]);
+          }
         }
       }
     } else if (active) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) q[k] = (k < nv) ? Elem<T>::to(row_ptr[c + k]) : 0.0f;
+      for (int k = 0; k < 32; ++k) {
+        if constexpr (kF32)
+          q[k] = (k < nv) ? row_ptr[c + k] : 0.0f;
+        else
+          q[k] = (k < nv) ? Elem<T>::to(row_ptr[c + k]) : 0.0f;
+      }
     } else {
 #pragma unroll
       for (int k = 0; k < 32; ++k) q[k] = 0.0f;
@@ -253,6 +306,47 @@ __device__ __forceinline__ void emit_dlogits(float (&d)[32], const CUtensorMap* 
   if (bias_sums) ctl->red[quarter][ch][lane] = transpose_reduce32(d, lane);
 }
 
+// The same for D stored as its three bf16 parts (fp32 operands split into
+// bf16 parts): hi = bf16(d), mid = bf16(d - hi), lo = d - hi - mid (exact), each
+// staged in turn through the warp's buffer and stored to dmap (hi) and
+// dmap_x[0], dmap_x[1] (mid, lo).
+__device__ __forceinline__ void emit_dlogits_split(float (&d)[32], const CUtensorMap* dmap,
+                                                   const CUtensorMap* dmap_x, int64_t row0,
+                                                   int64_t buf_rows, int cb, bool bias_sums,
+                                                   int ch, int quarter, int part, int lane,
+                                                   GemmCtl* ctl) {
+  uint8_t* buf = ctl->out_stage + (part * 4 + quarter) * kDlogitsStageBytes;
+  float r[32];  // what the parts stored so far leave of d
+#pragma unroll
+  for (int k = 0; k < 32; ++k) r[k] = d[k];
+#pragma unroll 1
+  for (int q = 0; q < 3; ++q) {
+    if (lane == 0) tma_store_wait_read();  // the previous box has left the buffer
+    __syncwarp();
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const __nv_bfloat16 a = __float2bfloat16_rn(r[2 * k]);
+      const __nv_bfloat16 b = __float2bfloat16_rn(r[2 * k + 1]);
+      r[2 * k] -= __bfloat162float(a);
+      r[2 * k + 1] -= __bfloat162float(b);
+      w[k] = static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) dst[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < buf_rows) {
+      tma_store_2d(q == 0 ? dmap : dmap_x + (q - 1), smem_addr(buf), cb,
+                   static_cast<int32_t>(row0));
+      tma_store_commit();
+    }
+  }
+  if (bias_sums) ctl->red[quarter][ch][lane] = transpose_reduce32(d, lane);
+}
+
 // After the chunks of a tile: grad_bias partials of the tile's columns, the
 // sum of the four lane quarters' column sums in a fixed order. With W
 // epilogue warps, warp (quarter, part) flushes chunks e * 8/W .. +8/W - 1,
@@ -286,7 +380,10 @@ __device__ __forceinline__ void flush_bias_sums(float* gb_partial, int64_t gb_ld
 // W = 8: two warps per TMEM lane quarter, each folding one 128-column half
 // of the tile into its own statistics (partials per 128 columns; for short
 // contractions, where the epilogue would outlast the MMAs).
-template <typename T, bool METRICS = true, int W = 4>
+// TB: the bias type (T, or float when the operands are fp32 split into bf16
+// parts). A launch may cover one vocabulary chunk from column p.c0 (a
+// multiple of 256): tiles, partial slots and columns are offset by it.
+template <typename T, bool METRICS = true, int W = 4, typename TB = T>
 struct EpiFwdStats {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
@@ -301,8 +398,9 @@ struct EpiFwdStats {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
     const int64_t t = row_ok ? __ldg(p.targets + row) : INT64_MIN;
-    const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
-    const int64_t slot = static_cast<int64_t>(n_tile) * (W / 4) + part;  // partials index
+    const int64_t tile = p.c0 / kBN + n_tile;  // vocabulary tile of the whole row
+    const int64_t col0 = tile * kBN;
+    const int64_t slot = tile * (W / 4) + part;  // partials index
     RowStats st;
     st.init();
     float zt = 0.0f;
@@ -315,7 +413,7 @@ struct EpiFwdStats {
       const int nv = static_cast<int>(p.v - cb < 32 ? p.v - cb : 32);
       float z[32], b[32];
       acc.load(ch, z);
-      load_bias32<T>(p.bias, cb, nv, b);
+      load_bias32<TB>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
         fold_chunk<true, METRICS, METRICS>(st, z, nv, static_cast<int>(cb));
@@ -347,7 +445,9 @@ struct EpiFwdStats {
 // ------------------------------------------------------------------ dlogits
 // W = 8: two warps per TMEM lane quarter, one per column half of the tile
 // (for short contractions, where the epilogue would outlast the MMAs).
-template <typename T, int W = 4>
+// TB: the bias type (T, or float for fp32 operands split into bf16 parts);
+// DS: store D as its three bf16 parts (p.d_map, p.d_map_x).
+template <typename T, int W = 4, typename TB = T, bool DS = false>
 struct EpiDlogits {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
@@ -383,7 +483,7 @@ struct EpiDlogits {
       const int nv = p.width - cb < 32 ? p.width - cb : 32;
       float z[32], b[32];
       acc.load(ch, z);
-      load_bias32<T>(p.bias, p.c0 + cb, nv, b);
+      load_bias32<TB>(p.bias, p.c0 + cb, nv, b);
       float d[32];
       p.xf.apply32(z, b);
       if (!p.xf.has_cap) {
@@ -420,8 +520,13 @@ struct EpiDlogits {
 #pragma unroll
         for (int k = 0; k < 32; ++k) d[k] = d[k] * gs * p.xf.dz_du(z[k]);
       }
-      emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows,
-                      cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
+      if constexpr (DS)
+        emit_dlogits_split(d, &p.d_map, p.d_map_x,
+                           static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows, cb,
+                           bias_sums, ch, quarter, part, lane, ctl);
+      else
+        emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32,
+                        p.n_rows, cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
     }
     if (bias_sums)
       flush_bias_sums<W>(p.gb_partial, p.gb_ld, m_tile, p.c0, col0, p.width, quarter, part,
@@ -432,7 +537,9 @@ struct EpiDlogits {
 // ------------------------------------------------------------ KL forward
 // W = 8: two warps per TMEM lane quarter, one per 128-column half, each with
 // its own statistics (partials per 128 columns), as in EpiFwdStats.
-template <typename T, int W = 4>
+// TB: the type of the bias and of the teacher probabilities (T, or float for
+// fp32 operands split into bf16 parts); p.c0 as in EpiFwdStats.
+template <typename T, int W = 4, typename TB = T>
 struct EpiFwdKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
@@ -447,15 +554,16 @@ struct EpiFwdKL {
     const int64_t row = static_cast<int64_t>(m_tile) * kBM + row_in_tile;
     const bool row_ok = row < n_eff;
     const int64_t orig = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
-    const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v;
-    const int64_t col0 = static_cast<int64_t>(n_tile) * kBN;
-    const int64_t slot = static_cast<int64_t>(n_tile) * (W / 4) + part;  // partials index
+    const TB* qrow = static_cast<const TB*>(p.q) + (row_ok ? orig : 0) * p.v;
+    const int64_t tile = p.c0 / kBN + n_tile;  // vocabulary tile of the whole row
+    const int64_t col0 = tile * kBN;
+    const int64_t slot = tile * (W / 4) + part;  // partials index
     RowStats st;
     st.init();
     float a_sum = 0.0f;  // sum q (log max(q, eps) - z)
     float q_sum = 0.0f;  // sum q
     const bool vec = p.q_vec != 0;
-    RowChunk32<T> cur, nxt;
+    RowChunk32<TB> cur, nxt;
     const int ch_end = (part + 1) * kChunks;
     const int64_t c_first = col0 + part * kChunks * 32;
     if (c_first < p.v)
@@ -471,7 +579,7 @@ struct EpiFwdKL {
         nxt.issue(qrow, cn, p.v - cn < 32 ? static_cast<int>(p.v - cn) : 32, vec, row_ok);
       float z[32], b[32];
       acc.load(ch, z);
-      load_bias32<T>(p.bias, cb, nv, b);
+      load_bias32<TB>(p.bias, cb, nv, b);
       p.xf.apply32(z, b);
       if (nv == 32) {
         fold_chunk<true, false, false>(st, z, nv, static_cast<int>(cb));
@@ -500,7 +608,8 @@ struct EpiFwdKL {
 
 // ------------------------------------------------------------ KL dlogits
 // D = g (p * sum_k q_k - q) * dz/dlin, with dz/dlin = 1 / temperature.
-template <typename T, int W = 4>
+// TB: as in EpiFwdKL; DS: D stored as its three bf16 parts (see EpiDlogits).
+template <typename T, int W = 4, typename TB = T, bool DS = false>
 struct EpiDlogitsKL {
   static constexpr uint32_t kABFormat = Elem<T>::kFormat;
   static constexpr int kEpiWarps = W;
@@ -521,12 +630,12 @@ struct EpiDlogitsKL {
     const float lse2 = row_ok ? __ldg(p.lse + row) * kLog2e : 0.0f;
     const float qs = row_ok ? __ldg(p.qsum + row) : 0.0f;
     const int64_t orig = (row_ok && p.row_map != nullptr) ? p.row_map[row] : row;
-    const T* qrow = static_cast<const T*>(p.q) + (row_ok ? orig : 0) * p.v + p.c0;
+    const TB* qrow = static_cast<const TB*>(p.q) + (row_ok ? orig : 0) * p.v + p.c0;
     const int col0 = n_tile * kBN;
     const float dscale = p.dscale != nullptr ? *p.dscale : 1.0f;
     const bool bias_sums = p.gb_partial != nullptr && static_cast<int64_t>(m_tile) * kBM < n_eff;
     const bool vec = p.q_vec != 0;
-    RowChunk32<T> cur, nxt;
+    RowChunk32<TB> cur, nxt;
     const int ch_end = (part + 1) * kChunks;
     const int c_first = col0 + part * kChunks * 32;
     if (c_first < p.width)
@@ -541,7 +650,7 @@ struct EpiDlogitsKL {
         nxt.issue(qrow, cn, p.width - cn < 32 ? p.width - cn : 32, vec, row_ok);
       float z[32], b[32], q[32];
       acc.load(ch, z);
-      load_bias32<T>(p.bias, p.c0 + cb, nv, b);
+      load_bias32<TB>(p.bias, p.c0 + cb, nv, b);
       cur.get(qrow, cb, nv, row_ok, q);
       float d[32];
       p.xf.apply32(z, b);
@@ -562,8 +671,13 @@ struct EpiDlogitsKL {
           f2_unpack(f2_mul(pq, g2), d[k], d[k + 1]);
         }
       }
-      emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows,
-                      cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
+      if constexpr (DS)
+        emit_dlogits_split(d, &p.d_map, p.d_map_x,
+                           static_cast<int64_t>(m_tile) * kBM + quarter * 32, p.n_rows, cb,
+                           bias_sums, ch, quarter, part, lane, ctl);
+      else
+        emit_dlogits<T>(d, &p.d_map, static_cast<int64_t>(m_tile) * kBM + quarter * 32,
+                        p.n_rows, cb, dscale, bias_sums, ch, quarter, part, lane, ctl);
       cur = nxt;
     }
     if (bias_sums)
@@ -592,18 +706,7 @@ struct EpiStoreRows {
       const int nv = p.cols - cb < 32 ? p.cols - cb : 32;
       const int64_t off = (p.row0 + row) * p.ld + cb;
       if (p.out_f32) {
-        float* dst = static_cast<float*>(p.out) + off;
-        if (nv == 32) {
-          float4* dv = reinterpret_cast<float4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dv[q] = make_float4(z[4 * q] * scale, z[4 * q + 1] * scale, z[4 * q + 2] * scale,
-                                z[4 * q + 3] * scale);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k < nv) dst[k] = z[k] * scale;
-        }
+        store32_f32(static_cast<float*>(p.out) + off, z, nv, scale);
       } else {
         store32<T>(static_cast<T*>(p.out) + off, z, nv, scale);
       }
@@ -669,6 +772,8 @@ struct EpiAccRows {
           for (int k = 0; k < 32; ++k)
             if (k < nv) dst[k] = z[k];
         }
+      } else if (p.out_f32) {
+        store32_f32(static_cast<float*>(p.out) + out_off, z, nv, 1.0f);
       } else {
         store32<T>(static_cast<T*>(p.out) + out_off, z, nv, 1.0f);
       }
@@ -788,6 +893,25 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   return launch_gemm_args<CG>(a, sms, stream);
 }
 
+// One GEMM over split operands: parts[0] of A and B in the segment's own
+// maps, parts 1 and 2 (mid, lo) in the extra maps; g.passes / pass_a /
+// pass_b say which part pairs the contraction runs over.
+template <int CG, bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm_split(const CUtensorMap (&ta)[3], const CUtensorMap (&tb)[3],
+                              const GemmGeom& g, const typename Epi::Params& ep, int sms,
+                              cudaStream_t stream) {
+  GemmArgs<Seg<A_MN, B_MN, Epi, true>, NoSeg> a{};
+  a.a0 = ta[0];
+  a.b0 = tb[0];
+  a.x0.a[0] = ta[1];
+  a.x0.a[1] = ta[2];
+  a.x0.b[0] = tb[1];
+  a.x0.b[1] = tb[2];
+  a.g0 = g;
+  a.ep0 = ep;
+  return launch_gemm_args<CG>(a, sms, stream);
+}
+
 // grad_hidden (D K-major times W MN-major, accumulated rows) and grad_weight
 // (D^T times hidden, both MN-major, stored rows) of one vocabulary chunk in
 // one dynamically scheduled launch; the segment with the longer contraction
@@ -850,6 +974,25 @@ cudaError_t launch_tc_fwd_stats(int type, const CUtensorMap& tm_hidden_k,
                    tm_hidden_k, tm_weight_k, g, p, sms, s);
 }
 
+cudaError_t launch_tc_fwd_stats_split(const CUtensorMap (&tm_hidden_k)[3],
+                                      const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                      const FwdStatsParams& p, int epi_warps, int sms,
+                                      cudaStream_t s) {
+  using B = __nv_bfloat16;
+  if (epi_warps == 8) {
+    if (p.metrics)
+      return launch_gemm_split<kPairCG, false, false, EpiFwdStats<B, true, 8, float>>(
+          tm_hidden_k, tm_weight_k, g, p, sms, s);
+    return launch_gemm_split<kPairCG, false, false, EpiFwdStats<B, false, 8, float>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  }
+  if (p.metrics)
+    return launch_gemm_split<kPairCG, false, false, EpiFwdStats<B, true, 4, float>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  return launch_gemm_split<kPairCG, false, false, EpiFwdStats<B, false, 4, float>>(
+      tm_hidden_k, tm_weight_k, g, p, sms, s);
+}
+
 cudaError_t launch_tc_dlogits(int type, const CUtensorMap& tm_hidden_k,
                               const CUtensorMap& tm_weight_k, const GemmGeom& g,
                               const DlogitsParams& p, int epi_warps, int sms, cudaStream_t s) {
@@ -906,6 +1049,88 @@ cudaError_t launch_tc_dlogits_kl(int type, const CUtensorMap& tm_hidden_k,
 cudaError_t launch_tc_grads(int type, const GradsLaunch& l, int sms, cudaStream_t s) {
   if (type == kTcF16) return launch_grads_typed<__half>(l, sms, s);
   return launch_grads_typed<__nv_bfloat16>(l, sms, s);
+}
+
+cudaError_t launch_tc_dlogits_split(const CUtensorMap (&tm_hidden_k)[3],
+                                    const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                    const DlogitsParams& p, int epi_warps, int sms,
+                                    cudaStream_t s) {
+  using B = __nv_bfloat16;
+  if (epi_warps == 8)
+    return launch_gemm_split<kPairCG, false, false, EpiDlogits<B, 8, float, true>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  return launch_gemm_split<kPairCG, false, false, EpiDlogits<B, 4, float, true>>(
+      tm_hidden_k, tm_weight_k, g, p, sms, s);
+}
+
+cudaError_t launch_tc_fwd_kl_split(const CUtensorMap (&tm_hidden_k)[3],
+                                   const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                   const FwdKLParams& p, int epi_warps, int sms, cudaStream_t s) {
+  using B = __nv_bfloat16;
+  if (epi_warps == 8)
+    return launch_gemm_split<kPairCG, false, false, EpiFwdKL<B, 8, float>>(tm_hidden_k,
+                                                                           tm_weight_k, g, p,
+                                                                           sms, s);
+  return launch_gemm_split<kPairCG, false, false, EpiFwdKL<B, 4, float>>(tm_hidden_k,
+                                                                         tm_weight_k, g, p,
+                                                                         sms, s);
+}
+
+cudaError_t launch_tc_dlogits_kl_split(const CUtensorMap (&tm_hidden_k)[3],
+                                       const CUtensorMap (&tm_weight_k)[3], const GemmGeom& g,
+                                       const DlogitsKLParams& p, int epi_warps, int sms,
+                                       cudaStream_t s) {
+  using B = __nv_bfloat16;
+  if (epi_warps == 8)
+    return launch_gemm_split<kPairCG, false, false, EpiDlogitsKL<B, 8, float, true>>(
+        tm_hidden_k, tm_weight_k, g, p, sms, s);
+  return launch_gemm_split<kPairCG, false, false, EpiDlogitsKL<B, 4, float, true>>(
+      tm_hidden_k, tm_weight_k, g, p, sms, s);
+}
+
+// The fused gradient launch over split operands (as launch_grads_typed).
+cudaError_t launch_tc_grads_split(const GradsSplitLaunch& l, int sms, cudaStream_t s) {
+  using B = __nv_bfloat16;
+  using GH = Seg<false, true, EpiAccRows<B>, true>;
+  using GW = Seg<true, true, EpiStoreRows<B>, true>;
+  auto fill_gh = [&](auto& a, auto& maps_a, auto& maps_b, CUtensorMap& ta, CUtensorMap& tb) {
+    ta = l.d_k[0];
+    tb = l.weight_mn[0];
+    maps_a[0] = l.d_k[1];
+    maps_a[1] = l.d_k[2];
+    maps_b[0] = l.weight_mn[1];
+    maps_b[1] = l.weight_mn[2];
+    (void)a;
+  };
+  auto fill_gw = [&](auto& a, auto& maps_a, auto& maps_b, CUtensorMap& ta, CUtensorMap& tb) {
+    ta = l.d_mn[0];
+    tb = l.hidden_mn[0];
+    maps_a[0] = l.d_mn[1];
+    maps_a[1] = l.d_mn[2];
+    maps_b[0] = l.hidden_mn[1];
+    maps_b[1] = l.hidden_mn[2];
+    (void)a;
+  };
+  if (l.gh_first) {
+    GemmArgs<GH, GW> a{};
+    fill_gh(a, a.x0.a, a.x0.b, a.a0, a.b0);
+    fill_gw(a, a.x1.a, a.x1.b, a.a1, a.b1);
+    a.g0 = l.g_gh;
+    a.ep0 = l.ap;
+    a.g1 = l.g_gw;
+    a.ep1 = l.sp;
+    a.g0.sched = l.sched;
+    return launch_gemm_args<kPairCG>(a, sms, s);
+  }
+  GemmArgs<GW, GH> a{};
+  fill_gw(a, a.x0.a, a.x0.b, a.a0, a.b0);
+  fill_gh(a, a.x1.a, a.x1.b, a.a1, a.b1);
+  a.g0 = l.g_gw;
+  a.ep0 = l.sp;
+  a.g1 = l.g_gh;
+  a.ep1 = l.ap;
+  a.g0.sched = l.sched;
+  return launch_gemm_args<kPairCG>(a, sms, s);
 }
 
 }  // namespace flce

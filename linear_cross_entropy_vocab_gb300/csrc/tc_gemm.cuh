@@ -128,6 +128,13 @@ struct GemmGeom {
   // kernels before its first load; kPdlWaitEpilogue: the epilogue threads
   // wait before their first tile.
   int pdl;
+  // Split operands (segments with Seg::kSplit: fp32 inputs as three bf16
+  // parts, x = hi + mid + lo): every tile runs its contraction `passes`
+  // times over the same K range, pass p reading part pass_a[p] of A and part
+  // pass_b[p] of B (0: the segment's own map; 1, 2: its two extra maps), all
+  // into the same accumulator.
+  int passes;
+  uint8_t pass_a[6], pass_b[6];
 };
 constexpr int kPdlWaitLoads = 1;
 constexpr int kPdlWaitEpilogue = 2;
@@ -390,12 +397,14 @@ __device__ __forceinline__ void st_shared_cluster(uint32_t addr, int v) {
 // warps that run tile() may use named barrier kEpiBar (32 * kEpiWarps
 // threads).
 
-// One GEMM of a launch: operand majorness and epilogue.
-template <bool A_MN_, bool B_MN_, class Epi_>
+// One GEMM of a launch: operand majorness, epilogue, and whether its
+// operands are split into parts (GemmGeom::passes).
+template <bool A_MN_, bool B_MN_, class Epi_, bool SPLIT_ = false>
 struct Seg {
   static constexpr bool kPresent = true;
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
+  static constexpr bool kSplit = SPLIT_;
   using Epi = Epi_;
 };
 
@@ -409,18 +418,34 @@ struct NoSeg {
   static constexpr bool kPresent = false;
   static constexpr bool A_MN = false;
   static constexpr bool B_MN = false;
+  static constexpr bool kSplit = false;
   using Epi = NoEpi;
+};
+
+// The extra parts (mid, lo) of a split segment's operands; nothing otherwise.
+template <bool SPLIT>
+struct SplitMaps {};
+template <>
+struct SplitMaps<true> {
+  CUtensorMap a[2], b[2];
 };
 
 // Kernel arguments: tensor maps, geometry and epilogue parameters of both
 // segments (the second ones unused for a one-GEMM launch). Tile indices
 // [0, tiles of segment 0) are segment 0's, the rest segment 1's.
+__device__ __forceinline__ const CUtensorMap* split_a(const SplitMaps<true>& x) { return x.a; }
+__device__ __forceinline__ const CUtensorMap* split_b(const SplitMaps<true>& x) { return x.b; }
+__device__ __forceinline__ const CUtensorMap* split_a(const SplitMaps<false>&) { return nullptr; }
+__device__ __forceinline__ const CUtensorMap* split_b(const SplitMaps<false>&) { return nullptr; }
+
 template <class S0, class S1>
 struct GemmArgs {
   CUtensorMap a0, b0, a1, b1;
   GemmGeom g0, g1;
   typename S0::Epi::Params ep0;
   typename S1::Epi::Params ep1;
+  SplitMaps<S0::kSplit> x0;
+  SplitMaps<S1::kSplit> x1;
 };
 
 template <int CG, class S0, class S1>
@@ -561,23 +586,36 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
       uint32_t last_phase = 0;  // bit s: phase of the last load into stage s
       bool ok = true;
       // loads of one tile of segment S (tile index ul within the segment)
+      // xa, xb: the extra parts of a split segment's operands (else unused);
+      // a split segment's tile runs g.passes passes of k_iters stages each
       auto produce = [&](auto seg, const CUtensorMap* ta, const CUtensorMap* tb,
-                         const GemmGeom& g, int m_tiles, int k_iters, int ul) -> bool {
+                         const CUtensorMap* xa, const CUtensorMap* xb, const GemmGeom& g,
+                         int m_tiles, int k_iters, int ul) -> bool {
         using S = decltype(seg);
         int m, n;
         tile_coords(g, m_tiles, ul, m, n);
-        for (int k = 0; k < k_iters; ++k) {
+        const int k_total = S::kSplit ? g.passes * k_iters : k_iters;
+        for (int kt = 0; kt < k_total; ++kt) {
+          int k = kt;
+          const CUtensorMap* ma = ta;
+          const CUtensorMap* mb = tb;
+          if constexpr (S::kSplit) {
+            const int pass = kt / k_iters;
+            k = kt - pass * k_iters;
+            if (g.pass_a[pass] != 0) ma = xa + (g.pass_a[pass] - 1);
+            if (g.pass_b[pass] != 0) mb = xb + (g.pass_b[pass] - 1);
+          }
           if (!wait_bar<CG>(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, err_word))
             return false;
           const uint32_t full_local = smem_addr(&ctl->full[stage]);
           uint32_t full = full_local;
           if constexpr (CG == 2) full = map_to_rank(full_local, 0);
           if (leader) mbar_arrive_expect_tx(full_local, CG * Cfg::kStageBytes);
-          load_operand<CG, S::A_MN, kBM>(stage_a(stage), ta, full,
+          load_operand<CG, S::A_MN, kBM>(stage_a(stage), ma, full,
                                          g.a_mn0 + m * Cfg::kTileRows + static_cast<int>(rank) * kBM,
                                          g.a_k0 + k * kBK);
           load_operand<CG, S::B_MN, Cfg::kBNLoad>(
-              stage_b(stage), tb, full,
+              stage_b(stage), mb, full,
               g.b_mn0 + n * kBN + static_cast<int>(rank) * Cfg::kBNLoad, g.b_k0 + k * kBK);
           armed |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -630,9 +668,11 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
           if (u < 0) break;
         }
         if (!S1::kPresent || u < total0)
-          ok = produce(S0{}, &args.a0, &args.b0, args.g0, m_tiles0, k_iters0, u);
+          ok = produce(S0{}, &args.a0, &args.b0, split_a(args.x0), split_b(args.x0), args.g0,
+                       m_tiles0, k_iters0, u);
         else
-          ok = produce(S1{}, &args.a1, &args.b1, args.g1, m_tiles1, k_iters1, u - total0);
+          ok = produce(S1{}, &args.a1, &args.b1, split_a(args.x1), split_b(args.x1), args.g1,
+                       m_tiles1, k_iters1, u - total0);
       }
       if (!ok && leader) {
         // let every copy already issued land before the CTAs exit
@@ -699,9 +739,9 @@ __global__ void __launch_bounds__(gemm_threads<typename S0::Epi>(), 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
         if (!S1::kPresent || u < total0)
-          ok = mma(S0{}, k_iters0, d_tmem);
+          ok = mma(S0{}, S0::kSplit ? args.g0.passes * k_iters0 : k_iters0, d_tmem);
         else
-          ok = mma(S1{}, k_iters1, d_tmem);
+          ok = mma(S1{}, S1::kSplit ? args.g1.passes * k_iters1 : k_iters1, d_tmem);
         if (!ok) break;
         if constexpr (CG == 1)
           umma_commit(smem_addr(&ctl->acc_full[buf]));
