@@ -246,10 +246,10 @@ bool is_tc(const flce_problem* p) { return p->dtype == FLCE_BF16 || p->dtype == 
 
 int tc_type(const flce_problem* p) { return p->dtype == FLCE_F16 ? flce::kTcF16 : flce::kTcBF16; }
 
-// fp32 inputs whose rows are a multiple of 16 bytes run the cross-entropy
-// forward on the tensor cores with split operands: each value as three bf16
-// parts (hi + mid + lo, exact), each product as the six part products whose
-// dropped companions are below 2^-24 of it, accumulated in fp32.
+// fp32 inputs whose rows are a multiple of 16 bytes run on the tensor cores
+// with split operands: each value as three bf16 parts (hi + mid + lo, exact),
+// each product as six part products (the three dropped ones, mid.lo, lo.mid
+// and lo.lo, come to about 2^-23 of it), accumulated in fp32.
 constexpr bool kSplitF32 = true;
 int64_t split_chunk(const flce_problem* p, bool caller_chunk = true);
 // Split operands also need their bf16 parts in the workspace: hidden's, one
