@@ -84,6 +84,21 @@ def test_roofline_fused_gradient_role_counts_both_contractions():
     assert abs(r["achieved"] - 4.0 * n * h * v / 5 / 2.0e-3 / 1e12) < 0.1
 
 
+def test_roofline_split_roles_use_a_sixth_of_the_bf16_peak():
+    """fp32 operands split into three bf16 parts take six bf16 products per
+    fp32 product: the split roles count the algorithmic fp32 flops against the
+    bf16 peak / 6."""
+    b = _bench()
+    n, h, v, steps = 8192, 4096, 128256, 3
+    r = b.roofline_entry("bwd_grads_split", 18 * steps, 18 * steps * 3.66, steps, n, h, v,
+                         380.0, PEAKS, "measured", 152)
+    assert r["bound"] == "tensor"
+    assert r["peak"] == round(1856.7 / 6, 1)
+    assert "/ 6" in r["peak_kind"]
+    assert r["flops_per_launch"] == 4.0 * n * h * v / 18
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+
+
 def test_roofline_fp32_roles_use_the_fma_peak():
     """The fp32 (FFMA) roles are ALU-bound: the peak is SMs x 128 lanes x 2 flops
     x the maximum SM clock, whatever the length of the timed region."""
