@@ -40,7 +40,11 @@
  *     FLCE_F32 needs 4-byte alignment. Violations return FLCE_ERR_UNSUPPORTED
  *     before any launch.
  *   - Dtypes: FLCE_BF16 and FLCE_F16 run on the tensor cores (bf16 or fp16
- *     products, fp32 accumulation); FLCE_F32 runs fp32 FFMA kernels.
+ *     products, fp32 accumulation). FLCE_F32 runs on the tensor cores too,
+ *     each operand split into three bf16 parts that sum to it exactly and each
+ *     product formed from six part products (within about 2^-23 of it), when
+ *     H % 8 == 0 and the parts' workspace stays under 40 % of one fp32 N x V
+ *     matrix; otherwise on fp32 FFMA kernels. Both meet the same fp32 bars.
  *   - Argument errors are detected on the host, before any launch, and
  *     return a non-OK status; flce_last_error() then describes the problem.
  *     A failed launch returns FLCE_ERR_CUDA.
@@ -201,9 +205,11 @@ flce_status flce_forward_noalloc(const flce_problem* p, const void* hidden,
 
 /* Bytes of device workspace flce_backward() needs for `p` (0 if invalid):
  * the dlogits buffer of one vocabulary chunk (N x chunk, in the input type for
- * FLCE_BF16 / FLCE_F16 and fp32 for FLCE_F32), an fp32 [N,H] grad_hidden
- * accumulator when there is more than one chunk on the tensor-core path, and
- * fp32 grad_bias partial sums when has_bias. */
+ * FLCE_BF16 / FLCE_F16; fp32 for FLCE_F32 on FFMA kernels, or three bf16 parts
+ * on the tensor cores, which also hold the bf16 parts of hidden and of the
+ * chunk's weight rows), an fp32 [N,H] grad_hidden accumulator when there is
+ * more than one chunk on the tensor-core path, and fp32 grad_bias partial sums
+ * when has_bias. */
 size_t flce_backward_workspace_size(const flce_problem* p);
 
 /* Backward pass: all three gradients. Cite: §Algorithm (backward: recompute
