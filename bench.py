@@ -547,7 +547,10 @@ def bench_ours(args, rank, world, dev):
             "of_burst": round(achieved_step / peaks["bf16_tflops"], 4),
             "of_sustained": round(achieved_step / peaks["bf16_tflops_sustained"], 4),
             "of_burst_valid_rows": round(achieved_step * n_valid / n / peaks["bf16_tflops"], 4),
-            "flops_per_step": flops_step, "peaks": peak_src},
+            "flops_per_step": flops_step, "peaks": peak_src,
+            # fp32 operands split into bf16 parts: six bf16 products per fp32 product
+            **({"of_split_burst": round(achieved_step / (peaks["bf16_tflops"] / SPLIT_PASSES), 4)}
+               if any(r in SPLIT_ROLES for r in roles) else {})},
         "roofline": roofline,
         "kernels": kernels,
         "kernels_how": kernels_how,
