@@ -206,3 +206,32 @@ def test_kl_validation_and_workspace(lib):
     assert _kl_bwd(ok, grad_out=None) == abi.FLCE_ERR_INVALID_ARG
     assert _kl_bwd(ok, workspace_bytes=0) == abi.FLCE_ERR_WORKSPACE
     assert lib.flce_kl_forward(None, *([None] * 12), 0, None) == abi.FLCE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "mid_bf16", "llama3_head_bf16", "softcap_bf16",
+                                  "long_bf16"])
+@pytest.mark.parametrize("as_f32", [False, True])
+def test_planned_peak_below_logits(lib, name, as_f32):
+    """The host plan behind the no-N x V guarantee: the larger of the two
+    workspaces plus the gradients a step returns (grad_weight [V, H],
+    grad_hidden [N, H], grad_bias [V]) stay under one N x V logit matrix in
+    the input type, for every listed workload in its own type and in fp32
+    (where the split path adds the operands' bf16 parts and D's three parts).
+    The GPU test of peak allocation measures the same bound on the device;
+    this pins the sizing on the host, so that a larger default chunk or a
+    new workspace region that would break it fails without a GPU."""
+    from linear_cross_entropy_vocab_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[name]
+    dt = abi.FLCE_F32 if (as_f32 or w.dtype == "f32") else abi.FLCE_BF16
+    el = 4 if dt == abi.FLCE_F32 else 2
+    has_bias = w.bias_var is not None
+    p = abi.make_problem(w.n, w.h, w.v, dt, has_bias, skip_ignored=True)
+    ws = max(abi.flce_forward_workspace_size(p), abi.flce_backward_workspace_size(p))
+    k = abi.make_kl_problem(w.n, w.h, w.v, dt, False, skip_ignored=True)
+    wk = max(abi.flce_kl_forward_workspace_size(k), abi.flce_kl_backward_workspace_size(k))
+    assert ws > 0 and wk > 0
+    grads = (w.v * w.h + w.n * w.h) * el
+    logits = w.n * w.v * el
+    assert ws + grads + (w.v * el if has_bias else 0) < logits, (ws, grads, logits)
+    assert wk + grads < logits, (wk, grads, logits)
